@@ -1,0 +1,192 @@
+"""Float64 CPU oracle for the Kimi Delta Attention core recurrence (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline / reference leg may import this module; the library under
+``linear_attention_serving_k1_gb300`` never does.  It shares no code with the
+CUDA path.  The arithmetic lives in ``kda_oracle.c`` (plain C, float64,
+OpenMP over sequence x head); this file only compiles it with gcc and
+marshals numpy arrays.
+
+Sources: the page "Kimi K3 reconstructs long-context inference efficiency
+through KDA, cross-depth attention, and latent expert routing", sections
+"Methodology notes" (DeltaNet and Delta Rule; Kimi Delta Attention; FlashKDA)
+and "Key data" (decode cost); the zsxq post on SemiAnalysis' Kimi K3 analysis,
+sections "一、Kimi Delta Attention（KDA）" and "五、KV缓存效率与服务性能".
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py
+(closed forms, invariants, special cases and an independent chunked
+formulation); tests/test_oracle_mutants.py plants mistakes in a copy of the C
+source and checks that the pins catch each one.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle with gcc into a shared object (rebuilt if stale)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    lib.oracle_prefill.restype = ctypes.c_int
+    lib.oracle_prefill.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64p, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, _dp, _dp, ctypes.c_int, _dp,
+                                   ctypes.c_int64]
+    lib.oracle_prefill_chunked.restype = ctypes.c_int
+    lib.oracle_prefill_chunked.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64p, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           _dp, _dp, ctypes.c_int, _dp, ctypes.c_int64]
+    lib.oracle_decode.restype = None
+    lib.oracle_decode.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int]
+    lib.oracle_gdn_prefill.restype = None
+    lib.oracle_gdn_prefill.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64p, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp]
+    lib.oracle_ckpt_count.restype = ctypes.c_int64
+    lib.oracle_ckpt_count.argtypes = [_i64p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (compiling if needed) the oracle library.  ``path`` loads another build."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(compile_oracle()))
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor -> numpy without importing torch here
+        x = x.detach().cpu()
+        if str(x.dtype) in ("torch.bfloat16", "torch.float16"):
+            x = x.float()
+        x = x.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def _cu(cu_seqlens, T):
+    if cu_seqlens is None:
+        return np.array([0, T], dtype=np.int64)
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+
+
+def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, ckpt_stride=0, lib=None,
+            chunk=None):
+    """Token-by-token (or, with ``chunk``, chunked) float64 prefill.
+
+    q, k, g: [T, H, Dk]; v: [T, H, Dv]; beta: [T, H]; init_state: [N, H, Dk, Dv]
+    or None (zeros); cu_seqlens: [N + 1] or None (one sequence of length T).
+    Returns (out [T, H, Dv], final_state [N, H, Dk, Dv], ckpts [n_ckpt, H, Dk, Dv]).
+    """
+    lib = lib or load()
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    T, H, Dk = q.shape
+    Dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    s0 = _f64(init_state)
+    out = np.zeros((T, H, Dv), np.float64)
+    fin = np.zeros((N, H, Dk, Dv), np.float64)
+    nck = int(lib.oracle_ckpt_count(cu.ctypes.data_as(_i64p), N, int(ckpt_stride)))
+    ck = np.zeros((max(nck, 1), H, Dk, Dv), np.float64)
+    if chunk is None:
+        rc = lib.oracle_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0),
+                                cu.ctypes.data_as(_i64p), N, H, Dk, Dv, _ptr(out), _ptr(fin),
+                                int(ckpt_stride), _ptr(ck), nck)
+    else:
+        rc = lib.oracle_prefill_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0),
+                                        cu.ctypes.data_as(_i64p), N, H, Dk, Dv, int(chunk),
+                                        _ptr(out), _ptr(fin), int(ckpt_stride), _ptr(ck), nck)
+    if rc != 0:
+        raise ValueError(f"oracle prefill failed with code {rc}")
+    return out, fin, ck[:nck]
+
+
+def prefill_heads(q, k, v, g, beta, init_state=None, cu_seqlens=None, ckpt_stride=0, heads=None):
+    """Prefill restricted to a subset of heads (heads are independent chains).
+
+    Returns the same triple as ``prefill`` with the head axis reduced to ``heads``.
+    """
+    if heads is None:
+        return prefill(q, k, v, g, beta, init_state, cu_seqlens, ckpt_stride)
+    idx = list(heads)
+
+    def sel(x, axis):
+        if x is None:
+            return None
+        x = _f64(x)
+        return np.ascontiguousarray(np.take(x, idx, axis=axis))
+
+    return prefill(sel(q, 1), sel(k, 1), sel(v, 1), sel(g, 1), sel(beta, 1),
+                   sel(init_state, 1), cu_seqlens, ckpt_stride)
+
+
+def decode(q, k, v, g, beta, state, lib=None):
+    """One decode step.  q, k, g: [N, H, Dk]; v: [N, H, Dv]; beta: [N, H];
+    state: [N, H, Dk, Dv].  Returns (out [N, H, Dv], new_state) without
+    modifying the argument."""
+    lib = lib or load()
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    N, H, Dk = q.shape
+    Dv = v.shape[2]
+    st = np.array(_f64(state), dtype=np.float64, copy=True)
+    out = np.zeros((N, H, Dv), np.float64)
+    lib.oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(st), _ptr(out),
+                      N, H, Dk, Dv)
+    return out, st
+
+
+def gdn_prefill(q, k, v, a, beta, init_state=None, cu_seqlens=None, lib=None):
+    """Scalar-gate Gated DeltaNet prefill; a: [T, H] log-decay."""
+    lib = lib or load()
+    q, k, v, a, beta = (_f64(x) for x in (q, k, v, a, beta))
+    T, H, Dk = q.shape
+    Dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    s0 = _f64(init_state)
+    out = np.zeros((T, H, Dv), np.float64)
+    fin = np.zeros((N, H, Dk, Dv), np.float64)
+    lib.oracle_gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(beta), _ptr(s0),
+                           cu.ctypes.data_as(_i64p), N, H, Dk, Dv, _ptr(out), _ptr(fin))
+    return out, fin
+
+
+def num_threads(lib=None) -> int:
+    lib = lib or load()
+    return int(lib.oracle_num_threads())
