@@ -1,0 +1,410 @@
+"""Benchmark of the KDA core library on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 2|4|5] [--no-decode] [--no-cpu-baseline]
+
+A step is one chunked prefill (sequence table, K1 preparation, K2 recurrence,
+checkpoint writer) over the chosen prefill workload, default "prefill B1 H32
+T8192 D128 bf16".  Decode (state GB/s) is timed in the same run over the
+decode workload "decode N256 H32 D128 bf16", 64 consecutive steps, and
+reported under "decode".  Inputs are seeded synthetic draws (see
+linear_attention_serving_k1_gb300/workloads.py) made on the device; L2 is
+flushed (a 512 MiB write) before every timed step.
+
+Rank 0 prints one JSON line.  With --impl reference the float64 CPU oracle is
+timed instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_attention_serving_k1_gb300 import kda, workloads  # noqa: E402
+
+METRIC = "KDA chunked-prefill tokens/s and decode state GB/s, % of roofline, 1×GB300"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ accounting
+def prefill_algorithmic_bytes(w) -> int:
+    """Bytes a prefill must move at minimum: q, k, v (dtype), g (fp32), beta
+    (fp32), out (dtype) per token-head, plus the initial and final state and
+    every checkpoint (fp32)."""
+    es = 2 if w.dtype == "bf16" else 4
+    D, H = w.D, w.H
+    per_th = 3 * D * es + D * 4 + 4 + D * es
+    n_ck = kda.num_checkpoints(w.lens, w.ckpt_stride)
+    states = (2 if w.init != "zeros" else 1) * w.num_seqs * H * D * D * 4
+    return w.total_tokens * H * per_th + states + n_ck * H * D * D * 4
+
+
+def prefill_flops(w) -> int:
+    """Triangle-aware FLOPs of the chunked form per token-head: 5CD + 6D^2 + C^2/3."""
+    C, D = 64, w.D
+    return int(w.total_tokens * w.H * (5 * C * D + 6 * D * D + C * C / 3))
+
+
+def decode_cost_per_head(D: int, es: int = 2):
+    """(FLOPs, bytes) of one decode step of one head.  The state part is the
+    KDA pages' estimate, 7*D^2 FLOPs and 8*D^2 bytes (fp32 read + write); the
+    per-token vectors q, k, v, out (dtype) and g (fp32), beta add 4*D*es+4*D+4."""
+    return 7 * D * D, 8 * D * D + 4 * D * es + 4 * D + 4
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(fn, steps, warmup, flush_buf, stream):
+    """Runs fn() warmup + steps times; returns per-step ms (CUDA events on stream)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush_buf.fill_(1.0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+# ------------------------------------------------------------------ our arm
+def bench_prefill(w, steps, warmup, dev, flush_buf, world):
+    inp = workloads.make_prefill(w, device=dev)
+    q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    s0, cu = inp["init_state"], inp["cu_seqlens"]
+    T, H, D, N = w.total_tokens, w.H, w.D, w.num_seqs
+    n_ck = kda.num_checkpoints(w.lens, w.ckpt_stride)
+    desc = kda.make_desc(T, H, D, N, kda.DTYPE_BF16 if w.dtype == "bf16" else kda.DTYPE_FP32, 64,
+                         w.ckpt_stride, n_ck)
+    ws = kda.alloc_workspace(desc, dev)
+    out = torch.empty_like(v)
+    fin = torch.empty(N, H, D, D, dtype=torch.float32, device=dev)
+    ck = torch.empty(max(n_ck, 1), H, D, D, dtype=torch.float32, device=dev) if n_ck else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.prefill(q, k, v, g, beta, s0, cu, num_seqs=N, ckpt_stride=w.ckpt_stride, ckpts=ck,
+                    ckpt_capacity=n_ck, out=out, final_state=fin, workspace=ws, stream=stream)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = time_steps(step, steps, warmup, flush_buf, stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    assert kda.prefill_status(ws) == 0
+
+    # end to end: pinned host inputs -> device, prefill, outputs -> host, every step
+    host_in = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    host_s0 = s0.cpu().pin_memory() if s0 is not None else None
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d += host_s0.numel() * 4 if host_s0 is not None else 0
+    d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * 4
+    dev_in = {n: torch.empty_like(inp[n]) for n in host_in}
+    dev_s0 = torch.empty_like(s0) if s0 is not None else None
+
+    def e2e_step():
+        for n in host_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        if dev_s0 is not None:
+            dev_s0.copy_(host_s0, non_blocking=True)
+        kda.prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_s0, cu,
+                    num_seqs=N, ckpt_stride=w.ckpt_stride, ckpts=ck, ckpt_capacity=n_ck, out=out,
+                    final_state=fin, workspace=ws, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_fin.copy_(fin, non_blocking=True)
+
+    e2e_ms = time_steps(e2e_step, max(2, steps // 2), 1, flush_buf, stream)
+    del dev_in, host_in
+    return ms, e2e_ms, h2d, d2h
+
+
+def bench_decode(steps_total, dev, flush_buf, warmup=3):
+    w = workloads.workload(3)
+    st = workloads.make_decode_state(w, device=dev)
+    xs = [workloads.make_decode_step(w, s, device=dev) for s in range(steps_total)]
+    out = torch.empty(w.N, w.H, w.D, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    for s in range(warmup):
+        x = xs[s % len(xs)]
+        kda.decode(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=out, stream=stream)
+    torch.cuda.synchronize()
+    evs = []
+    for s in range(steps_total):
+        x = xs[s]
+        flush_buf.fill_(1.0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kda.decode(x["q"], x["k"], x["v"], x["g"], x["beta"], st, out=out, stream=stream)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return w, ms
+
+
+def cpu_baseline_prefill(w, budget_s=15.0):
+    """Times the float64 oracle on a bounded sample of the prefill workload:
+    the first tokens of every sequence over a subset of heads, grown until the
+    run takes a few seconds.  Returns the dict of the JSON line."""
+    from oracle import oracle
+    inp = workloads.make_prefill(workloads.custom_prefill(
+        H=w.H, D=w.D, lens=[min(w.lens[0], 4096)], dtype=w.dtype, init=w.init, seed=w.seed))
+    T = inp["q"].shape[0]
+    heads = list(range(min(4, w.H)))
+    tok = 256
+    elapsed = 0.0
+    while True:
+        sl = slice(0, tok)
+        args = [inp[n][sl] for n in ("q", "k", "v", "g", "beta")]
+        t0 = time.perf_counter()
+        oracle.prefill_heads(*args, inp["init_state"], None, 0, heads=heads)
+        elapsed = time.perf_counter() - t0
+        if elapsed > budget_s / 4 or tok >= T:
+            break
+        tok = min(T, tok * 4)
+    token_heads_per_s = tok * len(heads) / elapsed
+    return {"value": token_heads_per_s / w.H, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{tok} tokens x {len(heads)} of {w.H} heads of the prefill workload, float64 "
+                      f"token recurrence, {elapsed:.2f} s; tokens/s = token-heads/s / H"}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    kda.load_library()
+    peaks = load_peaks()
+    w = workloads.workload(args.workload)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    clk.start()
+    ms, e2e_ms, h2d, d2h = bench_prefill(w, args.steps, args.warmup, dev, flush_buf, world)
+    dec = None
+    if not args.no_decode:
+        dec_w, dec_ms = bench_decode(64, dev, flush_buf)
+    clocks = clk.stop()
+
+    total_ms = max_over_ranks(sum(ms), world)
+    ms_per_step = total_ms / len(ms)
+    tokens_per_step = w.total_tokens * world
+    value = tokens_per_step / (ms_per_step / 1e3)
+    e2e_val = tokens_per_step / (max_over_ranks(sum(e2e_ms), world) / len(e2e_ms) / 1e3)
+
+    alg_bytes = prefill_algorithmic_bytes(w)
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    roof = {"kernel": "kda_prefill (sequence table + K1 + K2 launches of one call)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "tensor_tflops": round(prefill_flops(w) / (ms_per_step / 1e3) / 1e12, 2),
+            "peak_source": peaks["source"]}
+    if not args.no_decode:
+        f_h, b_h = decode_cost_per_head(dec_w.D)
+        heads = dec_w.N * dec_w.H
+        dec_ms_med = statistics.median(dec_ms)
+        dec_mean = sum(dec_ms) / len(dec_ms)
+        dec_gbs = b_h * heads / (dec_mean / 1e3) / 1e9
+        dec = {"workload": dec_w.name, "metric": "decode state GB/s", "unit": "GB/s",
+               "value": round(dec_gbs, 1), "us_per_step": round(dec_mean * 1e3, 2),
+               "us_per_step_median": round(dec_ms_med * 1e3, 2), "steps": len(dec_ms),
+               "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                            "algorithmic_bytes_per_launch": b_h * heads}}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": len(ms), "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded, on device)",
+            "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H,
+                       "head_dim": w.D, "chunk": 64, "ckpt_stride": w.ckpt_stride,
+                       "l2": "flushed (512 MiB write) before every timed step; inputs also exceed L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * len(ms),
+            "clocks": clocks,
+            "decode": dec}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from oracle import oracle
+    w = workloads.workload(args.workload)
+    inp = workloads.make_prefill(workloads.custom_prefill(
+        H=w.H, D=w.D, lens=[1024], dtype=w.dtype, init=w.init, seed=w.seed))
+    heads = [0, 1]
+    args_ = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+
+    def step():
+        oracle.prefill_heads(*args_, inp["init_state"], None, 0, heads=heads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms_per_step = el / args.steps * 1e3
+    tok_heads = 1024 * len(heads)
+    value = tok_heads / w.H / (ms_per_step / 1e3)
+    sample = f"1024 tokens x {len(heads)} of {w.H} heads per step, float64 token recurrence; tokens/s = token-heads/s / H"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 4, 5])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

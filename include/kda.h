@@ -1,0 +1,159 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention core library.
+ *
+ * The library computes, per sequence and head, the KDA recurrence that the
+ * page "Kimi K3 reconstructs long-context inference efficiency through KDA,
+ * cross-depth attention, and latent expert routing" describes in its section
+ * "Methodology notes" (Delta Rule, per-channel diagonal decay, L2-normalised
+ * q/k) and its section "Key data" (cost figures):
+ *
+ *     qh = q / sqrt(|q|^2 + 1e-6),   kh = k / sqrt(|k|^2 + 1e-6)    (fp32)
+ *     S' = Diag(exp g_t) S_{t-1}                      key rows decay
+ *     S_t = S' + beta_t kh (v_t - S'^T kh)^T          delta-rule step
+ *     o_t = S_t^T qh                                  reads the updated state
+ *
+ * with S an fp32 Dk x Dv state per (sequence, head).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers into contiguous, row-major buffers
+ *     that the caller owns and allocates (the library allocates nothing).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No entry point synchronises the stream.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a negative kda_status and touches no buffer.
+ *     kda_last_error() then returns a message (thread-local).
+ *   - Conditions only the device can see (malformed cu_seqlens, checkpoint
+ *     capacity too small) are recorded in a status word inside the caller's
+ *     workspace; kda_prefill_status() reads it back (this one call
+ *     synchronises the stream).
+ *   - Supported shapes: Dk == Dv in {64, 128}; chunk == 64; dtype of q, k, v
+ *     and out bf16 or fp32; g, beta, states and checkpoints always fp32.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,    /* null pointer, bad size, malformed cu_seqlens */
+    KDA_ERR_UNSUPPORTED = -2,    /* valid but not implemented (head dim, chunk) */
+    KDA_ERR_CUDA = -3,           /* a CUDA launch or runtime call failed */
+    KDA_ERR_CKPT_OVERFLOW = -4,  /* more checkpoints due than ckpt_capacity slots */
+    KDA_ERR_WORKSPACE = -5,      /* workspace missing or smaller than required */
+    KDA_ERR_TIMEOUT = -6         /* a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum {
+    KDA_DTYPE_BF16 = 0,          /* q, k, v, out are bf16 */
+    KDA_DTYPE_FP32 = 1           /* q, k, v, out are fp32 */
+} kda_dtype;
+
+/*
+ * Shape and options of one prefill call.
+ *   num_seqs       N >= 1.
+ *   total_tokens   T >= 0: rows of q/k/v/g/beta/out.  With cu_seqlens == NULL
+ *                  the batch is N equal-length sequences laid out one after
+ *                  another (T must be a multiple of N).
+ *   num_heads      H >= 1.
+ *   head_dim_k/v   Dk, Dv (must be equal, 64 or 128).
+ *   dtype          element type of q, k, v and out.
+ *   chunk          C, the block length of the chunked form (64).
+ *   ckpt_stride    0 = no checkpoints; else a multiple of chunk: after every
+ *                  ckpt_stride tokens of a sequence the state is copied to
+ *                  the next checkpoint slot (the page's prefix-cache
+ *                  snapshots every 32K tokens, zsxq post on SemiAnalysis'
+ *                  Kimi K3 analysis, section "五、KV缓存效率与服务性能").
+ *   ckpt_capacity  number of [H, Dk, Dv] slots in `ckpts`.
+ */
+typedef struct {
+    int32_t num_seqs;
+    int64_t total_tokens;
+    int32_t num_heads;
+    int32_t head_dim_k;
+    int32_t head_dim_v;
+    kda_dtype dtype;
+    int32_t chunk;
+    int32_t ckpt_stride;
+    int64_t ckpt_capacity;
+} kda_prefill_desc;
+
+/*
+ * Bytes of device workspace kda_prefill needs for `desc` (0 if desc is
+ * invalid).  The workspace is caller-owned scratch; it holds the per-chunk
+ * table, the device status word and the handoff between the preparation and
+ * recurrence kernels.  One workspace must not be shared by calls that can run
+ * concurrently.
+ */
+size_t kda_prefill_workspace_size(const kda_prefill_desc *desc);
+
+/*
+ * Chunked prefill over packed sequences (K1 tensor preparation + K2 blockwise
+ * recurrence; page "Kimi K3 reconstructs long-context inference efficiency
+ * ...", section "Methodology notes", item "System optimization: FlashKDA";
+ * zsxq post, section "一、Kimi Delta Attention（KDA）": chunk-level
+ * parallelism through the UT transform).
+ *
+ *   q, k        [T, H, Dk]  dtype          (normalised inside, in fp32)
+ *   v           [T, H, Dv]  dtype
+ *   g           [T, H, Dk]  fp32  log-decay, alpha = exp(g); within one chunk
+ *                                 the running sum of g must stay above -80
+ *   beta        [T, H]      fp32
+ *   init_state  [N, H, Dk, Dv] fp32, or NULL for zeros
+ *   cu_seqlens  [N + 1] int32 token offsets (0 = cu[0] <= ... <= cu[N] = T),
+ *               or NULL for N equal-length sequences
+ *   out         [T, H, Dv]  dtype          (written)
+ *   final_state [N, H, Dk, Dv] fp32 or NULL; may alias init_state
+ *   ckpts       [ckpt_capacity, H, Dk, Dv] fp32, or NULL when ckpt_stride == 0;
+ *               slots are filled in sequence order, then snapshot order; a
+ *               sequence of length L emits floor(L / ckpt_stride) snapshots
+ *   workspace   >= kda_prefill_workspace_size(desc) bytes, 256-byte aligned
+ *
+ * out must not alias any input.  Returns KDA_OK once the work is enqueued.
+ */
+kda_status kda_prefill(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                       void *out, float *final_state, float *ckpts,
+                       const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                       kda_stream_t stream);
+
+/*
+ * Reads (and clears) the device status word of `workspace` after the work
+ * queued on `stream`: KDA_OK, KDA_ERR_INVALID_ARG (malformed cu_seqlens; the
+ * affected sequences were skipped) or KDA_ERR_CKPT_OVERFLOW (snapshots beyond
+ * ckpt_capacity were dropped).  Synchronises `stream`.
+ */
+kda_status kda_prefill_status(void *workspace, kda_stream_t stream);
+
+/*
+ * One decode step for N sequences x H heads, state updated in place (page
+ * "Kimi K3 reconstructs long-context inference efficiency ...", section "Key
+ * data": about 7*D^2 FLOPs and 8*D^2 bytes of fp32 state traffic per head).
+ *
+ *   q, k   [N, H, Dk] dtype;   v [N, H, Dv] dtype;   g [N, H, Dk] fp32;
+ *   beta   [N, H] fp32;        state [N, H, Dk, Dv] fp32, read and written;
+ *   out    [N, H, Dv] dtype    (written; must not alias the inputs or state)
+ */
+kda_status kda_decode(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, float *state, void *out, int32_t N, int32_t H,
+                      int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *kda_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,178 @@
+// api.cu -- the C ABI declared in include/kda.h: argument validation,
+// workspace layout and kernel dispatch.  No allocation, no synchronisation
+// (except kda_prefill_status, documented as synchronising).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "kda_common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kda_status fail(kda_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+kda_status cuda_fail(cudaError_t e, const char *where)
+{
+    return fail(KDA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t status, cu, chunk_off, ckpt_off, handoff, total;
+    int max_chunks;
+};
+
+// Validates the descriptor; fills the workspace layout on success.
+kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
+{
+    if (!d) return fail(KDA_ERR_INVALID_ARG, "desc is NULL");
+    if (d->num_seqs < 1) return fail(KDA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", d->num_seqs);
+    if (d->total_tokens < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens must be >= 0");
+    if (d->total_tokens > (int64_t)INT32_MAX / 2)
+        return fail(KDA_ERR_UNSUPPORTED, "total_tokens %lld too large", (long long)d->total_tokens);
+    if (d->num_heads < 1) return fail(KDA_ERR_INVALID_ARG, "num_heads must be >= 1");
+    if (d->head_dim_k != d->head_dim_v)
+        return fail(KDA_ERR_UNSUPPORTED, "head_dim_k (%d) != head_dim_v (%d)", d->head_dim_k, d->head_dim_v);
+    if (d->head_dim_k != 64 && d->head_dim_k != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", d->head_dim_k);
+    if (d->dtype != KDA_DTYPE_BF16 && d->dtype != KDA_DTYPE_FP32)
+        return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)d->dtype);
+    if (d->chunk != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk %d not supported (64)", d->chunk);
+    if (d->ckpt_stride < 0 || (d->ckpt_stride > 0 && d->ckpt_stride % d->chunk != 0))
+        return fail(KDA_ERR_INVALID_ARG, "ckpt_stride %d must be 0 or a positive multiple of chunk", d->ckpt_stride);
+    if (d->ckpt_capacity < 0) return fail(KDA_ERR_INVALID_ARG, "ckpt_capacity must be >= 0");
+    const int64_t maxc = d->total_tokens / d->chunk + d->num_seqs;
+    if (maxc > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many chunks");
+    Layout L;
+    L.max_chunks = (int)maxc;
+    size_t off = 0;
+    L.status = off; off = align256(off + sizeof(kda::DevStatus));
+    L.cu = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
+    L.chunk_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
+    L.ckpt_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
+    L.handoff = off;
+    off = align256(off + kda::simt_handoff_bytes_per_chunk(d->head_dim_k, d->chunk) *
+                             (size_t)maxc * (size_t)d->num_heads);
+    L.total = off;
+    *lay = L;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_last_error(void) { return g_last_error.c_str(); }
+
+int32_t kda_version(void) { return 100; }
+
+size_t kda_prefill_workspace_size(const kda_prefill_desc *desc)
+{
+    Layout L;
+    if (check_desc(desc, &L) != KDA_OK) return 0;
+    return L.total;
+}
+
+kda_status kda_prefill(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                       void *out, float *final_state, float *ckpts,
+                       const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                       kda_stream_t stream)
+{
+    Layout L;
+    kda_status s = check_desc(desc, &L);
+    if (s != KDA_OK) return s;
+    const int64_t T = desc->total_tokens;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta and out must be non-NULL");
+    if (!cu_seqlens && T % desc->num_seqs != 0)
+        return fail(KDA_ERR_INVALID_ARG, "total_tokens %lld not a multiple of num_seqs %d (cu_seqlens NULL)",
+                    (long long)T, desc->num_seqs);
+    if (desc->ckpt_stride > 0 && !ckpts && desc->ckpt_capacity > 0)
+        return fail(KDA_ERR_INVALID_ARG, "ckpts is NULL but ckpt_capacity > 0");
+    if (!workspace) return fail(KDA_ERR_WORKSPACE, "workspace is NULL");
+    if (workspace_bytes < L.total)
+        return fail(KDA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
+    if (((uintptr_t)workspace & 255) != 0) return fail(KDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (out && (out == q || out == k || out == v))
+        return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
+
+    char *ws = (char *)workspace;
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.init_state = init_state;
+    a.cu_seqlens = cu_seqlens; a.out = out; a.final_state = final_state;
+    a.ckpts = desc->ckpt_stride > 0 ? ckpts : nullptr;
+    a.N = desc->num_seqs; a.H = desc->num_heads; a.D = desc->head_dim_k; a.C = desc->chunk;
+    a.T = T; a.ckpt_stride = desc->ckpt_stride; a.ckpt_capacity = desc->ckpt_capacity;
+    a.dtype = desc->dtype; a.max_chunks = L.max_chunks;
+    a.status = (kda::DevStatus *)(ws + L.status);
+    a.tab.cu = (int32_t *)(ws + L.cu);
+    a.tab.chunk_off = (int32_t *)(ws + L.chunk_off);
+    a.tab.ckpt_off = (int32_t *)(ws + L.ckpt_off);
+    a.handoff = ws + L.handoff;
+    a.handoff_bytes = L.total - L.handoff;
+    a.stream = (cudaStream_t)stream;
+
+    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
+    if ((e = kda::launch_prefill_simt(a)) != cudaSuccess) return cuda_fail(e, "prefill kernels");
+    return KDA_OK;
+}
+
+kda_status kda_prefill_status(void *workspace, kda_stream_t stream)
+{
+    if (!workspace) return fail(KDA_ERR_WORKSPACE, "workspace is NULL");
+    int32_t code = 0;
+    cudaError_t e = cudaMemcpyAsync(&code, workspace, sizeof code, cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    if (code == KDA_OK) return KDA_OK;
+    if (code == KDA_ERR_CKPT_OVERFLOW)
+        return fail(KDA_ERR_CKPT_OVERFLOW, "more checkpoints due than ckpt_capacity; extra snapshots dropped");
+    if (code == KDA_ERR_INVALID_ARG)
+        return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens (must start at 0, be non-decreasing, end at T)");
+    if (code == KDA_ERR_TIMEOUT) return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait gave up");
+    return fail((kda_status)code, "device reported status %d", code);
+}
+
+kda_status kda_decode(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, float *state, void *out, int32_t N, int32_t H,
+                      int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+{
+    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
+    if (Dk != Dv) return fail(KDA_ERR_UNSUPPORTED, "Dk (%d) != Dv (%d)", Dk, Dv);
+    if (Dk != 64 && Dk != 128) return fail(KDA_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", Dk);
+    if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32)
+        return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if ((size_t)N * H == 0) return KDA_OK;
+    if ((size_t)N * H > (size_t)INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N*H too large");
+    if (!q || !k || !v || !g || !beta || !state || !out)
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta, state and out must be non-NULL");
+    if (((uintptr_t)state & 15) != 0) return fail(KDA_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    if (out == q || out == k || out == v || out == (void *)state)
+        return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype,
+                                       (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    return KDA_OK;
+}
+
+}  // extern "C"

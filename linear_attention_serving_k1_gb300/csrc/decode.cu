@@ -1,0 +1,153 @@
+// decode.cu -- single-token KDA decode step, fp32 state updated in place.
+//
+// Page "Kimi K3 reconstructs long-context inference efficiency through KDA,
+// cross-depth attention, and latent expert routing", section "Key data": a
+// decode step costs about 7*D^2 FLOPs and 8*D^2 bytes per head, the bytes
+// being one read and one write of the fp32 recurrent state.  The kernel is
+// therefore a streaming pass over the state at HBM speed:
+//
+//   one CTA per (sequence, head); each warp streams whole 512-byte rows of S
+//   as float4 (fully coalesced 128-bit loads); every element of S is read
+//   once into registers, decayed there, used for both reductions, updated
+//   from the same registers and written once.
+//
+//   S' = Diag(alpha) S                     (row scale, in registers)
+//   sk = S'^T kh, sq = S'^T qh             (one pass, CTA reduction in smem)
+//   u  = v - sk
+//   o  = sq + beta (kh . qh) u             (= S_new^T qh, no second pass)
+//   S_new = S' + beta kh u^T               (from registers, one write)
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+template <int D, typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+              const float *__restrict__ g, const float *__restrict__ beta,
+              float *__restrict__ state, T *__restrict__ out)
+{
+    constexpr int C4 = D / 4;            // float4 groups per state row
+    constexpr int RPI = THREADS / C4;    // rows covered per pass of the CTA
+    constexpr int RPT = D / RPI;         // rows per thread
+    static_assert(THREADS % C4 == 0 && D % RPI == 0, "shape");
+    constexpr int NW = THREADS / 32;
+
+    const size_t head = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int c4 = tid % C4;
+    const int r0 = tid / C4;
+
+    float4 *S = reinterpret_cast<float4 *>(state + head * (size_t)D * D);
+
+    // Issue every state load first: RPT independent 16-byte loads per thread.
+    float4 s[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) s[j] = __ldcs(S + (size_t)(r0 + j * RPI) * C4 + c4);
+
+    __shared__ float sh_qh[D], sh_kh[D], sh_a[D], sh_u[D];
+    __shared__ float sh_part[3][NW];
+    __shared__ float4 red_k[RPI][C4];
+    __shared__ float4 red_q[RPI][C4];
+
+    // Token vectors and the two L2 norms (fp32).
+    float qv = 0.f, kv = 0.f;
+    if (tid < D) {
+        qv = to_f32(q[head * D + tid]);
+        kv = to_f32(k[head * D + tid]);
+        sh_a[tid] = expf(g[head * D + tid]);
+    }
+    float pq = warp_sum(qv * qv), pk = warp_sum(kv * kv), pqk = warp_sum(qv * kv);
+    if ((tid & 31) == 0) {
+        sh_part[0][tid >> 5] = pq;
+        sh_part[1][tid >> 5] = pk;
+        sh_part[2][tid >> 5] = pqk;
+    }
+    __syncthreads();
+    float nq = 0.f, nk = 0.f, nqk = 0.f;
+#pragma unroll
+    for (int w = 0; w < (D + 31) / 32; ++w) {
+        nq += sh_part[0][w];
+        nk += sh_part[1][w];
+        nqk += sh_part[2][w];
+    }
+    const float rq = rsqrtf(nq + 1e-6f), rk = rsqrtf(nk + 1e-6f);
+    const float b = beta[head];
+    if (tid < D) {
+        sh_qh[tid] = qv * rq;
+        sh_kh[tid] = kv * rk;
+    }
+    __syncthreads();
+
+    // Decay in registers and accumulate S'^T kh and S'^T qh.
+    float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), aq = ak;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int i = r0 + j * RPI;
+        const float a = sh_a[i], kh = sh_kh[i], qh = sh_qh[i];
+        s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
+        ak.x += kh * s[j].x; ak.y += kh * s[j].y; ak.z += kh * s[j].z; ak.w += kh * s[j].w;
+        aq.x += qh * s[j].x; aq.y += qh * s[j].y; aq.z += qh * s[j].z; aq.w += qh * s[j].w;
+    }
+    red_k[r0][c4] = ak;
+    red_q[r0][c4] = aq;
+    __syncthreads();
+
+    if (tid < D) {
+        const float *rk_ = reinterpret_cast<const float *>(&red_k[0][0]);
+        const float *rq_ = reinterpret_cast<const float *>(&red_q[0][0]);
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int r = 0; r < RPI; ++r) {
+            sk += rk_[r * D + tid];
+            sq += rq_[r * D + tid];
+        }
+        const float u = to_f32(v[head * D + tid]) - sk;
+        sh_u[tid] = u;
+        const float kq = nqk * rq * rk;   // kh . qh
+        out[head * D + tid] = from_f32<T>(sq + b * kq * u);
+    }
+    __syncthreads();
+
+    const float4 u4 = reinterpret_cast<const float4 *>(sh_u)[c4];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int i = r0 + j * RPI;
+        const float bk = b * sh_kh[i];
+        float4 o;
+        o.x = s[j].x + bk * u4.x;
+        o.y = s[j].y + bk * u4.y;
+        o.z = s[j].z + bk * u4.z;
+        o.w = s[j].w + bk * u4.w;
+        __stcs(S + (size_t)i * C4 + c4, o);
+    }
+}
+
+template <int D, typename T>
+cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
+                     const float *beta, float *state, void *out, int N, int H, cudaStream_t st)
+{
+    constexpr int THREADS = (D == 128) ? 256 : 128;
+    const unsigned blocks = (unsigned)((size_t)N * H);
+    decode_kernel<D, T, THREADS><<<blocks, THREADS, 0, st>>>(
+        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *state, void *out, int N, int H, int D,
+                          kda_dtype dtype, cudaStream_t stream)
+{
+    if ((size_t)N * H == 0) return cudaSuccess;
+    if (D == 128)
+        return dtype == KDA_DTYPE_BF16
+                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, stream)
+                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, stream);
+    return dtype == KDA_DTYPE_BF16
+               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, stream)
+               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, stream);
+}
+
+}  // namespace kda

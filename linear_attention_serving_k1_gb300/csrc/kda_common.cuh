@@ -1,0 +1,76 @@
+// kda_common.cuh -- small device helpers shared by the KDA kernels of this
+// library (element conversion, warp reductions, cache-hinted loads/stores),
+// and the internal launcher interface between the C ABI and the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------- elements
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------ workspace map
+// Device status word values (a subset of kda_status, stored as int32).
+struct DevStatus {
+    int32_t code;        // 0 or a negative kda_status
+    int32_t pad[63];
+};
+
+// Per-call table produced on the device from cu_seqlens (no host sync):
+//   cu[n]        token offset of sequence n (a validated copy)
+//   chunk_off[n] first global chunk index of sequence n (prefix sum of ceil(len/C))
+//   ckpt_off[n]  first checkpoint slot of sequence n (prefix sum of floor(len/stride))
+struct SeqTable {
+    int32_t *cu;
+    int32_t *chunk_off;
+    int32_t *ckpt_off;
+};
+
+// ------------------------------------------------------------ launchers
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *g, *beta, *init_state;
+    const int32_t *cu_seqlens;   // may be NULL
+    void *out;
+    float *final_state, *ckpts;
+    int N, H, D, C;
+    int64_t T;
+    int ckpt_stride;
+    int64_t ckpt_capacity;
+    kda_dtype dtype;
+    int max_chunks;              // upper bound of chunks over all sequences
+    DevStatus *status;
+    SeqTable tab;
+    void *handoff;               // K1 -> K2 buffer
+    size_t handoff_bytes;
+    cudaStream_t stream;
+};
+
+// Bytes of the K1 -> K2 handoff buffer for one (chunk, head).
+size_t simt_handoff_bytes_per_chunk(int D, int C);
+
+cudaError_t launch_seq_table(const PrefillArgs &a);
+cudaError_t launch_prefill_simt(const PrefillArgs &a);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *state, void *out, int N, int H, int D,
+                          kda_dtype dtype, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,163 @@
+"""Thin Python binding of the C ABI in include/kda.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of ``_build/libkda.so``;
+PyTorch only provides device memory and the current stream.  There is no CPU
+fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+STATUS_NAMES = {0: "KDA_OK", -1: "KDA_ERR_INVALID_ARG", -2: "KDA_ERR_UNSUPPORTED", -3: "KDA_ERR_CUDA",
+                -4: "KDA_ERR_CKPT_OVERFLOW", -5: "KDA_ERR_WORKSPACE", -6: "KDA_ERR_TIMEOUT"}
+DTYPE_BF16, DTYPE_FP32 = 0, 1
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_status", "kda_decode",
+           "kda_last_error", "kda_version")
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
+                ("num_heads", ctypes.c_int32), ("head_dim_k", ctypes.c_int32),
+                ("head_dim_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
+                ("ckpt_capacity", ctypes.c_int64)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def load_library(path: Optional[str] = None):
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with linear_attention_serving_k1_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc)]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp, ctypes.c_size_t, _vp]
+    lib.kda_prefill_status.restype = ctypes.c_int
+    lib.kda_prefill_status.argtypes = [_vp, _vp]
+    lib.kda_decode.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_last_error.argtypes = []
+    lib.kda_version.restype = ctypes.c_int32
+    lib.kda_version.argtypes = []
+    if path == _build.library_path():
+        _lib = lib
+    return lib
+
+
+def _check(code: int):
+    if code != KDA_OK:
+        raise KDAError(code, load_library().kda_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the KDA library must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the KDA library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise ValueError(f"q/k/v must be bf16 or fp32, got {t.dtype}")
+
+
+def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
+              ckpt_stride: int = 0, ckpt_capacity: int = 0) -> PrefillDesc:
+    return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity)
+
+
+def workspace_size(desc: PrefillDesc) -> int:
+    n = load_library().kda_prefill_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise KDAError(-1, load_library().kda_last_error().decode())
+    return int(n)
+
+
+def alloc_workspace(desc: PrefillDesc, device) -> torch.Tensor:
+    return torch.empty(workspace_size(desc), dtype=torch.uint8, device=device)
+
+
+def num_checkpoints(lens, ckpt_stride: int) -> int:
+    return 0 if ckpt_stride <= 0 else int(sum(int(L) // ckpt_stride for L in lens))
+
+
+def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
+            chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
+            out=None, final_state=None, workspace=None, stream=None, want_final: bool = True):
+    """Chunked KDA prefill through ``kda_prefill``.
+
+    q, k, g: [T, H, D]; v: [T, H, D]; beta: [T, H]; init_state: [N, H, D, D] fp32 or
+    None; cu_seqlens: [N + 1] int32 on the device, or None with ``num_seqs``
+    equal-length sequences (default 1).  Returns (out, final_state, ckpts).
+    """
+    T, H, D = q.shape
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (num_seqs or 1)
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, v.shape[2], dtype=q.dtype, device=dev)
+    if final_state is None and want_final:
+        final_state = torch.empty(N, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    if ckpt_stride > 0 and ckpts is None:
+        cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
+        ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap)
+    if workspace is None:
+        workspace = alloc_workspace(desc, dev)
+    code = load_library().kda_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+        _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(code)
+    return out, final_state, ckpts
+
+
+def prefill_status(workspace: torch.Tensor, stream=None) -> int:
+    """Device-side status of the last prefill on ``workspace`` (synchronises)."""
+    return int(load_library().kda_prefill_status(_ptr(workspace), _stream(stream)))
+
+
+def decode(q, k, v, g, beta, state, out=None, stream=None):
+    """One decode step through ``kda_decode``; ``state`` [N, H, D, D] is updated in place."""
+    N, H, D = q.shape
+    if out is None:
+        out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
+    code = load_library().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                     _ptr(out), N, H, D, v.shape[2], _dtype_code(q), _stream(stream))
+    _check(code)
+    return out
