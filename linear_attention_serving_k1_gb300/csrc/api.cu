@@ -65,8 +65,10 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     L.chunk_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.ckpt_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.handoff = off;
-    off = align256(off + kda::simt_handoff_bytes_per_chunk(d->head_dim_k, d->chunk) *
-                             (size_t)maxc * (size_t)d->num_heads);
+    const size_t rec = kda::use_tc_path(d->dtype, d->head_dim_k, d->chunk)
+                           ? kda::tc_handoff_bytes_per_chunk()
+                           : kda::simt_handoff_bytes_per_chunk(d->head_dim_k, d->chunk);
+    off = align256(off + rec * (size_t)maxc * (size_t)d->num_heads);
     L.total = off;
     *lay = L;
     return KDA_OK;
@@ -130,7 +132,8 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
-    if ((e = kda::launch_prefill_simt(a)) != cudaSuccess) return cuda_fail(e, "prefill kernels");
+    e = kda::use_tc_path(a.dtype, a.D, a.C) ? kda::launch_prefill_tc(a) : kda::launch_prefill_simt(a);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill kernels");
     return KDA_OK;
 }
 

@@ -67,8 +67,19 @@ struct PrefillArgs {
 // Bytes of the K1 -> K2 handoff buffer for one (chunk, head).
 size_t simt_handoff_bytes_per_chunk(int D, int C);
 
+// Bytes of the tensor-core path's K1 -> K2 record for one (chunk, head).
+size_t tc_handoff_bytes_per_chunk();
+
+// The tensor-core path serves bf16 inputs with Dk = Dv = 128 and chunk 64;
+// everything else runs on the fp32 CUDA-core path.
+inline bool use_tc_path(kda_dtype dtype, int D, int C)
+{
+    return dtype == KDA_DTYPE_BF16 && D == 128 && C == 64;
+}
+
 cudaError_t launch_seq_table(const PrefillArgs &a);
 cudaError_t launch_prefill_simt(const PrefillArgs &a);
+cudaError_t launch_prefill_tc(const PrefillArgs &a);
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, cudaStream_t stream);

@@ -17,6 +17,7 @@ from . import build as _build
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", -1: "KDA_ERR_INVALID_ARG", -2: "KDA_ERR_UNSUPPORTED", -3: "KDA_ERR_CUDA",
                 -4: "KDA_ERR_CKPT_OVERFLOW", -5: "KDA_ERR_WORKSPACE", -6: "KDA_ERR_TIMEOUT"}
+STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.

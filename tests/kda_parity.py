@@ -14,13 +14,38 @@ TOL_OUT_BF16 = 2e-2
 TOL_STATE = 1e-2
 
 
-def out_err(o_gpu, o_ref) -> float:
+def bf16_half_ulp(x) -> np.ndarray:
+    """Largest error of rounding the exact value x to bf16 (8 significant bits):
+    half the bf16 spacing 2^(e-7) of the binade [2^e, 2^(e+1)) holding |x|."""
+    ax = np.maximum(np.abs(np.asarray(x, np.float64)), np.finfo(np.float32).tiny)
+    e = np.floor(np.log2(ax))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
+def out_err(o_gpu, o_ref, bf16_output=None) -> float:
+    """max |o - o_ref| / rms(o_ref).
+
+    For bf16 outputs (detected from the values when bf16_output is None) the
+    half-ulp that rounding the exact result to bf16 costs by itself is not
+    counted: |o - o_ref| is reduced by bf16_half_ulp(o_ref) before the max.
+    Outputs here are heavy-tailed (max/rms ~ 10-20), so that rounding alone can
+    reach 2e-2 * rms; the bar is meant for the arithmetic."""
     o_gpu = np.asarray(o_gpu, np.float64)
     o_ref = np.asarray(o_ref, np.float64)
     if o_ref.size == 0:
         return 0.0
     rms = np.sqrt(np.mean(o_ref * o_ref))
-    return float(np.abs(o_gpu - o_ref).max() / max(rms, 1e-30))
+    diff = np.abs(o_gpu - o_ref)
+    if bf16_output is None:
+        bf16_output = bool(np.all(o_gpu.astype(np.float32).view(np.uint32) & 0xFFFF == 0))
+    if bf16_output:
+        diff = np.maximum(diff - bf16_half_ulp(o_ref), 0.0)
+    return float(diff.max() / max(rms, 1e-30))
+
+
+def out_err_raw(o_gpu, o_ref) -> float:
+    """max |o - o_ref| / rms(o_ref) with nothing discounted."""
+    return out_err(o_gpu, o_ref, bf16_output=False)
 
 
 def state_err(s_gpu, s_ref) -> float:

@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/kda.h declares, and rejects invalid calls on the host
+before touching the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_serving_k1_gb300 import build, kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        build.nvcc()
+    except RuntimeError:
+        pytest.skip("no CUDA toolkit to build the library")
+    build.build()
+    return kda.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(kda.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert lib.kda_version() >= 100
+
+
+def _desc(**kw):
+    d = dict(T=256, H=2, D=64, num_seqs=1, dtype_code=kda.DTYPE_FP32, chunk=64, ckpt_stride=0,
+             ckpt_capacity=0)
+    d.update(kw)
+    return kda.make_desc(**d)
+
+
+def test_workspace_size(lib):
+    n = lib.kda_prefill_workspace_size(ctypes.byref(_desc()))
+    assert n > 0 and n % 256 == 0
+    bigger = lib.kda_prefill_workspace_size(ctypes.byref(_desc(T=1024)))
+    assert bigger > n
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), -2), (dict(chunk=32), -2), (dict(num_seqs=0), -1), (dict(T=-1), -1),
+    (dict(H=0), -1), (dict(dtype_code=7), -1), (dict(ckpt_stride=100), -1),
+])
+def test_invalid_desc(lib, kw, code):
+    d = _desc(**kw)
+    assert lib.kda_prefill_workspace_size(ctypes.byref(d)) == 0
+    rc = lib.kda_prefill(*([ctypes.c_void_p(16)] * 7), ctypes.c_void_p(16), None, None,
+                         ctypes.byref(d), ctypes.c_void_p(256), ctypes.c_size_t(1 << 30), None)
+    assert rc == code
+    assert lib.kda_last_error()
+
+
+def test_prefill_rejects_before_launch(lib):
+    d = _desc()
+    ws = lib.kda_prefill_workspace_size(ctypes.byref(d))
+    p = ctypes.c_void_p(4096)
+    # NULL q
+    assert lib.kda_prefill(None, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d), ctypes.c_void_p(1 << 20), ws, None) == -1
+    # workspace too small / misaligned / missing
+    assert lib.kda_prefill(p, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d), ctypes.c_void_p(1 << 20), ws - 1, None) == -5
+    assert lib.kda_prefill(p, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d), ctypes.c_void_p((1 << 20) + 8), ws, None) == -5
+    assert lib.kda_prefill(p, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d), None, ws, None) == -5
+    # out aliasing q
+    assert lib.kda_prefill(p, ctypes.c_void_p(8192), p, p, p, None, None, p, None, None,
+                           ctypes.byref(d), ctypes.c_void_p(1 << 20), ws, None) == -1
+    # equal-length batch that does not divide
+    d2 = _desc(T=255, num_seqs=2)
+    ws2 = lib.kda_prefill_workspace_size(ctypes.byref(d2))
+    assert lib.kda_prefill(p, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d2), ctypes.c_void_p(1 << 20), ws2, None) == -1
+    # checkpoints requested with capacity but no buffer
+    d3 = _desc(ckpt_stride=64, ckpt_capacity=4)
+    ws3 = lib.kda_prefill_workspace_size(ctypes.byref(d3))
+    assert lib.kda_prefill(p, p, p, p, p, None, None, ctypes.c_void_p(8192), None, None,
+                           ctypes.byref(d3), ctypes.c_void_p(1 << 20), ws3, None) == -1
+
+
+def test_decode_rejects_before_launch(lib):
+    p = ctypes.c_void_p(4096)
+    o = ctypes.c_void_p(8192)
+    assert lib.kda_decode(p, p, p, p, p, p, o, 2, 2, 64, 128, 0, None) == -2    # Dk != Dv
+    assert lib.kda_decode(p, p, p, p, p, p, o, 2, 2, 96, 96, 0, None) == -2     # head dim
+    assert lib.kda_decode(p, p, p, p, p, p, o, -1, 2, 64, 64, 0, None) == -1    # N < 0
+    assert lib.kda_decode(None, p, p, p, p, p, o, 2, 2, 64, 64, 0, None) == -1  # NULL q
+    assert lib.kda_decode(p, p, p, p, p, ctypes.c_void_p(4100), o, 2, 2, 64, 64, 0, None) == -1  # misaligned state
+    assert lib.kda_decode(p, p, p, p, p, p, p, 2, 2, 64, 64, 0, None) == -1     # out aliases q
+    assert lib.kda_decode(p, p, p, p, p, p, o, 2, 2, 64, 64, 5, None) == -1     # dtype
+    assert lib.kda_decode(p, p, p, p, p, p, o, 0, 2, 64, 64, 0, None) == 0      # empty: nothing to do
