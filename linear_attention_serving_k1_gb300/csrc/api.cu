@@ -133,7 +133,9 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
     e = kda::use_tc_path(a.dtype, a.D, a.C) ? kda::launch_prefill_tc(a) : kda::launch_prefill_simt(a);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill kernels");
+    if (e != cudaSuccess)
+        return fail(KDA_ERR_CUDA, "prefill kernels: %s %s", cudaGetErrorString(e),
+                    kda::use_tc_path(a.dtype, a.D, a.C) ? kda::launch_failure_detail() : "");
     return KDA_OK;
 }
 

@@ -80,6 +80,8 @@ inline bool use_tc_path(kda_dtype dtype, int D, int C)
 cudaError_t launch_seq_table(const PrefillArgs &a);
 cudaError_t launch_prefill_simt(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a);
+// Kernel attributes noted by the last failed tensor-core launch on this thread ("" if none).
+const char *launch_failure_detail();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, cudaStream_t stream);

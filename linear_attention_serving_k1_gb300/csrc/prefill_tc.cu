@@ -16,9 +16,10 @@
 //       T  = (I + L)^-1                            (fp32, blocked, CUDA cores)
 //       Wk = T diag(beta) Kg, Uv = T diag(beta) V   (MMAs)
 //       A' = -Ke^T Wk,  Q' = Qg - Mc Wk             (MMAs)
-//   K2  S_next = Diag(gamma) S + A' S + Ke^T Uv     (fp32 state, one MMA
-//                                                    on the serial path)
-//       O      = Q' S + Mc Uv
+//       Bc = Ke^T Uv, Ol = Mc Uv                    (MMAs)
+//   K2  S_next = Diag(gamma) S + A' S + Bc          (fp32 state, one MMA
+//                                                    group on the serial path)
+//       O      = Q' S + Ol
 // which is W = Uv - Wk S, O = Qg S + Mc W, S_next = Diag(gamma) S + Ke^T W
 // with W eliminated: the serial chain carries one state-dependent MMA per
 // chunk instead of two.
@@ -27,14 +28,16 @@
 // tf32 for the Gram product of K1 and f16 for every other product (values
 // of v and of the state must stay within the f16 range, |x| < 65504).
 //
-// K1 writes, per (chunk, head), one 90,624-byte record holding the K2 operand
-// tiles already in the tensor-core shared-memory layout (no-swizzle K-major
-// core matrices), so K2 moves each record into shared memory with a single
-// bulk (TMA) copy.
+// K1 writes, per (chunk, head), one record: the operands of K2's two state
+// products (A', Q') already in the tensor-core shared-memory layout
+// (no-swizzle K-major core matrices, moved by one bulk TMA copy), gamma, and
+// the state-independent terms Ke^T Uv and Mc Uv, which K2's state threads
+// read straight from global memory.
 #include "kda_common.cuh"
 #include "tc.cuh"
 
 #include <cuda_fp16.h>
+#include <stdio.h>
 
 namespace kda {
 namespace {
@@ -46,19 +49,22 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 
 // ------------------------------------------------------------ record layout
-// A'  : B operand, rows d (128) x K = d' (128)   LBO 128, SBO 2048
-// Q'  : B operand, rows r (64)  x K = d (128)    LBO 128, SBO 2048
-// Uv^T: A operand, rows e (128) x K = r (64)     LBO 128, SBO 1024
-// Ke^T: B operand, rows d (128) x K = r (64)     LBO 128, SBO 1024
-// Mc  : B operand, rows r (64)  x K = i (64)     LBO 128, SBO 1024
+// The first REC_SMEM bytes are copied into K2's shared memory (tensor-core
+// operand tiles, no-swizzle K-major core matrices); the rest is read by K2's
+// state threads straight from global memory.
+// A'   : B operand, rows d (128) x K = d' (128)   LBO 128, SBO 2048   f16
+// Q'   : B operand, rows r (64)  x K = d (128)    LBO 128, SBO 2048   f16
 // gamma: fp32 [128]
+// Bc^T : (Ke^T Uv)^T row-major [e][d]                                  f16
+// Ol^T : (Mc Uv)^T  row-major [e][r]                                   f16
 constexpr uint32_t REC_AP = 0;
 constexpr uint32_t REC_QP = 32768;
-constexpr uint32_t REC_UVT = 49152;
-constexpr uint32_t REC_KET = 65536;
-constexpr uint32_t REC_M = 81920;
-constexpr uint32_t REC_G = 90112;
-constexpr uint32_t REC_BYTES = 90624;
+constexpr uint32_t REC_G = 49152;
+constexpr uint32_t REC_SMEM = 49664;
+constexpr uint32_t REC_BC = REC_SMEM;
+constexpr uint32_t REC_OL = REC_BC + 32768;
+constexpr uint32_t REC_BYTES = REC_OL + 16384;
+static_assert(REC_SMEM % 16 == 0 && REC_BYTES % 256 == 0, "record alignment");
 constexpr uint32_t SBO_K128 = 2048;   // 8-row group stride when K = 128 (K-inner packing)
 constexpr uint32_t SBO_K64 = 1024;    // ... when K = 64
 constexpr uint32_t LBO_KIN = 128;     // K-inner packing: core matrices along K are adjacent
@@ -96,7 +102,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // ============================================================ K1
-// One CTA (128 threads) per (chunk, head).  The Gram product G = [Kg; Qg] Kd^T
+// One CTA (256 threads) per (chunk, head).  The Gram product G = [Kg; Qg] Kd^T
 // runs as tf32 (its decayed factors e^{+-b} need the fp32 exponent range);
 // every other product takes f16 operands (11 significant bits: the bf16
 // rounding of 8 bits was measured to put the max output error of long
@@ -111,18 +117,23 @@ constexpr uint32_t K1_F32_SBO = 32 * K1_F32_LBO;
 constexpr uint32_t K1_KGT = K1_GA + 16 * K1_F32_SBO;   // f16 Kg^T: rows d x K = i (128 x 64)
 constexpr uint32_t K1_VT = K1_KGT + 16384;             // f16 V^T : rows e x K = i
 constexpr uint32_t K1_KET = K1_VT + 16384;             // f16 Ke^T: rows d x K = r
-constexpr uint32_t K1_SMEM = K1_KET + 16384;
+constexpr uint32_t K1_RAW = K1_KET + 16384;            // bf16 q, k, v rows of the chunk [3][64][128]
+constexpr uint32_t K1_SMEM = K1_RAW + 3 * 64 * 256;
 // second phase, inside [0, 73728)
-constexpr uint32_t K1_LM = 0;            // fp32 [64][65]  L (strict lower, beta-scaled)
-constexpr uint32_t K1_TM = 16640;        // fp32 [64][65]  T = (I + L)^-1
-constexpr uint32_t K1_XS = 33280;        // fp32 [3][16][17] scratch of the blocked inverse
-constexpr uint32_t K1_TB = 36864;        // f16 T diag(beta): rows r x K = i (64 x 64)
-constexpr uint32_t K1_MC = 45056;        // f16 Mc: rows r x K = i (64 x 64)
-constexpr uint32_t K1_WKT = 53248;       // f16 Wk^T: rows d x K = r (128 x 64)
+constexpr int K1_P = 68;                 // fp32 row pitch of L and T (16-byte aligned rows)
+constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower, beta-scaled)
+constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
+constexpr uint32_t K1_XS = 34816;        // fp32 [3][16][16] scratch of the blocked inverse (ends 37888)
+constexpr uint32_t K1_TB = 37888;        // f16 T diag(beta): rows r x K = i (64 x 64)
+constexpr uint32_t K1_MC = 46080;        // f16 Mc: rows r x K = i (64 x 64)
+constexpr uint32_t K1_WKT = 54272;       // f16 Wk^T: rows d x K = r (128 x 64)
+constexpr uint32_t K1_UVT = 0;           // f16 Uv^T: rows e x K = r (128 x 64), over L once T is built
 static_assert(K1_WKT + 16384 <= K1_GA + 8 * K1_F32_SBO, "second phase must stay in the freed region");
+static_assert(K1_SMEM <= 227 * 1024 - 2048, "shared memory");
+constexpr int K1_THREADS = 256;
 
 // TMEM columns (256 allocated)
-constexpr uint32_t T1_G = 0, T1_W1 = 64, T1_W2 = 128, T1_AP = 0, T1_QP = 128;
+constexpr uint32_t T1_G = 0, T1_W1 = 64, T1_W2 = 128, T1_AP = 0, T1_QP = 128, T1_BC = 0, T1_OL = 128;
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
@@ -130,7 +141,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ uint4 pack_f16x8(const float *x)
+{
+    return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                      pack_f16x2(x[6], x[7]));
+}
+
+__global__ void __launch_bounds__(K1_THREADS, 1)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ handoff, DevStatus *st)
@@ -139,14 +156,20 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float rq[kC], rk[kC], bs[kC];
+    __shared__ float bhalf[kD], blast[kD];
 
-    const int gc = blockIdx.x, h = blockIdx.y;
+    // heads vary fastest across the grid: CTAs running together read adjacent
+    // 256-byte slices of the same token rows
+    const int gc = blockIdx.y, h = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (gc >= tab.chunk_off[N]) return;   // uniform across the CTA, before any allocation
     const int n = find_seq_tc(tab.chunk_off, N, gc);
     const int t0 = tab.cu[n] + (gc - tab.chunk_off[n]) * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = handoff + ((size_t)gc * H + h) * REC_BYTES;
+    const bf16 *rawq = reinterpret_cast<const bf16 *>(sm + K1_RAW);
+    const bf16 *rawk = rawq + 64 * kD;
+    const bf16 *rawv = rawk + 64 * kD;
 
     if (warp == 0) {
         tmem_alloc(&tmem_sh, 256);
@@ -156,80 +179,113 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
-
-    // 1. row norms of q and k (warp w: rows 16w..16w+15), beta
-    for (int rr = 0; rr < 16; ++rr) {
-        const int r = warp * 16 + rr;
-        float sq = 0.f, sk = 0.f;
-        if (r < L) {
-            const size_t base = ((size_t)(t0 + r) * H + h) * kD + lane * 4;
-            const uint2 qa = *reinterpret_cast<const uint2 *>(q + base);
-            const uint2 ka = *reinterpret_cast<const uint2 *>(k + base);
-            float a0 = bf_lo(qa.x), a1 = bf_hi(qa.x), a2 = bf_lo(qa.y), a3 = bf_hi(qa.y);
-            float c0 = bf_lo(ka.x), c1 = bf_hi(ka.x), c2 = bf_lo(ka.y), c3 = bf_hi(ka.y);
-            sq = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-            sk = c0 * c0 + c1 * c1 + c2 * c2 + c3 * c3;
+    __syncthreads();
+    // 0. the chunk's q, k, v rows (256 bytes each) into shared memory: every
+    //    thread issues its 16-byte loads first, then stores them
+    {
+        uint4 buf[12];
+#pragma unroll
+        for (int j = 0; j < 12; ++j) {
+            const int idx = tid + j * K1_THREADS;          // 0 .. 3071
+            const int tsr = idx >> 10, r = (idx >> 4) & 63, c16 = idx & 15;
+            const bf16 *srcp = tsr == 0 ? q : (tsr == 1 ? k : v);
+            buf[j] = r < L ? __ldg(reinterpret_cast<const uint4 *>(srcp + ((size_t)(t0 + r) * H + h) * kD) + c16)
+                           : make_uint4(0u, 0u, 0u, 0u);
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        if (lane == 0) {
-            rq[r] = r < L ? rsqrtf(sq + 1e-6f) : 0.f;
-            rk[r] = r < L ? rsqrtf(sk + 1e-6f) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 12; ++j) {
+            const int idx = tid + j * K1_THREADS;
+            reinterpret_cast<uint4 *>(sm + K1_RAW)[idx] = buf[j];
         }
     }
+    // meanwhile: beta and this thread's g column (rows of its half), batched loads
+    const int d = tid & (kD - 1), half = tid >> 7, r0 = half * 32;
+    float b[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int r = r0 + j;
+        b[j] = (r < L) ? g[((size_t)(t0 + r) * H + h) * kD + d] : 0.f;
+    }
     if (tid < kC) bs[tid] = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    // in-half inclusive cumsum of g; the upper half adds the lower half's total
+#pragma unroll
+    for (int j = 1; j < 32; ++j) b[j] += b[j - 1];
+    if (half == 0) bhalf[d] = b[31];
+    const bool loaded = true;
+    __syncthreads();
+    if (half == 1) {
+        const float p = bhalf[d];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) b[j] += p;
+        blast[d] = b[31];
+    }
+
+    // 1. row norms of q and k (warp w: rows 8w..8w+7) from shared memory; the
+    //    eight rows' reductions are interleaved
+    {
+        float sq[8], sk[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+            const int r = warp * 8 + rr;
+            sq[rr] = sk[rr] = 0.f;
+            if (r < L) {
+                const uint2 qa = *reinterpret_cast<const uint2 *>(rawq + r * kD + lane * 4);
+                const uint2 ka = *reinterpret_cast<const uint2 *>(rawk + r * kD + lane * 4);
+                float a0 = bf_lo(qa.x), a1 = bf_hi(qa.x), a2 = bf_lo(qa.y), a3 = bf_hi(qa.y);
+                float c0 = bf_lo(ka.x), c1 = bf_hi(ka.x), c2 = bf_lo(ka.y), c3 = bf_hi(ka.y);
+                sq[rr] = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+                sk[rr] = c0 * c0 + c1 * c1 + c2 * c2 + c3 * c3;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
+                sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
+            }
+        if (lane < 8) {
+            const int r = warp * 8 + lane;
+            float vq = sq[0], vk = sk[0];
+#pragma unroll
+            for (int rr = 1; rr < 8; ++rr)
+                if (lane == rr) { vq = sq[rr]; vk = sk[rr]; }
+            rq[r] = r < L ? rsqrtf(vq + 1e-6f) : 0.f;
+            rk[r] = r < L ? rsqrtf(vk + 1e-6f) : 0.f;
+        }
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = tmem_sh;
 
-    // 2. thread d = tid: cumulative log-decay, then the decayed q/k operands
-    const int d = tid;
-    float b[kC];
-    {
-        float acc = 0.f;
-#pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            if (r < L) acc += g[((size_t)(t0 + r) * H + h) * kD + d];
-            b[r] = acc;
-        }
-    }
-    const float bl = b[kC - 1];
+    // 2. decayed q/k in operand layouts (thread: channel d, rows r0..r0+31)
+    const float bl = blast[d];
     const float gl = __expf(bl);
-    reinterpret_cast<float *>(rec + REC_G)[d] = gl;
+    if (half == 0) reinterpret_cast<float *>(rec + REC_G)[d] = gl;
 #pragma unroll
-    for (int r8 = 0; r8 < kC; r8 += 8) {
-        uint32_t pkg[4], pv[4], pke[4];
+    for (int j8 = 0; j8 < 32; j8 += 8) {
+        float kgv[8], vv8[8], kev[8];
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            float kgv[2], vv2[2], kev[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int r = r8 + j + u;
-                float qv = 0.f, kv = 0.f, vv = 0.f;
-                if (r < L) {
-                    const size_t base = ((size_t)(t0 + r) * H + h) * kD + d;
-                    qv = __bfloat162float(q[base]);
-                    kv = __bfloat162float(k[base]);
-                    vv = __bfloat162float(v[base]);
-                }
-                const float qh = qv * rq[r], kh = kv * rk[r];
-                const float e = __expf(b[r]), ei = __expf(-b[r]);
-                const float Kg = kh * e, Qg = qh * e, Kd = kh * ei;
-                *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kg);
-                *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(64 + r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Qg);
-                *reinterpret_cast<float *>(sm + K1_KD + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kd);
-                kgv[u] = Kg;
-                vv2[u] = vv;
-                kev[u] = Kd * gl;   // kh * exp(b_last - b_r)
-            }
-            pkg[j / 2] = pack_f16x2(kgv[0], kgv[1]);
-            pv[j / 2] = pack_f16x2(vv2[0], vv2[1]);
-            pke[j / 2] = pack_f16x2(kev[0], kev[1]);
+        for (int u = 0; u < 8; ++u) {
+            const int j = j8 + u, r = r0 + j;
+            const bool valid = r < L;
+            const float qv = valid ? __bfloat162float(rawq[r * kD + d]) : 0.f;
+            const float kv = valid ? __bfloat162float(rawk[r * kD + d]) : 0.f;
+            const float vv = valid ? __bfloat162float(rawv[r * kD + d]) : 0.f;
+            const float qh = qv * rq[r], kh = kv * rk[r];
+            const float e = __expf(b[j]), ei = __expf(-b[j]);
+            const float Kg = kh * e, Qg = qh * e, Kd = kh * ei;
+            *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kg);
+            *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(64 + r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Qg);
+            *reinterpret_cast<float *>(sm + K1_KD + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kd);
+            kgv[u] = Kg;
+            vv8[u] = vv;
+            kev[u] = Kd * gl;   // kh * exp(b_last - b_r)
         }
-        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d, r8, LBO_KIN, SBO_K64)) = make_uint4(pkg[0], pkg[1], pkg[2], pkg[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d, r8, LBO_KIN, SBO_K64)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d, r8, LBO_KIN, SBO_K64)) = make_uint4(pke[0], pke[1], pke[2], pke[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(kgv);
+        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(vv8);
+        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(kev);
     }
     fence_async_smem();
     fence_before_sync();
@@ -237,7 +293,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     // 3. G = [Kg; Qg] Kd^T  (tf32, M = 128, N = 64, K = 128: 16 instructions of K = 8)
-    if (tid == 0) {
+    if (tid == 0 && loaded) {
         const uint32_t idesc = idesc_tf32(128, 64);
         const uint32_t a0 = smem_u32(sm + K1_GA), b0 = smem_u32(sm + K1_KD);
 #pragma unroll
@@ -246,99 +302,114 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                      make_desc(b0 + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO), idesc, ks > 0);
         mma_commit(&mbar);
     }
-    bool ok = mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    bool ok = loaded && mbar_wait_bounded(&mbar, 0, kWaitLimit);
     fence_after_sync();
     __syncthreads();   // every thread has seen G complete: the first-phase region may be reused
 
-    // 4. read G: warps 0-1 hold rows of Kg Kd^T (-> L), warps 2-3 rows of Qg Kd^T (-> Mc)
+    // 4. read G: lane quarter q4 = warp & 3 holds rows 32 q4 .. +31; warps w and
+    //    w + 4 take columns [0, 32) and [32, 64).  Rows < 64: Kg Kd^T -> L;
+    //    rows >= 64: Qg Kd^T -> Mc.
+    const int q4 = warp & 3, ch = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int row = 32 * q4 + lane;
     float *Lm = reinterpret_cast<float *>(sm + K1_LM);
     float *Tm = reinterpret_cast<float *>(sm + K1_TM);
     float *Xs = reinterpret_cast<float *>(sm + K1_XS);
     if (ok) {
-        float gv[64];
-#pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-            float t16[16];
-            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + T1_G + c, t16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) gv[c + i] = t16[i];
-        }
-        if (warp < 2) {
-            const int r = tid;
+        float gv[32];
+        tmem_ld16(tm + lane_base + T1_G + 32 * ch, *reinterpret_cast<float(*)[16]>(gv));
+        tmem_ld16(tm + lane_base + T1_G + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(gv + 16));
+        tmem_ld_wait();
+        if (row < 64) {
+            const int r = row;
             const float br = bs[r];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) Lm[r * 65 + i] = (i < r) ? br * gv[i] : 0.f;
+            for (int i = 0; i < 32; ++i) {
+                const int col = 32 * ch + i;
+                Lm[r * K1_P + col] = (col < r) ? br * gv[i] : 0.f;
+            }
         } else {
-            const int r = tid - 64;
+            const int r = row - 64;
 #pragma unroll
-            for (int i8 = 0; i8 < 64; i8 += 8) {
-                uint32_t p[4];
+            for (int i8 = 0; i8 < 32; i8 += 8) {
+                float m8[8];
 #pragma unroll
-                for (int j = 0; j < 8; j += 2)
-                    p[j / 2] = pack_f16x2((i8 + j <= r) ? gv[i8 + j] : 0.f,
-                                          (i8 + j + 1 <= r) ? gv[i8 + j + 1] : 0.f);
-                const uint4 val = make_uint4(p[0], p[1], p[2], p[3]);
-                *reinterpret_cast<uint4 *>(sm + K1_MC + kmaj_off(r, i8, LBO_KIN, SBO_K64)) = val;
-                *reinterpret_cast<uint4 *>(rec + REC_M + kmaj_off(r, i8, LBO_KIN, SBO_K64)) = val;
+                for (int j = 0; j < 8; ++j) m8[j] = (32 * ch + i8 + j <= r) ? gv[i8 + j] : 0.f;
+                const uint4 val = pack_f16x8(m8);
+                *reinterpret_cast<uint4 *>(sm + K1_MC + kmaj_off(r, 32 * ch + i8, LBO_KIN, SBO_K64)) = val;
             }
         }
     }
     __syncthreads();
 
     // 5. T = (I + L)^-1, blocked by 16: diagonal blocks by forward substitution,
-    //    then T_ab = -T_aa * sum_{k=b}^{a-1} L_ak T_kb by block distance.
+    //    then T_ab = -T_aa * sum_{k=b}^{a-1} L_ak T_kb by block distance.  Each
+    //    thread of the block products computes a 1 x 4 strip (float4 rows).
     if (tid < 64) {
         const int blk = tid >> 4, c = tid & 15, col = 16 * blk + c;
+        float tcol[16];
+#pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * blk + rr;
             float x = (rr == c) ? 1.f : 0.f;
-            for (int i = col; i < r; ++i) x -= Lm[r * 65 + i] * Tm[i * 65 + col];
-            Tm[r * 65 + col] = (rr >= c) ? x : 0.f;
+#pragma unroll
+            for (int ii = 0; ii < rr; ++ii)
+                if (ii >= c) x -= Lm[r * K1_P + 16 * blk + ii] * tcol[ii];
+            tcol[rr] = (rr >= c) ? x : 0.f;
+            Tm[r * K1_P + col] = tcol[rr];
         }
     } else {
-        for (int idx = tid - 64; idx < 64 * 64; idx += 64) {
-            const int r = idx >> 6, j = idx & 63;
-            if ((j >> 4) > (r >> 4)) Tm[r * 65 + j] = 0.f;
+        for (int idx = tid - 64; idx < 64 * 16; idx += K1_THREADS - 64) {
+            const int r = idx >> 4, j4 = (idx & 15) * 4;
+            if ((j4 >> 4) > (r >> 4))
+                *reinterpret_cast<float4 *>(Tm + r * K1_P + j4) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     __syncthreads();
     for (int lvl = 1; lvl < 4; ++lvl) {
         const int nb = 4 - lvl;
-        for (int idx = tid; idx < nb * 256; idx += 128) {
-            const int bb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, a = bb + lvl;
-            float s = 0.f;
-            for (int kk = bb; kk < a; ++kk)
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    s += Lm[(16 * a + i) * 65 + 16 * kk + m] * Tm[(16 * kk + m) * 65 + 16 * bb + j];
-            Xs[(bb * 16 + i) * 17 + j] = s;
+        // X_ab = sum_{k=b}^{a-1} L_ak T_kb   (a = b + lvl), strip (i, 4 j4 .. 4 j4 + 3)
+        if (tid < nb * 64) {
+            const int bb = tid >> 6, i = (tid >> 2) & 15, j4 = (tid & 3) * 4, a = bb + lvl;
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *lrow = Lm + (16 * a + i) * K1_P;
+            for (int m = 16 * bb; m < 16 * a; ++m) {
+                const float l = lrow[m];
+                const float4 t = *reinterpret_cast<const float4 *>(Tm + m * K1_P + 16 * bb + j4);
+                s4.x += l * t.x; s4.y += l * t.y; s4.z += l * t.z; s4.w += l * t.w;
+            }
+            *reinterpret_cast<float4 *>(Xs + (bb * 16 + i) * 16 + j4) = s4;
         }
         __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += 128) {
-            const int bb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, a = bb + lvl;
-            float s = 0.f;
+        // T_ab = -T_aa X_ab
+        if (tid < nb * 64) {
+            const int bb = tid >> 6, i = (tid >> 2) & 15, j4 = (tid & 3) * 4, a = bb + lvl;
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *trow = Tm + (16 * a + i) * K1_P + 16 * a;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) s += Tm[(16 * a + i) * 65 + 16 * a + m] * Xs[(bb * 16 + m) * 17 + j];
-            Tm[(16 * a + i) * 65 + 16 * bb + j] = -s;
+            for (int m = 0; m < 16; ++m) {
+                const float tv = trow[m];
+                const float4 x = *reinterpret_cast<const float4 *>(Xs + (bb * 16 + m) * 16 + j4);
+                s4.x += tv * x.x; s4.y += tv * x.y; s4.z += tv * x.z; s4.w += tv * x.w;
+            }
+            *reinterpret_cast<float4 *>(Tm + (16 * a + i) * K1_P + 16 * bb + j4) =
+                make_float4(-s4.x, -s4.y, -s4.z, -s4.w);
         }
         __syncthreads();
     }
 
-    // 6. T diag(beta) -> f16 operand (rows r, K = i)
+    // 6. T diag(beta) -> f16 operand (rows r, K = i): thread -> row tid/4, 16 columns
     {
-        const int r = tid >> 1, i0 = (tid & 1) * 32;
+        const int r = tid >> 2, i0 = (tid & 3) * 16;
 #pragma unroll
-        for (int i8 = 0; i8 < 32; i8 += 8) {
-            uint32_t p[4];
+        for (int i8 = 0; i8 < 16; i8 += 8) {
+            float t8[8];
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
+            for (int j = 0; j < 8; ++j) {
                 const int i = i0 + i8 + j;
-                p[j / 2] = pack_f16x2(i <= r ? Tm[r * 65 + i] * bs[i] : 0.f,
-                                      i + 1 <= r ? Tm[r * 65 + i + 1] * bs[i + 1] : 0.f);
+                t8[j] = i <= r ? Tm[r * K1_P + i] * bs[i] : 0.f;
             }
-            *reinterpret_cast<uint4 *>(sm + K1_TB + kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64)) =
-                make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4 *>(sm + K1_TB + kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64)) = pack_f16x8(t8);
         }
     }
     fence_async_smem();
@@ -361,22 +432,20 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
     fence_after_sync();
 
-    // 8. Wk^T -> smem operand (rows d, K = r); Uv^T -> record (rows e, K = r)
+    // 8. Wk^T and Uv^T -> smem operands (rows d / e, K = r).
+    //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < 32; c += 16) {
             float w[16], u[16];
-            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + T1_W1 + c, w);
-            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + T1_W2 + c, u);
+            tmem_ld16(tm + lane_base + T1_W1 + 32 * ch + c, w);
+            tmem_ld16(tm + lane_base + T1_W2 + 32 * ch + c, u);
             tmem_ld_wait();
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8) {
-                *reinterpret_cast<uint4 *>(sm + K1_WKT + kmaj_off(tid, c + h8, LBO_KIN, SBO_K64)) =
-                    make_uint4(pack_f16x2(w[h8], w[h8 + 1]), pack_f16x2(w[h8 + 2], w[h8 + 3]),
-                               pack_f16x2(w[h8 + 4], w[h8 + 5]), pack_f16x2(w[h8 + 6], w[h8 + 7]));
-                *reinterpret_cast<uint4 *>(rec + REC_UVT + kmaj_off(tid, c + h8, LBO_KIN, SBO_K64)) =
-                    make_uint4(pack_f16x2(u[h8], u[h8 + 1]), pack_f16x2(u[h8 + 2], u[h8 + 3]),
-                               pack_f16x2(u[h8 + 4], u[h8 + 5]), pack_f16x2(u[h8 + 6], u[h8 + 7]));
+                const int kk = 32 * ch + c + h8;
+                *reinterpret_cast<uint4 *>(sm + K1_WKT + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(w + h8);
+                *reinterpret_cast<uint4 *>(sm + K1_UVT + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(u + h8);
             }
         }
     }
@@ -401,46 +470,82 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     if (ok) {
-        // 10. A' = -(Ke^T Wk) -> record (rows d, K = d')
+        // 10. A' = -(Ke^T Wk) -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
 #pragma unroll
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = 0; c < 64; c += 16) {
             float a[16];
-            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + T1_AP + c, a);
+            tmem_ld16(tm + lane_base + T1_AP + 64 * ch + c, a);
             tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a[j] = -a[j];
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8)
-                *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(tid, c + h8, LBO_KIN, SBO_K128)) =
-                    make_uint4(pack_f16x2(-a[h8], -a[h8 + 1]), pack_f16x2(-a[h8 + 2], -a[h8 + 3]),
-                               pack_f16x2(-a[h8 + 4], -a[h8 + 5]), pack_f16x2(-a[h8 + 6], -a[h8 + 7]));
+                *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
+                    pack_f16x8(a + h8);
         }
-        // 11. Q' = Qg - Mc Wk: the M = 64 accumulator puts row r = 16 w + l in lane 32 w + l (l < 16)
-        const int r = 16 * warp + lane;
+        // 11. Q' = Qg - Mc Wk: the M = 64 accumulator puts row r = 16 q4 + l in lane 32 q4 + l (l < 16)
+        const int r = 16 * q4 + lane;
 #pragma unroll
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = 0; c < 64; c += 16) {
             float a[16];
-            tmem_ld16(tm + ((uint32_t)(32 * warp) << 16) + T1_QP + c, a);
+            tmem_ld16(tm + lane_base + T1_QP + 64 * ch + c, a);
             tmem_ld_wait();
             if (lane < 16) {
-                float qg[16];
+                float qd[16];
 #pragma unroll
                 for (int j4 = 0; j4 < 16; j4 += 4) {
                     const float4 t = *reinterpret_cast<const float4 *>(
-                        sm + K1_GA + kmaj_off4(64 + r, c + j4, K1_F32_LBO, K1_F32_SBO));
-                    qg[j4] = t.x; qg[j4 + 1] = t.y; qg[j4 + 2] = t.z; qg[j4 + 3] = t.w;
+                        sm + K1_GA + kmaj_off4(64 + r, 64 * ch + c + j4, K1_F32_LBO, K1_F32_SBO));
+                    qd[j4] = t.x - a[j4];
+                    qd[j4 + 1] = t.y - a[j4 + 1];
+                    qd[j4 + 2] = t.z - a[j4 + 2];
+                    qd[j4 + 3] = t.w - a[j4 + 3];
                 }
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8)
-                    *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, c + h8, LBO_KIN, SBO_K128)) =
-                        make_uint4(pack_f16x2(qg[h8] - a[h8], qg[h8 + 1] - a[h8 + 1]),
-                                   pack_f16x2(qg[h8 + 2] - a[h8 + 2], qg[h8 + 3] - a[h8 + 3]),
-                                   pack_f16x2(qg[h8 + 4] - a[h8 + 4], qg[h8 + 5] - a[h8 + 5]),
-                                   pack_f16x2(qg[h8 + 6] - a[h8 + 6], qg[h8 + 7] - a[h8 + 7]));
+                    *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
+                        pack_f16x8(qd + h8);
             }
         }
-        // 12. Ke^T -> record (same layout as in shared memory)
-        const uint4 *src = reinterpret_cast<const uint4 *>(sm + K1_KET);
-        uint4 *dst = reinterpret_cast<uint4 *>(rec + REC_KET);
-        for (int i = tid; i < 16384 / 16; i += 128) dst[i] = src[i];
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // 12. Bc^T = Uv^T Ke (M = 128, N = 128, K = 64); Ol^T = Uv^T Mc^T (M = 128, N = 64, K = 64)
+    if (tid == 0 && ok) {
+        const uint32_t auv = smem_u32(sm + K1_UVT), bke = smem_u32(sm + K1_KET), bmc = smem_u32(sm + K1_MC);
+        const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(128, 64);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = make_desc(auv + ks * 256, LBO_KIN, SBO_K64);
+            mma_f16(tm + T1_BC, ad, make_desc(bke + ks * 256, LBO_KIN, SBO_K64), id128, ks > 0);
+            mma_f16(tm + T1_OL, ad, make_desc(bmc + ks * 256, LBO_KIN, SBO_K64), id64, ks > 0);
+        }
+        mma_commit(&mbar);
+    }
+    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    fence_after_sync();
+    if (ok) {
+        // row e of Bc^T: columns [64 ch, 64 ch + 64); row e of Ol^T: columns [32 ch, 32 ch + 32)
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+            float a[16];
+            tmem_ld16(tm + lane_base + T1_BC + 64 * ch + c, a);
+            tmem_ld_wait();
+            uint4 *dst = reinterpret_cast<uint4 *>(rec + REC_BC + row * 256 + (64 * ch + c) * 2);
+            dst[0] = pack_f16x8(a);
+            dst[1] = pack_f16x8(a + 8);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            float a[16];
+            tmem_ld16(tm + lane_base + T1_OL + 32 * ch + c, a);
+            tmem_ld_wait();
+            uint4 *dst = reinterpret_cast<uint4 *>(rec + REC_OL + row * 128 + (32 * ch + c) * 2);
+            dst[0] = pack_f16x8(a);
+            dst[1] = pack_f16x8(a + 8);
+        }
     } else if (tid == 0) {
         record_timeout(st);
     }
@@ -452,32 +557,59 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 }
 
 // ============================================================ K2
-// One CTA per (sequence, head).  Warps 0-3: state / epilogue (thread e owns
-// value column e of S, i.e. row e of S^T, in fp32 registers); warp 4: bulk
-// copies of the K1 records (two stages); warp 5: tensor-core issue.
-constexpr uint32_t K2_STAGE0 = 0;
-constexpr uint32_t K2_SOP = 2 * REC_BYTES;            // f16 S^T: rows e x K = d (128 x 128)
-constexpr uint32_t K2_SMEM = K2_SOP + 32768;
-// TMEM columns (512 allocated): S accumulators (2 x 128), O accumulators (2 x 64)
-constexpr uint32_t T2_S0 = 0, T2_O0 = 256;
+// One CTA per (sequence, head), serial over the sequence's chunks.
+//   warps 0-7 : state.  Thread (e = 32 (w & 3) + lane, half = w >> 2) keeps
+//               S[d][e] for d in [64 half, 64 half + 64) in fp32 registers.
+//   warp 8    : copies the records' tensor-core part into a 3-stage ring.
+//   warp 9    : issues the MMAs.
+// Per chunk the state product A' S runs as two independent K-halves
+// (P0: d' < 64, P1: d' >= 64), each fed by the half of the state threads
+// that writes those rows of S^T, so the serial chain per chunk is one
+// 4-instruction MMA group.  O = Q' S is split the same way (Oa, Ob) and
+// double-buffered; it is off the serial path.
+constexpr int K2_STAGES = 2;
+constexpr uint32_t K2_SOP = K2_STAGES * REC_SMEM;      // f16 S^T [2][rows e x K = d]
+constexpr uint32_t K2_OST = K2_SOP + 2 * 32768;   // bf16 output tile [2][64 rows][128], staged for coalesced stores
+constexpr uint32_t K2_SMEM = K2_OST + 2 * 16384;
+constexpr int K2_STATE_THREADS = 256;
+constexpr int K2_THREADS = K2_STATE_THREADS + 64;
+static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
+// TMEM columns (512 allocated)
+constexpr uint32_t T2_P0 = 0, T2_P1 = 128, T2_OA = 256, T2_OB = 320;   // O buffers at +0 / +128
+constexpr int kL2Ahead = 4;   // records prefetched into L2 ahead of the one being copied
 
-__device__ __forceinline__ void write_sop(uint8_t *sop, int e, const float (&S)[kD])
+__device__ __forceinline__ void write_sop_half(uint8_t *sop, int e, int half, const float (&S)[64])
 {
 #pragma unroll
-    for (int d8 = 0; d8 < kD; d8 += 8)
-        *reinterpret_cast<uint4 *>(sop + kmaj_off(e, d8, LBO_KIN, SBO_K128)) =
-            make_uint4(pack_f16x2(S[d8], S[d8 + 1]), pack_f16x2(S[d8 + 2], S[d8 + 3]),
-                       pack_f16x2(S[d8 + 4], S[d8 + 5]), pack_f16x2(S[d8 + 6], S[d8 + 7]));
+    for (int d8 = 0; d8 < 64; d8 += 8)
+        *reinterpret_cast<uint4 *>(sop + kmaj_off(e, 64 * half + d8, LBO_KIN, SBO_K128)) = pack_f16x8(S + d8);
 }
 
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ void ld_rec_bc(const uint8_t *rec, int e, int half, uint4 (&bc)[8])
+{
+    const uint4 *pb = reinterpret_cast<const uint4 *>(rec + REC_BC + e * 256 + 128 * half);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bc[j] = __ldg(pb + j);
+}
+
+__device__ __forceinline__ void ld_rec_ol(const uint8_t *rec, int e, int half, uint4 (&ol)[4])
+{
+    const uint4 *po = reinterpret_cast<const uint4 *>(rec + REC_OL + e * 128 + 64 * half);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ol[j] = __ldg(po + j);
+}
+
+__device__ __forceinline__ float h_lo(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u >> 16))); }
+
+__global__ void __maxnreg__(168)
 k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ handoff, bf16 *__restrict__ out,
              float *__restrict__ final_state, float *__restrict__ ckpts, int stride,
              int64_t capacity, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[2], empty[2], sdone[2], ofree[2], sready;
+    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2], odone[2], ofree[2], ostaged[2];
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -487,13 +619,18 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
 
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < K2_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 128);   // MMA commit + every state thread
-            mbar_init(&sdone[s], 1);
-            mbar_init(&ofree[s], 128);
+            mbar_init(&empty[s], 1 + K2_STATE_THREADS);   // MMA commit + every state thread
         }
-        mbar_init(&sready, 128);
+        mbar_init(&sdone, 1);
+        mbar_init(&pread, K2_STATE_THREADS);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&sready[j], K2_STATE_THREADS / 2);
+            mbar_init(&odone[j], 1);
+            mbar_init(&ofree[j], K2_STATE_THREADS);
+            mbar_init(&ostaged[j], K2_STATE_THREADS);
+        }
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -507,59 +644,105 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const uint32_t tm = tmem_sh;
     volatile int *abort_v = &abort_flag;
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ---------------------------------------------------------- state role
-        const int e = tid;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        float S[kD];
+        const int q4 = warp & 3, half = warp >> 2;
+        const int e = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        float S[64];
         const size_t sbase = ((size_t)n * H + h) * kD * kD;
 #pragma unroll
-        for (int d = 0; d < kD; ++d) S[d] = init_state ? init_state[sbase + (size_t)d * kD + e] : 0.f;
-        write_sop(sm + K2_SOP, e, S);
+        for (int j = 0; j < 64; ++j)
+            S[j] = init_state ? init_state[sbase + (size_t)(64 * half + j) * kD + e] : 0.f;
+        write_sop_half(sm + K2_SOP, e, half, S);
         fence_async_smem();
-        mbar_arrive(&sready);
+        mbar_arrive(&sready[half]);
+        uint4 bc[8];
+        if (nch > 0) ld_rec_bc(handoff + ((size_t)c_begin * H + h) * REC_BYTES, e, half, bc);
         bool alive = true;
-        for (int c = 0; c < nch && alive; ++c) {
-            const int s = c & 1;
-            if (!wait_or_abort(&sdone[s], (c >> 1) & 1, abort_v)) {
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % K2_STAGES, ob = c & 1;
+            // the stage's copy has landed (the MMA thread saw it too; waiting here
+            // makes gamma's bytes visible to this thread as well)
+            if (!wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v) ||
+                !wait_or_abort(&sdone, c & 1, abort_v)) {
                 alive = false;
                 break;
             }
             fence_after_sync();
-            const float *gam = reinterpret_cast<const float *>(sm + K2_STAGE0 + s * REC_BYTES + REC_G);
+            // S = gamma * S + P0 + P1 + Bc, 16 columns at a time (keeps registers low)
+            const float *gam = reinterpret_cast<const float *>(sm + s * REC_SMEM + REC_G) + 64 * half;
 #pragma unroll
-            for (int c32 = 0; c32 < kD; c32 += 32) {
-                float a0[16], a1[16];
-                tmem_ld16(tm + lane_base + T2_S0 + s * 128 + c32, a0);
-                tmem_ld16(tm + lane_base + T2_S0 + s * 128 + c32 + 16, a1);
+            for (int c16 = 0; c16 < 64; c16 += 16) {
+                float p0[16], p1[16];
+                tmem_ld16(tm + lane_base + T2_P0 + 64 * half + c16, p0);
+                tmem_ld16(tm + lane_base + T2_P1 + 64 * half + c16, p1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    S[c32 + j] = gam[c32 + j] * S[c32 + j] + a0[j];
-                    S[c32 + 16 + j] = gam[c32 + 16 + j] * S[c32 + 16 + j] + a1[j];
+                for (int j8 = 0; j8 < 16; j8 += 8) {
+                    const uint4 b4 = bc[(c16 + j8) / 8];
+                    const uint32_t w4[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int jl = j8 + 2 * u, j = c16 + jl;
+                        S[j] = gam[j] * S[j] + p0[jl] + p1[jl] + h_lo(w4[u]);
+                        S[j + 1] = gam[j + 1] * S[j + 1] + p0[jl + 1] + p1[jl + 1] + h_hi(w4[u]);
+                    }
                 }
             }
-            write_sop(sm + K2_SOP, e, S);
-            fence_async_smem();
             fence_before_sync();
-            mbar_arrive(&sready);
-            mbar_arrive(&empty[s]);            // this thread is done with the stage's gamma
+            mbar_arrive(&pread);
+            write_sop_half(sm + K2_SOP + ((c + 1) & 1) * 32768, e, half, S);
+            fence_async_smem();
+            mbar_arrive(&sready[half]);
+            mbar_arrive(&empty[s]);            // done with the stage's gamma
 
-            // output rows of this chunk
+            // output rows [32 half, 32 half + 32) of this chunk: O = Oa + Ob + Ol
+            uint4 ol[4];
+            ld_rec_ol(handoff + ((size_t)(c_begin + c) * H + h) * REC_BYTES, e, half, ol);
+            if (!wait_or_abort(&odone[ob], (c >> 1) & 1, abort_v)) { alive = false; break; }
+            fence_after_sync();
             const int t0 = seq_t0 + c * kC;
             const int L = min(kC, seq_t1 - t0);
 #pragma unroll
-            for (int c16 = 0; c16 < kC; c16 += 16) {
-                float o[16];
-                tmem_ld16(tm + lane_base + T2_O0 + s * 64 + c16, o);
+            for (int c16 = 0; c16 < 32; c16 += 16) {
+                float oa[16], obv[16];
+                tmem_ld16(tm + lane_base + T2_OA + 128 * ob + 32 * half + c16, oa);
+                tmem_ld16(tm + lane_base + T2_OB + 128 * ob + 32 * half + c16, obv);
                 tmem_ld_wait();
+                if (c16 == 16) {
+                    fence_before_sync();
+                    mbar_arrive(&ofree[ob]);
+                }
+                bf16 *ost = reinterpret_cast<bf16 *>(sm + K2_OST + ob * 16384);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c16 + j < L) out[((size_t)(t0 + c16 + j) * H + h) * kD + e] = __float2bfloat16_rn(o[j]);
+                for (int j8 = 0; j8 < 16; j8 += 8) {
+                    const uint4 o4 = ol[(c16 + j8) / 8];
+                    const uint32_t w4[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int jl = j8 + 2 * u;
+                        const int r = 32 * half + c16 + jl;
+                        ost[r * kD + e] = __float2bfloat16_rn(oa[jl] + obv[jl] + h_lo(w4[u]));
+                        ost[(r + 1) * kD + e] = __float2bfloat16_rn(oa[jl + 1] + obv[jl + 1] + h_hi(w4[u]));
+                    }
+                }
             }
-            fence_before_sync();
-            mbar_arrive(&ofree[s]);
-
+            // every state thread has staged its part: write the valid rows with 16-byte stores
+            mbar_arrive(&ostaged[ob]);
+            if (!wait_or_abort(&ostaged[ob], (c >> 1) & 1, abort_v)) { alive = false; break; }
+            {
+                const uint4 *ost4 = reinterpret_cast<const uint4 *>(sm + K2_OST + ob * 16384);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int idx = tid + j * K2_STATE_THREADS;     // 16-byte chunk of the tile
+                    const int r = idx >> 4, c16b = idx & 15;
+                    if (r < L)
+                        reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * kD)[c16b] = ost4[idx];
+                }
+            }
+            // the next chunk's state-independent terms, read while this one's tail runs
+            if (c + 1 < nch) ld_rec_bc(handoff + ((size_t)(c_begin + c + 1) * H + h) * REC_BYTES, e, half, bc);
             // checkpoint after every `stride` tokens of the sequence
             const int done = c * kC + L;
             if (stride > 0 && ckpts && L == kC && done % stride == 0) {
@@ -567,74 +750,79 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 if (slot < capacity) {
                     float *dst = ckpts + ((size_t)slot * H + h) * kD * kD + e;
 #pragma unroll
-                    for (int d = 0; d < kD; ++d) dst[(size_t)d * kD] = S[d];
+                    for (int j = 0; j < 64; ++j) dst[(size_t)(64 * half + j) * kD] = S[j];
                 }
             }
         }
         if (!alive) {
             *abort_v = 1;
-            if (tid == 0) record_timeout(st);
+            if (lane == 0) record_timeout(st);
         } else if (final_state) {
 #pragma unroll
-            for (int d = 0; d < kD; ++d) final_state[sbase + (size_t)d * kD + e] = S[d];
+            for (int j = 0; j < 64; ++j) final_state[sbase + (size_t)(64 * half + j) * kD + e] = S[j];
         }
-    } else if (warp == 4) {
-        // ---------------------------------------------------------- bulk-copy role
+    } else if (warp == 8) {
+        // ---------------------------------------------------------- copy role
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !wait_or_abort(&empty[s], ((c - 2) >> 1) & 1, abort_v)) {
+                const int s = c % K2_STAGES;
+                if (c >= K2_STAGES && !wait_or_abort(&empty[s], ((c / K2_STAGES) - 1) & 1, abort_v)) {
                     *abort_v = 1;
                     record_timeout(st);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], REC_BYTES);
-                bulk_g2s(sm + K2_STAGE0 + s * REC_BYTES,
-                         handoff + ((size_t)(c_begin + c) * H + h) * REC_BYTES, REC_BYTES, &full[s]);
+                if (c == 0)
+                    for (int a = 1; a < min(nch, 1 + kL2Ahead); ++a)
+                        prefetch_l2(handoff + ((size_t)(c_begin + a) * H + h) * REC_BYTES, REC_BYTES);
+                else if (c + kL2Ahead < nch)
+                    prefetch_l2(handoff + ((size_t)(c_begin + c + kL2Ahead) * H + h) * REC_BYTES, REC_BYTES);
+                mbar_arrive_expect_tx(&full[s], REC_SMEM);
+                bulk_g2s(sm + s * REC_SMEM, handoff + ((size_t)(c_begin + c) * H + h) * REC_BYTES, REC_SMEM,
+                         &full[s]);
                 issued = c + 1;
             }
-            // Never leave a copy in flight: wait for the last (up to two) copies.
-            for (int c = max(0, issued - 2); c < issued; ++c)
-                mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, kWaitLimit);
+            // Never leave a copy in flight.
+            for (int c = max(0, issued - K2_STAGES); c < issued; ++c)
+                mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kWaitLimit);
         }
     } else {
         // ---------------------------------------------------------- MMA role
         if (lane == 0) {
-            const uint32_t sop = smem_u32(sm + K2_SOP);
             const uint32_t id_s = idesc_f16(128, 128), id_o = idesc_f16(128, 64);
             for (int c = 0; c < nch; ++c) {
-                const int s = c & 1;
-                if (!wait_or_abort(&full[s], (c >> 1) & 1, abort_v) ||
-                    (c >= 2 && !wait_or_abort(&ofree[s], ((c - 2) >> 1) & 1, abort_v))) {
+                const int s = c % K2_STAGES, ob = c & 1;
+                const uint32_t stg = smem_u32(sm + s * REC_SMEM);
+                const uint32_t sop = smem_u32(sm + K2_SOP + (c & 1) * 32768);
+                bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v);
+                okw = okw && (c == 0 || wait_or_abort(&pread, (c - 1) & 1, abort_v));
+                // P0 = S^T[:, 0:64] A'[:, 0:64]^T once the first half of S^T is written
+                okw = okw && wait_or_abort(&sready[0], c & 1, abort_v);
+                if (!okw) { *abort_v = 1; record_timeout(st); break; }
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tm + T2_P0, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, ks > 0);
+                if (!wait_or_abort(&sready[1], c & 1, abort_v)) { *abort_v = 1; record_timeout(st); break; }
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 4; ks < 8; ++ks)
+                    mma_f16(tm + T2_P1, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, ks > 4);
+                mma_commit(&sdone);
+                // O = Q' S in two K-halves, into buffer ob once its previous contents were read
+                if (c >= 2 && !wait_or_abort(&ofree[ob], ((c - 2) >> 1) & 1, abort_v)) {
                     *abort_v = 1;
                     record_timeout(st);
                     break;
                 }
                 fence_after_sync();
-                const uint32_t stg = smem_u32(sm + K2_STAGE0 + s * REC_BYTES);
-                const uint32_t dS = tm + T2_S0 + s * 128, dO = tm + T2_O0 + s * 64;
-                // state-independent part: Ke^T Uv -> S acc, Mc Uv -> O acc
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t a = make_desc(stg + REC_UVT + ks * 256, LBO_KIN, SBO_K64);
-                    mma_f16(dS, a, make_desc(stg + REC_KET + ks * 256, LBO_KIN, SBO_K64), id_s, ks > 0);
-                    mma_f16(dO, a, make_desc(stg + REC_M + ks * 256, LBO_KIN, SBO_K64), id_o, ks > 0);
-                }
-                if (!wait_or_abort(&sready, c & 1, abort_v)) {
-                    *abort_v = 1;
-                    record_timeout(st);
-                    break;
-                }
-                fence_after_sync();
-                // state-dependent part: S acc += S^T A'^T, O acc += S^T Q'^T
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t a = make_desc(sop + ks * 256, LBO_KIN, SBO_K128);
-                    mma_f16(dS, a, make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, 1);
-                    mma_f16(dO, a, make_desc(stg + REC_QP + ks * 256, LBO_KIN, SBO_K128), id_o, 1);
-                }
-                mma_commit(&sdone[s]);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16(tm + (ks < 4 ? T2_OA : T2_OB) + 128 * ob, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_QP + ks * 256, LBO_KIN, SBO_K128), id_o, (ks & 3) > 0);
+                mma_commit(&odone[ob]);
                 mma_commit(&empty[s]);
             }
         }
@@ -650,24 +838,46 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
 
 size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
 
+namespace {
+thread_local char g_detail[256];
+
+// Records the attributes of a kernel whose launch failed (for the error message).
+template <typename F>
+void note_launch_failure(F *fn, const char *name, int threads, uint32_t dyn_smem)
+{
+    cudaFuncAttributes at{};
+    cudaFuncGetAttributes(&at, fn);
+    snprintf(g_detail, sizeof g_detail,
+             "%s: %d threads x %d registers (max %d threads per block), %zu B static + %u B dynamic smem",
+             name, threads, at.numRegs, at.maxThreadsPerBlock, at.sharedSizeBytes, dyn_smem);
+}
+}  // namespace
+
+const char *launch_failure_detail() { return g_detail; }
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a)
 {
     cudaError_t e;
+    g_detail[0] = 0;
     e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
     if (e != cudaSuccess) return e;
     if (a.max_chunks > 0) {
-        dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
-        k1_tc_kernel<<<g1, 128, K1_SMEM, a.stream>>>(
+        dim3 g1((unsigned)a.H, (unsigned)a.max_chunks);
+        k1_tc_kernel<<<g1, K1_THREADS, K1_SMEM, a.stream>>>(
             (const bf16 *)a.q, (const bf16 *)a.k, (const bf16 *)a.v, a.g, a.beta, a.N, a.H, a.tab,
             (uint8_t *)a.handoff, a.status);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
+            return e;
+        }
     }
-    k2_tc_kernel<<<(unsigned)((size_t)a.N * a.H), 192, K2_SMEM, a.stream>>>(
+    k2_tc_kernel<<<(unsigned)((size_t)a.N * a.H), K2_THREADS, K2_SMEM, a.stream>>>(
         a.init_state, a.N, a.H, a.tab, (const uint8_t *)a.handoff, (bf16 *)a.out, a.final_state,
         a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
+    return e;
 }
 
 }  // namespace kda
