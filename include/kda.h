@@ -146,6 +146,34 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
                       const float *beta, float *state, void *out, int32_t N, int32_t H,
                       int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream);
 
+/*
+ * kda_prefill without a workspace argument, for callers that cannot allocate
+ * device memory (a framework that owns every allocation, a runtime that
+ * forbids cudaMalloc after start-up).  The KDA pages have no counterpart of
+ * this entry point; it exists only for such callers.
+ *
+ * Arguments are those of kda_prefill minus the workspace.  The scratch is a
+ * fixed device array of KDA_NOALLOC_SCRATCH_BYTES built into the library:
+ * every GPU that loads the library keeps it resident until the process exits.
+ * A call whose kda_prefill_workspace_size() exceeds it returns
+ * KDA_ERR_UNSUPPORTED before any work is queued.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture begins.  All calls share the one array, which keeps the previous
+ * call's contents; the parts that must start at zero are cleared by each
+ * call.  Calls that can overlap on the GPU race on the array and must be
+ * ordered by the caller.  Device-detected conditions (malformed cu_seqlens,
+ * too few checkpoint slots) are not reported by this entry point: use
+ * kda_prefill and kda_prefill_status when they matter.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, const float *init_state,
+                               const int32_t *cu_seqlens, void *out, float *final_state,
+                               float *ckpts, const kda_prefill_desc *desc, kda_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *kda_last_error(void);
 

@@ -76,6 +76,29 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
 
 }  // namespace
 
+namespace kda {
+
+kda_status prefill_workspace_bytes(const kda_prefill_desc *desc, size_t *bytes)
+{
+    Layout L;
+    const kda_status s = check_desc(desc, &L);
+    if (s == KDA_OK) *bytes = L.total;
+    return s;
+}
+
+kda_status fail_with_message(kda_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_last_error(void) { return g_last_error.c_str(); }

@@ -77,6 +77,12 @@ inline bool use_tc_path(kda_dtype dtype, int D, int C)
     return dtype == KDA_DTYPE_BF16 && D == 128 && C == 64;
 }
 
+// Validates `desc` and returns the workspace bytes kda_prefill needs for it
+// (on error: the status, with the thread-local message set).
+kda_status prefill_workspace_bytes(const kda_prefill_desc *desc, size_t *bytes);
+// Sets the thread-local message that kda_last_error() returns; returns `s`.
+kda_status fail_with_message(kda_status s, const char *fmt, ...);
+
 cudaError_t launch_seq_table(const PrefillArgs &a);
 cudaError_t launch_prefill_simt(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a);

@@ -22,7 +22,10 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_status", "kda_decode",
-           "kda_last_error", "kda_version")
+           "kda_prefill_noalloc", "kda_last_error", "kda_version")
+
+# Size of the library's built-in scratch array used by kda_prefill_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class KDAError(RuntimeError):
@@ -60,6 +63,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_prefill_status.argtypes = [_vp, _vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_prefill_noalloc.restype = ctypes.c_int
+    lib.kda_prefill_noalloc.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp]
     lib.kda_last_error.restype = ctypes.c_char_p
     lib.kda_last_error.argtypes = []
     lib.kda_version.restype = ctypes.c_int32
@@ -144,6 +149,32 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
         _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _ptr(workspace),
         ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(code)
+    return out, final_state, ckpts
+
+
+def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
+                    chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
+                    out=None, final_state=None, stream=None):
+    """``kda_prefill_noalloc``: the same prefill with the library's built-in
+    scratch array instead of a workspace, for callers that cannot allocate
+    device memory.  Calls on one device share that array: do not let them
+    overlap on the GPU.  Returns (out, final_state, ckpts)."""
+    T, H, D = q.shape
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (num_seqs or 1)
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, v.shape[2], dtype=q.dtype, device=dev)
+    if final_state is None:
+        final_state = torch.empty(N, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    if ckpt_stride > 0 and ckpts is None:
+        cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
+        ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap)
+    code = load_library().kda_prefill_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+        _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _stream(stream))
     _check(code)
     return out, final_state, ckpts
 
