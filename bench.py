@@ -12,7 +12,7 @@ linear_attention_serving_k1_gb300/workloads.py) made on the device; L2 is
 flushed (a 512 MiB write) before every timed step.
 
 Rank 0 prints one JSON line.  With --impl reference the float64 CPU oracle is
-timed instead, on a bounded sample of the same workload.
+timed instead, on the same workload (or its first heads when it is large).
 """
 from __future__ import annotations
 
@@ -60,6 +60,17 @@ def decode_cost_per_head(D: int, es: int = 2):
     KDA pages' estimate, 7*D^2 FLOPs and 8*D^2 bytes (fp32 read + write); the
     per-token vectors q, k, v, out (dtype) and g (fp32), beta add 4*D*es+4*D+4."""
     return 7 * D * D, 8 * D * D + 4 * D * es + 4 * D + 4
+
+
+def load_traffic(key):
+    """DRAM bytes per launch that an ncu capture of the current kernels
+    recorded (profiles/traffic.json, written with the summary that names the
+    command); None if absent."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            return json.load(f).get(key)
+    except Exception:
+        return None
 
 
 def load_peaks():
@@ -153,13 +164,23 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over the ranks (the job's time is the slowest rank's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = device if device is not None else ("cuda" if torch.cuda.is_available() else "cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, rank_ms_per_step: float, world: int, device=None) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank
+    per step (replicas of independent work, weak scaling); the step takes as
+    long as the slowest rank."""
+    ms = max_over_ranks(rank_ms_per_step, world, device)
+    return units_per_rank * world / (ms / 1e3)
 
 
 def time_steps(fn, steps, warmup, flush_buf, stream):
@@ -181,7 +202,7 @@ def time_steps(fn, steps, warmup, flush_buf, stream):
 
 
 # ------------------------------------------------------------------ our arm
-def bench_prefill(w, steps, warmup, dev, flush_buf, world):
+def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True):
     inp = workloads.make_prefill(w, device=dev)
     q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
     s0, cu = inp["init_state"], inp["cu_seqlens"]
@@ -206,6 +227,8 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world):
     torch.cuda.synchronize()
     assert kda.prefill_status(ws) == 0
 
+    if not e2e:
+        return ms, None, 0, 0
     # end to end: pinned host inputs -> device, prefill, outputs -> host, every step
     host_in = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
     host_s0 = s0.cpu().pin_memory() if s0 is not None else None
@@ -228,7 +251,7 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world):
         host_out.copy_(out, non_blocking=True)
         host_fin.copy_(fin, non_blocking=True)
 
-    e2e_ms = time_steps(e2e_step, max(2, steps // 2), 1, flush_buf, stream)
+    e2e_ms = time_steps(e2e_step, steps, max(3, warmup), flush_buf, stream)
     del dev_in, host_in
     return ms, e2e_ms, h2d, d2h
 
@@ -258,31 +281,24 @@ def bench_decode(steps_total, dev, flush_buf, warmup=3):
     return w, ms
 
 
-def cpu_baseline_prefill(w, budget_s=15.0):
-    """Times the float64 oracle on a bounded sample of the prefill workload:
-    the first tokens of every sequence over a subset of heads, grown until the
-    run takes a few seconds.  Returns the dict of the JSON line."""
+def cpu_baseline_prefill(w, max_token_heads=16_000_000):
+    """Times the float64 oracle (OpenMP over sequence x head) on the prefill
+    workload: the whole workload when it has at most max_token_heads
+    token-heads, else its first heads.  Returns the dict of the JSON line."""
     from oracle import oracle
-    inp = workloads.make_prefill(workloads.custom_prefill(
-        H=w.H, D=w.D, lens=[min(w.lens[0], 4096)], dtype=w.dtype, init=w.init, seed=w.seed))
-    T = inp["q"].shape[0]
-    heads = list(range(min(4, w.H)))
-    tok = 256
-    elapsed = 0.0
-    while True:
-        sl = slice(0, tok)
-        args = [inp[n][sl] for n in ("q", "k", "v", "g", "beta")]
-        t0 = time.perf_counter()
-        oracle.prefill_heads(*args, inp["init_state"], None, 0, heads=heads)
-        elapsed = time.perf_counter() - t0
-        if elapsed > budget_s / 4 or tok >= T:
-            break
-        tok = min(T, tok * 4)
-    token_heads_per_s = tok * len(heads) / elapsed
-    return {"value": token_heads_per_s / w.H, "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{tok} tokens x {len(heads)} of {w.H} heads of the prefill workload, float64 "
-                      f"token recurrence, {elapsed:.2f} s; tokens/s = token-heads/s / H"}
+    inp = workloads.make_prefill(w)
+    heads = list(range(w.H))
+    while len(heads) > 1 and w.total_tokens * len(heads) > max_token_heads:
+        heads = heads[: len(heads) // 2]
+    args = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+    t0 = time.perf_counter()
+    oracle.prefill_heads(*args, inp["init_state"], inp["cu_host"].numpy(), w.ckpt_stride, heads=heads)
+    elapsed = time.perf_counter() - t0
+    value = w.total_tokens * len(heads) / w.H / elapsed
+    what = "the whole workload" if len(heads) == w.H else f"{len(heads)} of {w.H} heads"
+    return {"value": round(value, 1), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{what} ({w.total_tokens} tokens), float64 token recurrence, {elapsed:.2f} s; "
+                      f"tokens/s counts all H heads of a token"}
 
 
 def run_ours(args):
@@ -295,23 +311,21 @@ def run_ours(args):
 
     clk = ClockSampler(dev.index if dev.index is not None else 0)
     clk.start()
-    ms, e2e_ms, h2d, d2h = bench_prefill(w, args.steps, args.warmup, dev, flush_buf, world)
+    ms, e2e_ms, h2d, d2h = bench_prefill(w, args.steps, args.warmup, dev, flush_buf, world, not args.no_e2e)
     dec = None
     if not args.no_decode:
         dec_w, dec_ms = bench_decode(64, dev, flush_buf)
     clocks = clk.stop()
 
-    total_ms = max_over_ranks(sum(ms), world)
-    ms_per_step = total_ms / len(ms)
-    tokens_per_step = w.total_tokens * world
-    value = tokens_per_step / (ms_per_step / 1e3)
-    e2e_val = tokens_per_step / (max_over_ranks(sum(e2e_ms), world) / len(e2e_ms) / 1e3)
+    ms_per_step = max_over_ranks(sum(ms) / len(ms), world)
+    value = job_throughput(w.total_tokens, sum(ms) / len(ms), world)
+    e2e_val = job_throughput(w.total_tokens, sum(e2e_ms) / len(e2e_ms), world) if e2e_ms else None
 
     alg_bytes = prefill_algorithmic_bytes(w)
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     roof = {"kernel": "kda_prefill (sequence table + K1 + K2 launches of one call)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": load_traffic(f"prefill_w{args.workload}"),
             "algorithmic_bytes_per_launch": alg_bytes,
             "tensor_tflops": round(prefill_flops(w) / (ms_per_step / 1e3) / 1e12, 2),
             "peak_source": peaks["source"]}
@@ -325,7 +339,8 @@ def run_ours(args):
                "value": round(dec_gbs, 1), "us_per_step": round(dec_mean * 1e3, 2),
                "us_per_step_median": round(dec_ms_med * 1e3, 2), "steps": len(dec_ms),
                "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                            "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+                            "traffic": load_traffic("decode_w3"),
                             "algorithmic_bytes_per_launch": b_h * heads}}
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": len(ms), "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -336,8 +351,8 @@ def run_ours(args):
                        "l2": "flushed (512 MiB write) before every timed step; inputs also exceed L2",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
-            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "e2e": ({"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                     "d2h_bytes_per_step": d2h} if e2e_val else None),
             "gpu_launches": 3 * len(ms),
             "clocks": clocks,
             "decode": dec}
@@ -352,19 +367,25 @@ def run_ours(args):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
+    """The float64 CPU oracle on the same workload, metric and unit (the
+    pages publish no implementation to run): every step is the whole prefill
+    workload (about a second on 16 cores for the default workload), or its
+    first heads when the workload is larger."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
     from oracle import oracle
     w = workloads.workload(args.workload)
-    inp = workloads.make_prefill(workloads.custom_prefill(
-        H=w.H, D=w.D, lens=[1024], dtype=w.dtype, init=w.init, seed=w.seed))
-    heads = [0, 1]
+    inp = workloads.make_prefill(w)
+    heads = list(range(w.H))
+    while len(heads) > 1 and w.total_tokens * len(heads) > 1_000_000:
+        heads = heads[: len(heads) // 2]
     args_ = [inp[n] for n in ("q", "k", "v", "g", "beta")]
+    cu = inp["cu_host"].numpy()
 
     def step():
-        oracle.prefill_heads(*args_, inp["init_state"], None, 0, heads=heads)
+        oracle.prefill_heads(*args_, inp["init_state"], cu, w.ckpt_stride, heads=heads)
 
     for _ in range(args.warmup):
         step()
@@ -373,9 +394,9 @@ def run_reference(args):
         step()
     el = time.perf_counter() - t0
     ms_per_step = el / args.steps * 1e3
-    tok_heads = 1024 * len(heads)
-    value = tok_heads / w.H / (ms_per_step / 1e3)
-    sample = f"1024 tokens x {len(heads)} of {w.H} heads per step, float64 token recurrence; tokens/s = token-heads/s / H"
+    value = w.total_tokens * len(heads) / w.H / (ms_per_step / 1e3)
+    what = "the whole workload" if len(heads) == w.H else f"{len(heads)} of {w.H} heads of the workload"
+    sample = f"{what} per step ({w.total_tokens} tokens), float64 token recurrence; tokens/s counts all H heads"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -397,6 +418,7 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 4, 5])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
