@@ -32,8 +32,9 @@ kda_status cuda_fail(cudaError_t e, const char *where)
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t status, cu, chunk_off, ckpt_off, handoff, total;
+    size_t status, cu, chunk_off, ckpt_off, handoff, carry, total;
     int max_chunks;
+    kda::SegPlan plan;
 };
 
 // Validates the descriptor; fills the workspace layout on success.
@@ -55,8 +56,10 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     if (d->ckpt_stride < 0 || (d->ckpt_stride > 0 && d->ckpt_stride % d->chunk != 0))
         return fail(KDA_ERR_INVALID_ARG, "ckpt_stride %d must be 0 or a positive multiple of chunk", d->ckpt_stride);
     if (d->ckpt_capacity < 0) return fail(KDA_ERR_INVALID_ARG, "ckpt_capacity must be >= 0");
+    if (d->max_seq_len < 0) return fail(KDA_ERR_INVALID_ARG, "max_seq_len must be >= 0");
+    if (d->segment_chunks < 0) return fail(KDA_ERR_INVALID_ARG, "segment_chunks must be >= 0");
     const int64_t maxc = d->total_tokens / d->chunk + d->num_seqs;
-    if (maxc > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many chunks");
+    if (maxc * d->num_heads > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many chunks x heads");
     Layout L;
     L.max_chunks = (int)maxc;
     size_t off = 0;
@@ -65,10 +68,26 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     L.chunk_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.ckpt_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.handoff = off;
-    const size_t rec = kda::use_tc_path(d->dtype, d->head_dim_k, d->chunk)
-                           ? kda::tc_handoff_bytes_per_chunk()
-                           : kda::simt_handoff_bytes_per_chunk(d->head_dim_k, d->chunk);
-    off = align256(off + rec * (size_t)maxc * (size_t)d->num_heads);
+    L.plan = kda::SegPlan{0, 1, 1};
+    if (kda::use_tc_path(d->dtype, d->head_dim_k, d->chunk)) {
+        L.plan = kda::tc_segment_plan(d);
+        if ((int64_t)d->num_seqs * L.plan.G * d->num_heads > INT32_MAX)
+            return fail(KDA_ERR_UNSUPPORTED, "num_seqs x segment_chunks x num_heads too large");
+        const size_t rec = kda::tc_handoff_bytes_per_chunk();
+        if (L.plan.nseg == 1) {   // every chunk's record, indexed by global chunk
+            off = align256(off + rec * (size_t)maxc * (size_t)d->num_heads);
+        } else {                  // R ring slots of N x G x H records, then the carry
+            off = align256(off + rec * (size_t)L.plan.R * (size_t)d->num_seqs * (size_t)L.plan.G *
+                                     (size_t)d->num_heads);
+            L.carry = off;
+            off = align256(off + sizeof(float) * (size_t)d->num_seqs * (size_t)d->num_heads *
+                                     (size_t)d->head_dim_k * (size_t)d->head_dim_v);
+        }
+    } else {
+        const size_t rec = kda::simt_handoff_bytes_per_chunk(d->head_dim_k, d->chunk);
+        off = align256(off + rec * (size_t)maxc * (size_t)d->num_heads);
+    }
+    if (L.plan.nseg == 1) L.carry = off;
     L.total = off;
     *lay = L;
     return KDA_OK;
@@ -149,7 +168,10 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     a.tab.chunk_off = (int32_t *)(ws + L.chunk_off);
     a.tab.ckpt_off = (int32_t *)(ws + L.ckpt_off);
     a.handoff = ws + L.handoff;
-    a.handoff_bytes = L.total - L.handoff;
+    a.handoff_bytes = L.carry - L.handoff;
+    a.carry = L.plan.nseg > 1 ? (float *)(ws + L.carry) : nullptr;
+    a.plan = L.plan;
+    a.seq_cap_chunks = L.plan.nseg > 1 ? L.plan.nseg * L.plan.G : 0;
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);
@@ -176,7 +198,9 @@ kda_status kda_prefill_status(void *workspace, kda_stream_t stream)
     if (code == KDA_ERR_CKPT_OVERFLOW)
         return fail(KDA_ERR_CKPT_OVERFLOW, "more checkpoints due than ckpt_capacity; extra snapshots dropped");
     if (code == KDA_ERR_INVALID_ARG)
-        return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens (must start at 0, be non-decreasing, end at T)");
+        return fail(KDA_ERR_INVALID_ARG,
+                    "malformed cu_seqlens (must start at 0, be non-decreasing, end at T) "
+                    "or a sequence longer than max_seq_len");
     if (code == KDA_ERR_TIMEOUT) return fail(KDA_ERR_TIMEOUT, "a bounded device-side wait gave up");
     return fail((kda_status)code, "device reported status %d", code);
 }

@@ -45,6 +45,19 @@ struct SeqTable {
 };
 
 // ------------------------------------------------------------ launchers
+// Segment plan of the tensor-core prefill.  Every sequence is cut into
+// segments of G local chunks; the preparation kernel (K1) of segment s + 1
+// runs on the caller's stream while the recurrence kernel (K2) of segment s
+// runs on a side stream, and a segment's K1 -> K2 records occupy one of R ring
+// slots, small enough to stay in L2 between the two.  The state crosses a
+// segment boundary through an fp32 carry buffer.  nseg == 1: one K1 and one K2
+// launch over compactly indexed records (no ring slots, no carry).
+struct SegPlan {
+    int G;      // chunks per sequence in one segment
+    int nseg;   // number of segments
+    int R;      // ring slots
+};
+
 struct PrefillArgs {
     const void *q, *k, *v;
     const float *g, *beta, *init_state;
@@ -59,8 +72,11 @@ struct PrefillArgs {
     int max_chunks;              // upper bound of chunks over all sequences
     DevStatus *status;
     SeqTable tab;
-    void *handoff;               // K1 -> K2 buffer
+    void *handoff;               // K1 -> K2 buffer (the ring when plan.nseg > 1)
     size_t handoff_bytes;
+    float *carry;                // [N, H, D, D] state between segments (plan.nseg > 1)
+    SegPlan plan;
+    int seq_cap_chunks;          // chunks any sequence may have (0 = unbounded)
     cudaStream_t stream;
 };
 
@@ -76,6 +92,9 @@ inline bool use_tc_path(kda_dtype dtype, int D, int C)
 {
     return dtype == KDA_DTYPE_BF16 && D == 128 && C == 64;
 }
+
+// Segment plan of the tensor-core path for a validated descriptor.
+SegPlan tc_segment_plan(const kda_prefill_desc *desc);
 
 // Validates `desc` and returns the workspace bytes kda_prefill needs for it
 // (on error: the status, with the thread-local message set).

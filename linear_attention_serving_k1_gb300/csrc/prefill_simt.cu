@@ -31,10 +31,11 @@ constexpr int kThreads = 256;
 // chunk and checkpoint prefix sums.  Serial over sequences on one thread: the
 // number of sequences per call is small next to the token work.
 __global__ void seq_table_kernel(const int32_t *__restrict__ cu_in, int N, int64_t T, int C,
-                                 int stride, int64_t capacity, SeqTable tab, DevStatus *st)
+                                 int stride, int64_t capacity, int cap_chunks, SeqTable tab,
+                                 DevStatus *st)
 {
     if (threadIdx.x != 0) return;
-    bool ok = true;
+    bool ok = true, too_long = false;
     if (cu_in) {
         if (cu_in[0] != 0 || (int64_t)cu_in[N] != T) ok = false;
         for (int n = 0; n < N && ok; ++n)
@@ -52,9 +53,10 @@ __global__ void seq_table_kernel(const int32_t *__restrict__ cu_in, int N, int64
             int32_t len = c1 - c0;
             chunks += (len + C - 1) / C;
             if (stride > 0) ck += len / stride;
+            if (cap_chunks > 0 && (len + C - 1) / C > cap_chunks) too_long = true;
         }
     }
-    if (!ok) st->code = (int32_t)KDA_ERR_INVALID_ARG;
+    if (!ok || too_long) st->code = (int32_t)KDA_ERR_INVALID_ARG;
     else if (stride > 0 && (int64_t)ck > capacity) st->code = (int32_t)KDA_ERR_CKPT_OVERFLOW;
 }
 
@@ -349,7 +351,7 @@ size_t simt_handoff_bytes_per_chunk(int D, int /*C*/) { return sizeof(float) * h
 cudaError_t launch_seq_table(const PrefillArgs &a)
 {
     seq_table_kernel<<<1, 32, 0, a.stream>>>(a.cu_seqlens, a.N, a.T, a.C, a.ckpt_stride,
-                                             a.ckpt_capacity, a.tab, a.status);
+                                             a.ckpt_capacity, a.seq_cap_chunks, a.tab, a.status);
     return cudaGetLastError();
 }
 

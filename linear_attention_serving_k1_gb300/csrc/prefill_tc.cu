@@ -34,6 +34,8 @@
 // the state-independent terms Ke^T Uv and Mc Uv, which K2's state threads
 // read straight from global memory.
 #include "kda_common.cuh"
+#include <algorithm>
+
 #include "tc.cuh"
 
 #include <cuda_fp16.h>
@@ -150,7 +152,7 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
 __global__ void __launch_bounds__(K1_THREADS, 1)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
-             uint8_t *__restrict__ handoff, DevStatus *st)
+             uint8_t *__restrict__ ring, int seg_lo, int G, int slot, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar;
@@ -158,15 +160,29 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ float rq[kC], rk[kC], bs[kC];
     __shared__ float bhalf[kD], blast[kD];
 
-    // heads vary fastest across the grid: CTAs running together read adjacent
-    // 256-byte slices of the same token rows
-    const int gc = blockIdx.y, h = blockIdx.x;
+    // grid: one CTA per (item, head), head fastest (CTAs running together read
+    // adjacent 256-byte slices of the same token rows).  G == 0: the item is a
+    // global chunk index and so is the record's.  G > 0: the item is (sequence
+    // n, chunk seg_lo + i) and its record goes to position (n, i) of ring slot
+    // `slot`.  Exits are uniform and come before any allocation.
+    const int h = (int)(blockIdx.x % (unsigned)H), item = (int)(blockIdx.x / (unsigned)H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (gc >= tab.chunk_off[N]) return;   // uniform across the CTA, before any allocation
-    const int n = find_seq_tc(tab.chunk_off, N, gc);
-    const int t0 = tab.cu[n] + (gc - tab.chunk_off[n]) * kC;
+    int n, lc;
+    size_t ri;
+    if (G == 0) {
+        if (item >= tab.chunk_off[N]) return;
+        n = find_seq_tc(tab.chunk_off, N, item);
+        lc = item - tab.chunk_off[n];
+        ri = (size_t)item;
+    } else {
+        n = item / G;
+        lc = seg_lo + item % G;
+        if (lc >= tab.chunk_off[n + 1] - tab.chunk_off[n]) return;
+        ri = ((size_t)slot * N + n) * G + item % G;
+    }
+    const int t0 = tab.cu[n] + lc * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
-    uint8_t *rec = handoff + ((size_t)gc * H + h) * REC_BYTES;
+    uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
     const bf16 *rawq = reinterpret_cast<const bf16 *>(sm + K1_RAW);
     const bf16 *rawk = rawq + 64 * kD;
     const bf16 *rawv = rawk + 64 * kD;
@@ -569,13 +585,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 // double-buffered; it is off the serial path.
 constexpr int K2_STAGES = 2;
 constexpr uint32_t K2_SOP = K2_STAGES * REC_SMEM;      // f16 S^T [2][rows e x K = d]
-constexpr uint32_t K2_OST = K2_SOP + 2 * 32768;   // bf16 output tile [2][64 rows][128], staged for coalesced stores
-constexpr uint32_t K2_SMEM = K2_OST + 2 * 16384;
+constexpr uint32_t K2_OST = K2_SOP + 2 * 32768;   // bf16 output staging, 2 KB per state warp
+constexpr uint32_t K2_SMEM = K2_OST + 8 * 2048;
 constexpr int K2_STATE_THREADS = 256;
 constexpr int K2_THREADS = K2_STATE_THREADS + 64;
 static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
 // TMEM columns (512 allocated)
-constexpr uint32_t T2_P0 = 0, T2_P1 = 128, T2_OA = 256, T2_OB = 320;   // O buffers at +0 / +128
+constexpr uint32_t T2_P = 0, T2_O = 128;   // state product (128 columns); O buffers at +0 / +64
 constexpr int kL2Ahead = 4;   // records prefetched into L2 ahead of the one being copied
 
 __device__ __forceinline__ void write_sop_half(uint8_t *sop, int e, int half, const float (&S)[64])
@@ -585,18 +601,29 @@ __device__ __forceinline__ void write_sop_half(uint8_t *sop, int e, int half, co
         *reinterpret_cast<uint4 *>(sop + kmaj_off(e, 64 * half + d8, LBO_KIN, SBO_K128)) = pack_f16x8(S + d8);
 }
 
+// 16-byte read-only global load kept in program order (volatile), so that a
+// load issued early stays early instead of being moved next to its use.
+__device__ __forceinline__ uint4 ldg_early(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void ld_rec_bc(const uint8_t *rec, int e, int half, uint4 (&bc)[8])
 {
     const uint4 *pb = reinterpret_cast<const uint4 *>(rec + REC_BC + e * 256 + 128 * half);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) bc[j] = __ldg(pb + j);
+    for (int j = 0; j < 8; ++j) bc[j] = ldg_early(pb + j);
 }
 
 __device__ __forceinline__ void ld_rec_ol(const uint8_t *rec, int e, int half, uint4 (&ol)[4])
 {
     const uint4 *po = reinterpret_cast<const uint4 *>(rec + REC_OL + e * 128 + 64 * half);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) ol[j] = __ldg(po + j);
+    for (int j = 0; j < 4; ++j) ol[j] = ldg_early(po + j);
 }
 
 __device__ __forceinline__ float h_lo(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu))); }
@@ -604,19 +631,37 @@ __device__ __forceinline__ float h_hi(uint32_t u) { return __half2float(__ushort
 
 __global__ void __maxnreg__(168)
 k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
-             const uint8_t *__restrict__ handoff, bf16 *__restrict__ out,
+             const uint8_t *__restrict__ ring, int seg_lo, int G, int slot,
+             float *__restrict__ carry, bf16 *__restrict__ out,
              float *__restrict__ final_state, float *__restrict__ ckpts, int stride,
              int64_t capacity, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2], odone[2], ofree[2], ostaged[2];
+    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2], odone[2], ofree[2];
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
-    const int c_begin = tab.chunk_off[n], nch = tab.chunk_off[n + 1] - c_begin;
+    // This launch covers the sequence's local chunks [c_lo, c_lo + nch) of segment
+    // [seg_lo, seg_lo + G); the state enters from init_state (first segment) or
+    // the carry buffer and leaves to final_state (last segment) or the carry.
+    // G == 0: the whole sequence, records indexed by global chunk.
+    const int nch_seq = tab.chunk_off[n + 1] - tab.chunk_off[n];
+    const int c_lo = G == 0 ? 0 : seg_lo;
+    const int nch = G == 0 ? nch_seq : max(0, min(seg_lo + G, nch_seq) - seg_lo);
     const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
+    const bool first_seg = c_lo == 0, last_seg = G == 0 || seg_lo + G >= nch_seq;
+    const size_t sbase = ((size_t)n * H + h) * kD * kD;
+    const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * G;
+    if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
+        if (first_seg && nch_seq == 0 && final_state)
+            for (int i = tid; i < kD * kD; i += blockDim.x)
+                final_state[sbase + i] = init_state ? init_state[sbase + i] : 0.f;
+        return;
+    }
+    // record of the sequence's chunk c_lo + i
+    auto rec_at = [&](int i) { return ring + ((rec_base + i) * H + h) * REC_BYTES; };
 
     if (tid == 0) {
         for (int s = 0; s < K2_STAGES; ++s) {
@@ -629,13 +674,12 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
             mbar_init(&sready[j], K2_STATE_THREADS / 2);
             mbar_init(&odone[j], 1);
             mbar_init(&ofree[j], K2_STATE_THREADS);
-            mbar_init(&ostaged[j], K2_STATE_THREADS);
         }
         abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_sh, 512);
+        tmem_alloc(&tmem_sh, 256);
         tmem_relinquish();
     }
     fence_before_sync();
@@ -650,18 +694,20 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         const int e = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         float S[64];
-        const size_t sbase = ((size_t)n * H + h) * kD * kD;
+        const float *src_state = first_seg ? init_state : carry;
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-            S[j] = init_state ? init_state[sbase + (size_t)(64 * half + j) * kD + e] : 0.f;
+            S[j] = src_state ? src_state[sbase + (size_t)(64 * half + j) * kD + e] : 0.f;
         write_sop_half(sm + K2_SOP, e, half, S);
         fence_async_smem();
         mbar_arrive(&sready[half]);
         uint4 bc[8];
-        if (nch > 0) ld_rec_bc(handoff + ((size_t)c_begin * H + h) * REC_BYTES, e, half, bc);
+        if (nch > 0) ld_rec_bc(rec_at(0), e, half, bc);
         bool alive = true;
         for (int c = 0; c < nch; ++c) {
             const int s = c % K2_STAGES, ob = c & 1;
+            uint4 ol[4];   // this chunk's Mc Uv terms, needed at the output step
+            ld_rec_ol(rec_at(c), e, half, ol);
             // the stage's copy has landed (the MMA thread saw it too; waiting here
             // makes gamma's bytes visible to this thread as well)
             if (!wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v) ||
@@ -673,78 +719,72 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
             // S = gamma * S + P0 + P1 + Bc, 16 columns at a time (keeps registers low)
             const float *gam = reinterpret_cast<const float *>(sm + s * REC_SMEM + REC_G) + 64 * half;
 #pragma unroll
-            for (int c16 = 0; c16 < 64; c16 += 16) {
-                float p0[16], p1[16];
-                tmem_ld16(tm + lane_base + T2_P0 + 64 * half + c16, p0);
-                tmem_ld16(tm + lane_base + T2_P1 + 64 * half + c16, p1);
+            for (int c32 = 0; c32 < 64; c32 += 32) {
+                float p[32];
+                tmem_ld32(tm + lane_base + T2_P + 64 * half + c32, p);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j8 = 0; j8 < 16; j8 += 8) {
-                    const uint4 b4 = bc[(c16 + j8) / 8];
-                    const uint32_t w4[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int jl = j8 + 2 * u, j = c16 + jl;
-                        S[j] = gam[j] * S[j] + p0[jl] + p1[jl] + h_lo(w4[u]);
-                        S[j + 1] = gam[j + 1] * S[j + 1] + p0[jl + 1] + p1[jl + 1] + h_hi(w4[u]);
-                    }
+                for (int j4 = 0; j4 < 32; j4 += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + c32 + j4);
+                    const uint4 b4 = bc[(c32 + j4) / 8];
+                    const uint32_t w0 = ((j4 & 4) ? b4.z : b4.x), w1 = ((j4 & 4) ? b4.w : b4.y);
+                    const int j = c32 + j4;
+                    S[j] = g4.x * S[j] + p[j4] + h_lo(w0);
+                    S[j + 1] = g4.y * S[j + 1] + p[j4 + 1] + h_hi(w0);
+                    S[j + 2] = g4.z * S[j + 2] + p[j4 + 2] + h_lo(w1);
+                    S[j + 3] = g4.w * S[j + 3] + p[j4 + 3] + h_hi(w1);
                 }
             }
             fence_before_sync();
             mbar_arrive(&pread);
+            // the next chunk's Ke^T Uv terms: issued now, used one chunk later
+            if (c + 1 < nch) ld_rec_bc(rec_at(c + 1), e, half, bc);
             write_sop_half(sm + K2_SOP + ((c + 1) & 1) * 32768, e, half, S);
             fence_async_smem();
             mbar_arrive(&sready[half]);
             mbar_arrive(&empty[s]);            // done with the stage's gamma
 
             // output rows [32 half, 32 half + 32) of this chunk: O = Oa + Ob + Ol
-            uint4 ol[4];
-            ld_rec_ol(handoff + ((size_t)(c_begin + c) * H + h) * REC_BYTES, e, half, ol);
             if (!wait_or_abort(&odone[ob], (c >> 1) & 1, abort_v)) { alive = false; break; }
             fence_after_sync();
-            const int t0 = seq_t0 + c * kC;
+            const int t0 = seq_t0 + (c_lo + c) * kC;
             const int L = min(kC, seq_t1 - t0);
-#pragma unroll
-            for (int c16 = 0; c16 < 32; c16 += 16) {
-                float oa[16], obv[16];
-                tmem_ld16(tm + lane_base + T2_OA + 128 * ob + 32 * half + c16, oa);
-                tmem_ld16(tm + lane_base + T2_OB + 128 * ob + 32 * half + c16, obv);
+            {
+                float o[32];
+                tmem_ld32(tm + lane_base + T2_O + 64 * ob + 32 * half, o);
                 tmem_ld_wait();
-                if (c16 == 16) {
-                    fence_before_sync();
-                    mbar_arrive(&ofree[ob]);
-                }
-                bf16 *ost = reinterpret_cast<bf16 *>(sm + K2_OST + ob * 16384);
+                fence_before_sync();
+                mbar_arrive(&ofree[ob]);
+                // this warp's 32 rows x 32 columns, staged [row][lane] in its own 2 KB
+                bf16 *ost = reinterpret_cast<bf16 *>(sm + K2_OST + warp * 2048);
 #pragma unroll
-                for (int j8 = 0; j8 < 16; j8 += 8) {
-                    const uint4 o4 = ol[(c16 + j8) / 8];
+                for (int j8 = 0; j8 < 32; j8 += 8) {
+                    const uint4 o4 = ol[j8 / 8];
                     const uint32_t w4[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int jl = j8 + 2 * u;
-                        const int r = 32 * half + c16 + jl;
-                        ost[r * kD + e] = __float2bfloat16_rn(oa[jl] + obv[jl] + h_lo(w4[u]));
-                        ost[(r + 1) * kD + e] = __float2bfloat16_rn(oa[jl + 1] + obv[jl + 1] + h_hi(w4[u]));
+                        const int rl = j8 + 2 * u;
+                        ost[rl * 32 + lane] = __float2bfloat16_rn(o[rl] + h_lo(w4[u]));
+                        ost[(rl + 1) * 32 + lane] = __float2bfloat16_rn(o[rl + 1] + h_hi(w4[u]));
                     }
                 }
             }
-            // every state thread has staged its part: write the valid rows with 16-byte stores
-            mbar_arrive(&ostaged[ob]);
-            if (!wait_or_abort(&ostaged[ob], (c >> 1) & 1, abort_v)) { alive = false; break; }
+            // the warp writes its valid rows: 64 contiguous bytes per row, 16-byte stores
+            __syncwarp();
             {
-                const uint4 *ost4 = reinterpret_cast<const uint4 *>(sm + K2_OST + ob * 16384);
+                const uint4 *ost4 = reinterpret_cast<const uint4 *>(sm + K2_OST + warp * 2048);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int idx = tid + j * K2_STATE_THREADS;     // 16-byte chunk of the tile
-                    const int r = idx >> 4, c16b = idx & 15;
+                    const int idx = lane + 32 * j, rl = idx >> 2, part = idx & 3;
+                    const int r = 32 * half + rl;
                     if (r < L)
-                        reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * kD)[c16b] = ost4[idx];
+                        reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * kD + 32 * q4)[part] = ost4[idx];
                 }
             }
-            // the next chunk's state-independent terms, read while this one's tail runs
-            if (c + 1 < nch) ld_rec_bc(handoff + ((size_t)(c_begin + c + 1) * H + h) * REC_BYTES, e, half, bc);
+            __syncwarp();
+            // (output of this chunk done)
             // checkpoint after every `stride` tokens of the sequence
-            const int done = c * kC + L;
+            const int done = (c_lo + c) * kC + L;
             if (stride > 0 && ckpts && L == kC && done % stride == 0) {
                 const int64_t slot = (int64_t)tab.ckpt_off[n] + done / stride - 1;
                 if (slot < capacity) {
@@ -757,9 +797,9 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         if (!alive) {
             *abort_v = 1;
             if (lane == 0) record_timeout(st);
-        } else if (final_state) {
+        } else if (float *dst_state = last_seg ? final_state : carry) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) final_state[sbase + (size_t)(64 * half + j) * kD + e] = S[j];
+            for (int j = 0; j < 64; ++j) dst_state[sbase + (size_t)(64 * half + j) * kD + e] = S[j];
         }
     } else if (warp == 8) {
         // ---------------------------------------------------------- copy role
@@ -774,11 +814,11 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 }
                 if (c == 0)
                     for (int a = 1; a < min(nch, 1 + kL2Ahead); ++a)
-                        prefetch_l2(handoff + ((size_t)(c_begin + a) * H + h) * REC_BYTES, REC_BYTES);
+                        prefetch_l2(rec_at(a), REC_BYTES);
                 else if (c + kL2Ahead < nch)
-                    prefetch_l2(handoff + ((size_t)(c_begin + c + kL2Ahead) * H + h) * REC_BYTES, REC_BYTES);
+                    prefetch_l2(rec_at(c + kL2Ahead), REC_BYTES);
                 mbar_arrive_expect_tx(&full[s], REC_SMEM);
-                bulk_g2s(sm + s * REC_SMEM, handoff + ((size_t)(c_begin + c) * H + h) * REC_BYTES, REC_SMEM,
+                bulk_g2s(sm + s * REC_SMEM, rec_at(c), REC_SMEM,
                          &full[s]);
                 issued = c + 1;
             }
@@ -802,14 +842,14 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tm + T2_P0, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                    mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
                             make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, ks > 0);
                 if (!wait_or_abort(&sready[1], c & 1, abort_v)) { *abort_v = 1; record_timeout(st); break; }
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 4; ks < 8; ++ks)
-                    mma_f16(tm + T2_P1, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, ks > 4);
+                    mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, 1);
                 mma_commit(&sdone);
                 // O = Q' S in two K-halves, into buffer ob once its previous contents were read
                 if (c >= 2 && !wait_or_abort(&ofree[ob], ((c - 2) >> 1) & 1, abort_v)) {
@@ -820,8 +860,8 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_f16(tm + (ks < 4 ? T2_OA : T2_OB) + 128 * ob, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_QP + ks * 256, LBO_KIN, SBO_K128), id_o, (ks & 3) > 0);
+                    mma_f16(tm + T2_O + 64 * ob, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_QP + ks * 256, LBO_KIN, SBO_K128), id_o, ks > 0);
                 mma_commit(&odone[ob]);
                 mma_commit(&empty[s]);
             }
@@ -831,12 +871,44 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 0) tmem_dealloc(tm, 512);
+    if (warp == 0) tmem_dealloc(tm, 256);
 }
 
 }  // namespace
 
 size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
+
+SegPlan tc_segment_plan(const kda_prefill_desc *d)
+{
+    // Automatic choice: overlap only when the recurrence (one CTA per chain and
+    // SM) leaves most of the 152 SMs idle; enough chunks per segment that one
+    // K1 launch fills the remaining SMs about four times over (its last wave is
+    // then a small part of it); at most 56 MB per ring slot, so that two slots
+    // stay in the 129 MB L2; at least 4 chunks, so the carry (128 KB per chain
+    // and segment) stays small beside the records (96.5 KB per chunk); at most
+    // 256 segments.
+    constexpr int64_t kSMs = 152, kSlotMax = 56ll << 20, kMaxChains = 96, kMinG = 4, kMaxSegs = 256;
+    const int64_t T = d->total_tokens;
+    const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
+    const int64_t maxc = (len + d->chunk - 1) / d->chunk;
+    const int64_t chains = (int64_t)d->num_seqs * d->num_heads;
+    SegPlan p{0, 1, 1};
+    int64_t G;
+    if (d->segment_chunks > 0) {
+        G = d->segment_chunks;
+    } else {
+        if (chains > kMaxChains) return p;
+        G = (4 * (kSMs - chains) + chains - 1) / chains;
+        G = std::min<int64_t>(G, kSlotMax / (chains * (int64_t)REC_BYTES));
+        G = std::max<int64_t>(G, kMinG);
+        G = std::max<int64_t>(G, (maxc + kMaxSegs - 1) / kMaxSegs);
+    }
+    if (G >= maxc) return p;
+    p.G = (int)G;
+    p.nseg = (int)((maxc + G - 1) / G);
+    p.R = std::min(2, p.nseg);
+    return p;
+}
 
 namespace {
 thread_local char g_detail[256];
@@ -851,6 +923,42 @@ void note_launch_failure(F *fn, const char *name, int threads, uint32_t dyn_smem
              "%s: %d threads x %d registers (max %d threads per block), %zu B static + %u B dynamic smem",
              name, threads, at.numRegs, at.maxThreadsPerBlock, at.sharedSizeBytes, dyn_smem);
 }
+
+// The calling thread's side stream (highest priority: it carries the
+// recurrence, the critical chain) and events on one device.  Created on first
+// use and kept for the thread's lifetime.
+constexpr int kRingMax = 2;
+struct SideCtx {
+    int device = -1;
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, k1[kRingMax] = {}, k2[kRingMax] = {};
+};
+constexpr int kMaxDevices = 64;
+thread_local SideCtx g_side[kMaxDevices];
+
+cudaError_t side_ctx(SideCtx **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideCtx &c = g_side[dev];
+    if (c.device != dev) {
+        int lo = 0, hi = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
+        const unsigned fl = cudaEventDisableTiming;
+        if ((e = cudaEventCreateWithFlags(&c.fork, fl)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&c.join, fl)) != cudaSuccess) return e;
+        for (int r = 0; r < kRingMax; ++r) {
+            if ((e = cudaEventCreateWithFlags(&c.k1[r], fl)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&c.k2[r], fl)) != cudaSuccess) return e;
+        }
+        c.device = dev;
+    }
+    *out = &c;
+    return cudaSuccess;
+}
 }  // namespace
 
 const char *launch_failure_detail() { return g_detail; }
@@ -863,21 +971,58 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
     if (e != cudaSuccess) return e;
-    if (a.max_chunks > 0) {
-        dim3 g1((unsigned)a.H, (unsigned)a.max_chunks);
-        k1_tc_kernel<<<g1, K1_THREADS, K1_SMEM, a.stream>>>(
-            (const bf16 *)a.q, (const bf16 *)a.k, (const bf16 *)a.v, a.g, a.beta, a.N, a.H, a.tab,
-            (uint8_t *)a.handoff, a.status);
+    const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
+    uint8_t *ring = (uint8_t *)a.handoff;
+    const unsigned chains = (unsigned)((size_t)a.N * a.H);
+    const SegPlan &p = a.plan;
+
+    if (p.nseg <= 1) {   // one K1 over every chunk, then one K2 over every sequence
+        if (a.max_chunks > 0) {
+            k1_tc_kernel<<<(unsigned)((size_t)a.max_chunks * a.H), K1_THREADS, K1_SMEM, a.stream>>>(
+                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, a.status);
+            if ((e = cudaGetLastError()) != cudaSuccess) {
+                note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
+                return e;
+            }
+        }
+        k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
+            a.init_state, a.N, a.H, a.tab, ring, 0, 0, 0, nullptr, (bf16 *)a.out, a.final_state,
+            a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
+        return e;
+    }
+
+    // Segments: K1(s) on the caller's stream, K2(s) on the side stream after
+    // K1(s); K1(s) reuses ring slot s % R only after K2(s - R) has finished.
+    SideCtx *c = nullptr;
+    if ((e = side_ctx(&c)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(c->fork, a.stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(c->side, c->fork, 0)) != cudaSuccess) return e;
+    const unsigned k1_grid = (unsigned)((size_t)a.N * p.G * a.H);
+    for (int s = 0; s < p.nseg && e == cudaSuccess; ++s) {
+        const int slot = s % p.R;
+        if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
+        k1_tc_kernel<<<k1_grid, K1_THREADS, K1_SMEM, a.stream>>>(
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, s * p.G, p.G, slot, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
-            return e;
+            break;
         }
+        if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;
+        if ((e = cudaStreamWaitEvent(c->side, c->k1[slot], 0)) != cudaSuccess) break;
+        k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, c->side>>>(
+            a.init_state, a.N, a.H, a.tab, ring, s * p.G, p.G, slot, a.carry, (bf16 *)a.out,
+            a.final_state, a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
+            break;
+        }
+        e = cudaEventRecord(c->k2[slot], c->side);
     }
-    k2_tc_kernel<<<(unsigned)((size_t)a.N * a.H), K2_THREADS, K2_SMEM, a.stream>>>(
-        a.init_state, a.N, a.H, a.tab, (const uint8_t *)a.handoff, (bf16 *)a.out, a.final_state,
-        a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
-    if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
-    return e;
+    // join the side stream back, also after a failure (a stream capture needs it)
+    cudaError_t ej = cudaEventRecord(c->join, c->side);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(a.stream, c->join, 0);
+    return e != cudaSuccess ? e : ej;
 }
 
 }  // namespace kda

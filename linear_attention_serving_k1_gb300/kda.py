@@ -39,7 +39,8 @@ class PrefillDesc(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("head_dim_k", ctypes.c_int32),
                 ("head_dim_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
-                ("ckpt_capacity", ctypes.c_int64)]
+                ("ckpt_capacity", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
+                ("segment_chunks", ctypes.c_int32)]
 
 
 _lib = None
@@ -103,8 +104,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
-              ckpt_stride: int = 0, ckpt_capacity: int = 0) -> PrefillDesc:
-    return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity)
+              ckpt_stride: int = 0, ckpt_capacity: int = 0, max_seq_len: int = 0,
+              segment_chunks: int = 0) -> PrefillDesc:
+    return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity,
+                       max_seq_len, segment_chunks)
 
 
 def workspace_size(desc: PrefillDesc) -> int:
@@ -124,12 +127,15 @@ def num_checkpoints(lens, ckpt_stride: int) -> int:
 
 def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
             chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
-            out=None, final_state=None, workspace=None, stream=None, want_final: bool = True):
+            out=None, final_state=None, workspace=None, stream=None, want_final: bool = True,
+            max_seq_len: int = 0, segment_chunks: int = 0):
     """Chunked KDA prefill through ``kda_prefill``.
 
     q, k, g: [T, H, D]; v: [T, H, D]; beta: [T, H]; init_state: [N, H, D, D] fp32 or
     None; cu_seqlens: [N + 1] int32 on the device, or None with ``num_seqs``
-    equal-length sequences (default 1).  Returns (out, final_state, ckpts).
+    equal-length sequences (default 1).  ``max_seq_len`` (0 = unknown) bounds
+    every sequence's length; ``segment_chunks`` (0 = automatic) sets the
+    overlap granularity of the tensor-core path.  Returns (out, final_state, ckpts).
     """
     T, H, D = q.shape
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (num_seqs or 1)
@@ -142,7 +148,7 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
         cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
-    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks)
     if workspace is None:
         workspace = alloc_workspace(desc, dev)
     code = load_library().kda_prefill(
@@ -155,7 +161,8 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
 
 def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
                     chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
-                    out=None, final_state=None, stream=None):
+                    out=None, final_state=None, stream=None, max_seq_len: int = 0,
+                    segment_chunks: int = 0):
     """``kda_prefill_noalloc``: the same prefill with the library's built-in
     scratch array instead of a workspace, for callers that cannot allocate
     device memory.  Calls on one device share that array: do not let them
@@ -171,7 +178,7 @@ def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_s
         cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
-    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks)
     code = load_library().kda_prefill_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
         _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _stream(stream))

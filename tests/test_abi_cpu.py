@@ -57,6 +57,7 @@ def test_workspace_size(lib):
 @pytest.mark.parametrize("kw,code", [
     (dict(D=96), -2), (dict(chunk=32), -2), (dict(num_seqs=0), -1), (dict(T=-1), -1),
     (dict(H=0), -1), (dict(dtype_code=7), -1), (dict(ckpt_stride=100), -1),
+    (dict(max_seq_len=-1), -1), (dict(segment_chunks=-2), -1),
 ])
 def test_invalid_desc(lib, kw, code):
     d = _desc(**kw)
@@ -65,6 +66,24 @@ def test_invalid_desc(lib, kw, code):
                          ctypes.byref(d), ctypes.c_void_p(256), ctypes.c_size_t(1 << 30), None)
     assert rc == code
     assert lib.kda_last_error()
+
+
+def test_segmented_workspace_is_bounded(lib):
+    """The tensor-core path keeps a two-slot ring of records instead of every
+    chunk's: for a long single sequence (131072 tokens, 32 heads) the automatic
+    plan needs a fraction of the one-segment workspace, and a max_seq_len bound
+    shrinks a many-sequence batch's need the same way."""
+    long = dict(T=131072, H=32, D=128, dtype_code=kda.DTYPE_BF16)
+    auto = lib.kda_prefill_workspace_size(ctypes.byref(_desc(**long)))
+    whole = lib.kda_prefill_workspace_size(ctypes.byref(_desc(segment_chunks=1 << 20, **long)))
+    record_bytes = 98816
+    assert whole >= 2048 * 32 * record_bytes
+    assert 0 < auto < whole // 8
+    # explicit segment lengths: ring of 2 x G x H records plus a 64 KB state per head
+    for G in (1, 4, 16):
+        n = lib.kda_prefill_workspace_size(ctypes.byref(_desc(segment_chunks=G, **long)))
+        assert n >= 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4
+        assert n < 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4 + 8192
 
 
 def test_prefill_rejects_before_launch(lib):
