@@ -154,6 +154,9 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     if (((uintptr_t)workspace & 255) != 0) return fail(KDA_ERR_WORKSPACE, "workspace not 256-byte aligned");
     if (out && (out == q || out == k || out == v))
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
+    if (kda::use_tc_path(desc->dtype, desc->head_dim_k, desc->chunk) &&
+        ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out) & 15) != 0 || ((uintptr_t)g & 7) != 0))
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned and g 8-byte aligned");
 
     char *ws = (char *)workspace;
     kda::PrefillArgs a;

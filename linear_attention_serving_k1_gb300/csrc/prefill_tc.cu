@@ -104,34 +104,47 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // ============================================================ K1
-// One CTA (256 threads) per (chunk, head).  The Gram product G = [Kg; Qg] Kd^T
-// runs as tf32 (its decayed factors e^{+-b} need the fp32 exponent range);
-// every other product takes f16 operands (11 significant bits: the bf16
-// rounding of 8 bits was measured to put the max output error of long
-// sequences past 2e-2 of the rms, f16/tf32 operands keep it near 3e-3).
+// One CTA (256 threads, two CTAs per SM) per (chunk, head).  The Gram product
+// G = [Kg; Qg] Kd^T runs as tf32 (its decayed factors e^{+-b} need the fp32
+// exponent range); every other product takes f16 operands (11 significant
+// bits: the bf16 rounding of 8 bits was measured to put the max output error
+// of long sequences past 2e-2 of the rms, f16/tf32 operands keep it near 3e-3).
 //
-// Shared memory map (bytes).  The first 73,728 bytes (Kd and the Kg half of
-// [Kg; Qg]) are free once G is computed and are reused by the second phase.
-constexpr uint32_t K1_KD = 0;            // tf32 Kd: rows i 64 x K = d 128, K-inner, LBO 144
-constexpr uint32_t K1_GA = 36864;        // tf32 [Kg; Qg]: rows 128 x K = d 128, K-inner, LBO 144
-constexpr uint32_t K1_F32_LBO = 144;     // 128 + 16: conflict-free scattered 4-byte stores
-constexpr uint32_t K1_F32_SBO = 32 * K1_F32_LBO;
-constexpr uint32_t K1_KGT = K1_GA + 16 * K1_F32_SBO;   // f16 Kg^T: rows d x K = i (128 x 64)
-constexpr uint32_t K1_VT = K1_KGT + 16384;             // f16 V^T : rows e x K = i
-constexpr uint32_t K1_KET = K1_VT + 16384;             // f16 Ke^T: rows d x K = r
-constexpr uint32_t K1_RAW = K1_KET + 16384;            // bf16 q, k, v rows of the chunk [3][64][128]
-constexpr uint32_t K1_SMEM = K1_RAW + 3 * 64 * 256;
-// second phase, inside [0, 73728)
+// The L2 normalisation is folded into scalars instead of being applied to the
+// operands first: with primes for un-normalised rows (Kg' = k e^b, ...) and
+// rq, rk the inverse row norms of q and k,
+//   L   = diag(beta rk) G'_kk diag(rk),     Mc = diag(rq) G'_qk diag(rk)
+//   Wk  = T diag(beta rk) Kg',              Uv = T diag(beta) V
+//   Ke^T Wk = Ke'^T diag(rk) Wk,  Mc Wk = Mc' diag(rk) Wk  (Mc' = diag(rq) G'_qk)
+//   Ke^T Uv = Ke'^T diag(rk) Uv,  Mc Uv = Mc' diag(rk) Uv,   Qg = diag(rq) Qg'
+// so the operands are built in one pass over the inputs, in two halves of the
+// key channels (the Gram product accumulates over both), while the norms are
+// reduced on the side.  Un-normalised f16 operands require |k| < 65504.
+//
+// Shared memory map (bytes).  [0, 55296) holds one key-channel half of the
+// tf32 Gram operands and is reused by the later phases.
+constexpr uint32_t K1_F32_LBO = 144;                   // 128 + 16: conflict-free 8-byte stores
+constexpr uint32_t K1_F32_SBO = 16 * K1_F32_LBO;       // 8-row group stride (K = 64 tf32)
+constexpr uint32_t K1_GA = 0;                          // tf32 [Kg'; Qg']: rows 128 x K = 64 channels
+constexpr uint32_t K1_KD = K1_GA + 16 * K1_F32_SBO;    // tf32 Kd': rows 64 x K = 64 channels
+constexpr uint32_t K1_GRAM_END = K1_KD + 8 * K1_F32_SBO;
+constexpr uint32_t K1_KGT = K1_GRAM_END;               // f16 Kg'^T: rows d (128) x K = i (64)
+constexpr uint32_t K1_VT = K1_KGT + 16384;             // f16 V^T  : rows e x K = i
+constexpr uint32_t K1_KET = K1_VT + 16384;             // f16 Ke'^T: rows d x K = r
+constexpr uint32_t K1_SMEM = K1_KET + 16384;
+// later phases, inside [0, K1_GRAM_END)
 constexpr int K1_P = 68;                 // fp32 row pitch of L and T (16-byte aligned rows)
-constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower, beta-scaled)
+constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower)
 constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
-constexpr uint32_t K1_XS = 34816;        // fp32 [3][16][16] scratch of the blocked inverse (ends 37888)
-constexpr uint32_t K1_TB = 37888;        // f16 T diag(beta): rows r x K = i (64 x 64)
-constexpr uint32_t K1_MC = 46080;        // f16 Mc: rows r x K = i (64 x 64)
-constexpr uint32_t K1_WKT = 54272;       // f16 Wk^T: rows d x K = r (128 x 64)
-constexpr uint32_t K1_UVT = 0;           // f16 Uv^T: rows e x K = r (128 x 64), over L once T is built
-static_assert(K1_WKT + 16384 <= K1_GA + 8 * K1_F32_SBO, "second phase must stay in the freed region");
-static_assert(K1_SMEM <= 227 * 1024 - 2048, "shared memory");
+constexpr uint32_t K1_XS = 34816;        // fp32 [3][16][16] scratch of the blocked inverse
+constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
+constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
+constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
+constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
+constexpr uint32_t K1_UVT = 16384;       // f16 (diag(rk) Uv)^T: rows e x K = r
+static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_UVT + 16384 <= K1_MC, "later phases must fit the Gram region");
+static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 3072 <= K1_MC, "phase overlap");
+static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
 
 // TMEM columns (256 allocated)
@@ -149,7 +162,38 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
                       pack_f16x2(x[6], x[7]));
 }
 
-__global__ void __launch_bounds__(K1_THREADS, 1)
+// Sums each of 16 per-lane values over the warp by recursive halving (16
+// shuffles instead of 80): afterwards lanes 2i and 2i + 1 hold the total of
+// value i.
+__device__ __forceinline__ float warp_sum16_transposed(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 16;
+        const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 8;
+        const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 4;
+        const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const bool up = lane & 2;
+        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+__global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot, DevStatus *st)
@@ -157,8 +201,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_sh;
+    __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
+    __shared__ float nsq[2][2][kC];    // [channel half][q, k][row] partial sums of squares
     __shared__ float rq[kC], rk[kC], bs[kC];
-    __shared__ float bhalf[kD], blast[kD];
 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
     // adjacent 256-byte slices of the same token rows).  G == 0: the item is a
@@ -183,9 +228,33 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int t0 = tab.cu[n] + lc * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
-    const bf16 *rawq = reinterpret_cast<const bf16 *>(sm + K1_RAW);
-    const bf16 *rawk = rawq + 64 * kD;
-    const bf16 *rawv = rawk + 64 * kD;
+    // Qg' in fp32 [r][d] parks in the record's Ke^T Uv area until phase 11
+    float *qg_park = reinterpret_cast<float *>(rec + REC_BC);
+
+    // 0. inputs of the first channel half.  Thread: rows rb .. rb + 7 of its
+    //    warp, channels 64 p + 2 lane and + 1 of half p (4-byte bf16 pairs,
+    //    8-byte gate pairs: each warp reads whole 128- and 256-byte row slices).
+    const int rb = 8 * warp;
+    const bf16 *qrow = q + ((size_t)t0 * H + h) * kD, *krow = k + ((size_t)t0 * H + h) * kD;
+    const bf16 *vrow = v + ((size_t)t0 * H + h) * kD;
+    const float *grow = g + ((size_t)t0 * H + h) * kD;
+    const size_t rstride = (size_t)H * kD;
+    float2 gv[8];
+    uint32_t qv[8], kv[8], vv[8];
+    auto load_half = [&](int p) {
+        const int d = 64 * p + 2 * lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = rb + j;
+            const bool valid = r < L;
+            const size_t o = (size_t)r * rstride + d;
+            gv[j] = valid ? __ldg(reinterpret_cast<const float2 *>(grow + o)) : make_float2(0.f, 0.f);
+            qv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(qrow + o)) : 0u;
+            kv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(krow + o)) : 0u;
+            vv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(vrow + o)) : 0u;
+        }
+    };
+    load_half(0);
 
     if (warp == 0) {
         tmem_alloc(&tmem_sh, 256);
@@ -195,136 +264,117 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    // 0. the chunk's q, k, v rows (256 bytes each) into shared memory: every
-    //    thread issues its 16-byte loads first, then stores them
-    {
-        uint4 buf[12];
-#pragma unroll
-        for (int j = 0; j < 12; ++j) {
-            const int idx = tid + j * K1_THREADS;          // 0 .. 3071
-            const int tsr = idx >> 10, r = (idx >> 4) & 63, c16 = idx & 15;
-            const bf16 *srcp = tsr == 0 ? q : (tsr == 1 ? k : v);
-            buf[j] = r < L ? __ldg(reinterpret_cast<const uint4 *>(srcp + ((size_t)(t0 + r) * H + h) * kD) + c16)
-                           : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 12; ++j) {
-            const int idx = tid + j * K1_THREADS;
-            reinterpret_cast<uint4 *>(sm + K1_RAW)[idx] = buf[j];
-        }
-    }
-    // meanwhile: beta and this thread's g column (rows of its half), batched loads
-    const int d = tid & (kD - 1), half = tid >> 7, r0 = half * 32;
-    float b[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int r = r0 + j;
-        b[j] = (r < L) ? g[((size_t)(t0 + r) * H + h) * kD + d] : 0.f;
-    }
     if (tid < kC) bs[tid] = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    // in-half inclusive cumsum of g; the upper half adds the lower half's total
-#pragma unroll
-    for (int j = 1; j < 32; ++j) b[j] += b[j - 1];
-    if (half == 0) bhalf[d] = b[31];
-    const bool loaded = true;
-    __syncthreads();
-    if (half == 1) {
-        const float p = bhalf[d];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) b[j] += p;
-        blast[d] = b[31];
-    }
-
-    // 1. row norms of q and k (warp w: rows 8w..8w+7) from shared memory; the
-    //    eight rows' reductions are interleaved
-    {
-        float sq[8], sk[8];
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-            const int r = warp * 8 + rr;
-            sq[rr] = sk[rr] = 0.f;
-            if (r < L) {
-                const uint2 qa = *reinterpret_cast<const uint2 *>(rawq + r * kD + lane * 4);
-                const uint2 ka = *reinterpret_cast<const uint2 *>(rawk + r * kD + lane * 4);
-                float a0 = bf_lo(qa.x), a1 = bf_hi(qa.x), a2 = bf_lo(qa.y), a3 = bf_hi(qa.y);
-                float c0 = bf_lo(ka.x), c1 = bf_hi(ka.x), c2 = bf_lo(ka.y), c3 = bf_hi(ka.y);
-                sq[rr] = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-                sk[rr] = c0 * c0 + c1 * c1 + c2 * c2 + c3 * c3;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
-                sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
-            }
-        if (lane < 8) {
-            const int r = warp * 8 + lane;
-            float vq = sq[0], vk = sk[0];
-#pragma unroll
-            for (int rr = 1; rr < 8; ++rr)
-                if (lane == rr) { vq = sq[rr]; vk = sk[rr]; }
-            rq[r] = r < L ? rsqrtf(vq + 1e-6f) : 0.f;
-            rk[r] = r < L ? rsqrtf(vk + 1e-6f) : 0.f;
-        }
-    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = tmem_sh;
+    bool ok = true;
 
-    // 2. decayed q/k in operand layouts (thread: channel d, rows r0..r0+31)
-    const float bl = blast[d];
-    const float gl = __expf(bl);
-    if (half == 0) reinterpret_cast<float *>(rec + REC_G)[d] = gl;
+    // 1-3. per channel half p: cumulative gates, decayed operands, partial row
+    //      norms; then the half's share of G' = [Kg'; Qg'] Kd'^T (tf32, M = 128,
+    //      N = 64, K = 64: 8 instructions of K = 8, accumulating over the halves)
+#pragma unroll 1
+    for (int p = 0; p < 2; ++p) {
+        const int d = 64 * p + 2 * lane;
+        {
+            float c0 = 0.f, c1 = 0.f;
 #pragma unroll
-    for (int j8 = 0; j8 < 32; j8 += 8) {
-        float kgv[8], vv8[8], kev[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = j8 + u, r = r0 + j;
-            const bool valid = r < L;
-            const float qv = valid ? __bfloat162float(rawq[r * kD + d]) : 0.f;
-            const float kv = valid ? __bfloat162float(rawk[r * kD + d]) : 0.f;
-            const float vv = valid ? __bfloat162float(rawv[r * kD + d]) : 0.f;
-            const float qh = qv * rq[r], kh = kv * rk[r];
-            const float e = __expf(b[j]), ei = __expf(-b[j]);
-            const float Kg = kh * e, Qg = qh * e, Kd = kh * ei;
-            *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kg);
-            *reinterpret_cast<float *>(sm + K1_GA + kmaj_off4(64 + r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Qg);
-            *reinterpret_cast<float *>(sm + K1_KD + kmaj_off4(r, d, K1_F32_LBO, K1_F32_SBO)) = round_tf32(Kd);
-            kgv[u] = Kg;
-            vv8[u] = vv;
-            kev[u] = Kd * gl;   // kh * exp(b_last - b_r)
+            for (int j = 0; j < 8; ++j) { c0 += gv[j].x; c1 += gv[j].y; }
+            tot[warp][2 * lane] = c0;
+            tot[warp][2 * lane + 1] = c1;
         }
-        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(kgv);
-        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(vv8);
-        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d, r0 + j8, LBO_KIN, SBO_K64)) = pack_f16x8(kev);
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-
-    // 3. G = [Kg; Qg] Kd^T  (tf32, M = 128, N = 64, K = 128: 16 instructions of K = 8)
-    if (tid == 0 && loaded) {
-        const uint32_t idesc = idesc_tf32(128, 64);
-        const uint32_t a0 = smem_u32(sm + K1_GA), b0 = smem_u32(sm + K1_KD);
+        // the MMA of the previous half has read the operand tiles
+        if (p == 1) ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+        __syncthreads();
+        float pre0 = 0.f, pre1 = 0.f, last0 = 0.f, last1 = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < kD / 8; ++ks)
-            mma_tf32(tm + T1_G, make_desc(a0 + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO),
-                     make_desc(b0 + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO), idesc, ks > 0);
-        mma_commit(&mbar);
+        for (int w = 0; w < 8; ++w) {
+            const float a0 = tot[w][2 * lane], a1 = tot[w][2 * lane + 1];
+            if (w < warp) { pre0 += a0; pre1 += a1; }
+            last0 += a0;
+            last1 += a1;
+        }
+        const float gam0 = __expf(last0), gam1 = __expf(last1);
+        if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
+        float sq[16];
+        uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4];
+        float b0 = pre0, b1 = pre1;
+#pragma unroll
+        for (int j2 = 0; j2 < 8; j2 += 2) {
+            float kgx[2][2], vx[2][2], kex[2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = j2 + u, r = rb + j;
+                b0 += gv[j].x;
+                b1 += gv[j].y;
+                const float e0 = __expf(b0), e1 = __expf(b1), i0 = __expf(-b0), i1 = __expf(-b1);
+                const float q0 = bf_lo(qv[j]), q1 = bf_hi(qv[j]), k0 = bf_lo(kv[j]), k1 = bf_hi(kv[j]);
+                sq[j] = q0 * q0 + q1 * q1;
+                sq[8 + j] = k0 * k0 + k1 * k1;
+                const float kg_0 = k0 * e0, kg_1 = k1 * e1, qg_0 = q0 * e0, qg_1 = q1 * e1;
+                const float kd_0 = k0 * i0, kd_1 = k1 * i1;
+                const uint32_t lo = 2 * lane;
+                *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
+                    make_float2(round_tf32(kg_0), round_tf32(kg_1));
+                *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(64 + r, lo, K1_F32_LBO, K1_F32_SBO)) =
+                    make_float2(round_tf32(qg_0), round_tf32(qg_1));
+                *reinterpret_cast<float2 *>(sm + K1_KD + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
+                    make_float2(round_tf32(kd_0), round_tf32(kd_1));
+                *reinterpret_cast<float2 *>(qg_park + (size_t)r * kD + d) = make_float2(qg_0, qg_1);
+                kgx[0][u] = kg_0; kgx[1][u] = kg_1;
+                vx[0][u] = bf_lo(vv[j]); vx[1][u] = bf_hi(vv[j]);
+                kex[0][u] = kd_0 * gam0; kex[1][u] = kd_1 * gam1;   // k' e^(b_last - b)
+            }
+            kg0[j2 / 2] = pack_f16x2(kgx[0][0], kgx[0][1]);
+            kg1[j2 / 2] = pack_f16x2(kgx[1][0], kgx[1][1]);
+            vf0[j2 / 2] = pack_f16x2(vx[0][0], vx[0][1]);
+            vf1[j2 / 2] = pack_f16x2(vx[1][0], vx[1][1]);
+            ke0[j2 / 2] = pack_f16x2(kex[0][0], kex[0][1]);
+            ke1[j2 / 2] = pack_f16x2(kex[1][0], kex[1][1]);
+        }
+        // f16 operand rows d and d + 1, K = rows rb .. rb + 7
+        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(kg0[0], kg0[1], kg0[2], kg0[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(kg1[0], kg1[1], kg1[2], kg1[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(vf0[0], vf0[1], vf0[2], vf0[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(vf1[0], vf1[1], vf1[2], vf1[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]);
+        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
+        // this half's sums of squares of rows rb .. rb + 7 (q: values 0-7, k: 8-15)
+        {
+            const float s = warp_sum16_transposed(sq, lane);
+            if (!(lane & 1)) {
+                const int i = lane >> 1;
+                nsq[p][i >> 3][rb + (i & 7)] = s;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (p == 0) load_half(1);          // next half's inputs in flight during the MMA
+        if (tid == 0 && ok) {
+            const uint32_t idesc = idesc_tf32(128, 64);
+            const uint32_t a0 = smem_u32(sm + K1_GA), b0d = smem_u32(sm + K1_KD);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_tf32(tm + T1_G, make_desc(a0 + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO),
+                         make_desc(b0d + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO), idesc, p > 0 || ks > 0);
+            mma_commit(&mbar);
+        }
     }
-    bool ok = loaded && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    if (tid < kC) {
+        const int r = tid;
+        rq[r] = r < L ? rsqrtf(nsq[0][0][r] + nsq[1][0][r] + 1e-6f) : 0.f;
+        rk[r] = r < L ? rsqrtf(nsq[0][1][r] + nsq[1][1][r] + 1e-6f) : 0.f;
+    }
+    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
     fence_after_sync();
-    __syncthreads();   // every thread has seen G complete: the first-phase region may be reused
+    __syncthreads();   // G' complete and seen by all: the Gram region may be reused; norms visible
 
-    // 4. read G: lane quarter q4 = warp & 3 holds rows 32 q4 .. +31; warps w and
-    //    w + 4 take columns [0, 32) and [32, 64).  Rows < 64: Kg Kd^T -> L;
-    //    rows >= 64: Qg Kd^T -> Mc.
+    // 4. read G': lane quarter q4 = warp & 3 holds rows 32 q4 .. +31; warps w and
+    //    w + 4 take columns [0, 32) and [32, 64).  Rows < 64: Kg' Kd'^T -> L;
+    //    rows >= 64: Qg' Kd'^T -> Mc' (the row norm of q only).
     const int q4 = warp & 3, ch = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int row = 32 * q4 + lane;
@@ -332,32 +382,30 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     float *Tm = reinterpret_cast<float *>(sm + K1_TM);
     float *Xs = reinterpret_cast<float *>(sm + K1_XS);
     if (ok) {
-        float gv[32];
-        tmem_ld16(tm + lane_base + T1_G + 32 * ch, *reinterpret_cast<float(*)[16]>(gv));
-        tmem_ld16(tm + lane_base + T1_G + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(gv + 16));
+        float gq[32];
+        tmem_ld32(tm + lane_base + T1_G + 32 * ch, gq);
         tmem_ld_wait();
         if (row < 64) {
             const int r = row;
-            const float br = bs[r];
+            const float sr = bs[r] * rk[r];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int col = 32 * ch + i;
-                Lm[r * K1_P + col] = (col < r) ? br * gv[i] : 0.f;
+                Lm[r * K1_P + col] = (col < r) ? sr * rk[col] * gq[i] : 0.f;
             }
         } else {
             const int r = row - 64;
+            const float sr = rq[r];
 #pragma unroll
             for (int i8 = 0; i8 < 32; i8 += 8) {
                 float m8[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) m8[j] = (32 * ch + i8 + j <= r) ? gv[i8 + j] : 0.f;
-                const uint4 val = pack_f16x8(m8);
-                *reinterpret_cast<uint4 *>(sm + K1_MC + kmaj_off(r, 32 * ch + i8, LBO_KIN, SBO_K64)) = val;
+                for (int j = 0; j < 8; ++j) m8[j] = (32 * ch + i8 + j <= r) ? sr * gq[i8 + j] : 0.f;
+                *reinterpret_cast<uint4 *>(sm + K1_MC + kmaj_off(r, 32 * ch + i8, LBO_KIN, SBO_K64)) = pack_f16x8(m8);
             }
         }
     }
     __syncthreads();
-
     // 5. T = (I + L)^-1, blocked by 16: diagonal blocks by forward substitution,
     //    then T_ab = -T_aa * sum_{k=b}^{a-1} L_ak T_kb by block distance.  Each
     //    thread of the block products computes a 1 x 4 strip (float4 rows).
@@ -414,18 +462,22 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         __syncthreads();
     }
 
-    // 6. T diag(beta) -> f16 operand (rows r, K = i): thread -> row tid/4, 16 columns
+    // 6. T diag(beta rk) and T diag(beta) -> f16 operands (rows r, K = i):
+    //    thread -> row tid / 4, 16 columns
     {
         const int r = tid >> 2, i0 = (tid & 3) * 16;
 #pragma unroll
         for (int i8 = 0; i8 < 16; i8 += 8) {
-            float t8[8];
+            float tk[8], tv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + i8 + j;
-                t8[j] = i <= r ? Tm[r * K1_P + i] * bs[i] : 0.f;
+                tv[j] = i <= r ? Tm[r * K1_P + i] * bs[i] : 0.f;
+                tk[j] = tv[j] * rk[i];
             }
-            *reinterpret_cast<uint4 *>(sm + K1_TB + kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64)) = pack_f16x8(t8);
+            const uint32_t o = kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64);
+            *reinterpret_cast<uint4 *>(sm + K1_TBK + o) = pack_f16x8(tk);
+            *reinterpret_cast<uint4 *>(sm + K1_TBV + o) = pack_f16x8(tv);
         }
     }
     fence_async_smem();
@@ -433,22 +485,24 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // 7. Wk^T = Kg^T (T diag beta)^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
+    // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
         const uint32_t idesc = idesc_f16(128, 64);
-        const uint32_t akg = smem_u32(sm + K1_KGT), av = smem_u32(sm + K1_VT), bt = smem_u32(sm + K1_TB);
+        const uint32_t akg = smem_u32(sm + K1_KGT), av = smem_u32(sm + K1_VT);
+        const uint32_t btk = smem_u32(sm + K1_TBK), btv = smem_u32(sm + K1_TBV);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = make_desc(bt + ks * 256, LBO_KIN, SBO_K64);
-            mma_f16(tm + T1_W1, make_desc(akg + ks * 256, LBO_KIN, SBO_K64), bd, idesc, ks > 0);
-            mma_f16(tm + T1_W2, make_desc(av + ks * 256, LBO_KIN, SBO_K64), bd, idesc, ks > 0);
+            mma_f16(tm + T1_W1, make_desc(akg + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(btk + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
+            mma_f16(tm + T1_W2, make_desc(av + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(btv + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
         }
         mma_commit(&mbar);
     }
-    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
     fence_after_sync();
 
-    // 8. Wk^T and Uv^T -> smem operands (rows d / e, K = r).
+    // 8. (diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
 #pragma unroll
@@ -457,6 +511,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tmem_ld16(tm + lane_base + T1_W1 + 32 * ch + c, w);
             tmem_ld16(tm + lane_base + T1_W2 + 32 * ch + c, u);
             tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float s = rk[32 * ch + c + j];
+                w[j] *= s;
+                u[j] *= s;
+            }
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8) {
                 const int kk = 32 * ch + c + h8;
@@ -470,7 +530,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // 9. A'acc = Ke^T Wk (M = 128, N = 128, K = 64); Q'acc = Mc Wk (M = 64, N = 128, K = 64)
+    // 9. A'acc = Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); Q'acc = Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
     if (tid == 0 && ok) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
@@ -482,7 +542,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
     fence_after_sync();
 
     if (ok) {
@@ -499,7 +559,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
                     pack_f16x8(a + h8);
         }
-        // 11. Q' = Qg - Mc Wk: the M = 64 accumulator puts row r = 16 q4 + l in lane 32 q4 + l (l < 16)
+        // 11. Q' = diag(rq) Qg' - Mc Wk: the M = 64 accumulator puts row r = 16 q4 + l
+        //     in lane 32 q4 + l (l < 16); Qg' comes back from where phase 1 parked it
         const int r = 16 * q4 + lane;
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
@@ -507,15 +568,16 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tmem_ld16(tm + lane_base + T1_QP + 64 * ch + c, a);
             tmem_ld_wait();
             if (lane < 16) {
+                const float sr = rq[r];
+                const float4 *src = reinterpret_cast<const float4 *>(qg_park + (size_t)r * kD + 64 * ch + c);
                 float qd[16];
 #pragma unroll
-                for (int j4 = 0; j4 < 16; j4 += 4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(
-                        sm + K1_GA + kmaj_off4(64 + r, 64 * ch + c + j4, K1_F32_LBO, K1_F32_SBO));
-                    qd[j4] = t.x - a[j4];
-                    qd[j4 + 1] = t.y - a[j4 + 1];
-                    qd[j4 + 2] = t.z - a[j4 + 2];
-                    qd[j4 + 3] = t.w - a[j4 + 3];
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const float4 t = __ldcg(src + j4);
+                    qd[4 * j4] = sr * t.x - a[4 * j4];
+                    qd[4 * j4 + 1] = sr * t.y - a[4 * j4 + 1];
+                    qd[4 * j4 + 2] = sr * t.z - a[4 * j4 + 2];
+                    qd[4 * j4 + 3] = sr * t.w - a[4 * j4 + 3];
                 }
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8)
@@ -525,10 +587,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
     }
     fence_before_sync();
-    __syncthreads();
+    __syncthreads();   // the parked Qg' is consumed: its area takes Ke^T Uv next
     fence_after_sync();
 
-    // 12. Bc^T = Uv^T Ke (M = 128, N = 128, K = 64); Ol^T = Uv^T Mc^T (M = 128, N = 64, K = 64)
+    // 12. Bc^T = Uv^T diag(rk) Ke' (M = 128, N = 128, K = 64); Ol^T = Uv^T diag(rk) Mc'^T (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
         const uint32_t auv = smem_u32(sm + K1_UVT), bke = smem_u32(sm + K1_KET), bmc = smem_u32(sm + K1_MC);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(128, 64);
@@ -540,7 +602,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
     fence_after_sync();
     if (ok) {
         // row e of Bc^T: columns [64 ch, 64 ch + 64); row e of Ol^T: columns [32 ch, 32 ch + 32)
