@@ -118,8 +118,8 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 //   Ke^T Wk = Ke'^T diag(rk) Wk,  Mc Wk = Mc' diag(rk) Wk  (Mc' = diag(rq) G'_qk)
 //   Ke^T Uv = Ke'^T diag(rk) Uv,  Mc Uv = Mc' diag(rk) Uv,   Qg = diag(rq) Qg'
 // so the operands are built in one pass over the inputs, in two halves of the
-// key channels (the Gram product accumulates over both), while the norms are
-// reduced on the side.  Un-normalised f16 operands require |k| < 65504.
+// key channels (the Gram product accumulates over both), and the norms are
+// reduced while the Gram product runs.  Un-normalised f16 operands require |k| < 65504.
 //
 // Shared memory map (bytes).  [0, 55296) holds one key-channel half of the
 // tf32 Gram operands and is reused by the later phases.
@@ -133,17 +133,19 @@ constexpr uint32_t K1_VT = K1_KGT + 16384;             // f16 V^T  : rows e x K 
 constexpr uint32_t K1_KET = K1_VT + 16384;             // f16 Ke'^T: rows d x K = r
 constexpr uint32_t K1_SMEM = K1_KET + 16384;
 // later phases, inside [0, K1_GRAM_END)
-constexpr int K1_P = 68;                 // fp32 row pitch of L and T (16-byte aligned rows)
-constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower)
+constexpr int K1_P = 68;                 // fp32 row pitch of T (16-byte aligned rows)
+constexpr int K1_PL = 65;                // fp32 row pitch of L (odd: conflict-free column stores)
+constexpr uint32_t K1_LM = 0;            // fp32 [64][65]  L (strict lower)
 constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
-constexpr uint32_t K1_XS = 34816;        // fp32 [3][16][16] scratch of the blocked inverse
+constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][16] scratch of the 16 -> 32 merge
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
+constexpr uint32_t K1_XW = 46080;        // fp32 [32][32] scratch of the 32 -> 64 merge
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
 constexpr uint32_t K1_UVT = 16384;       // f16 (diag(rk) Uv)^T: rows e x K = r
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_UVT + 16384 <= K1_MC, "later phases must fit the Gram region");
-static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 3072 <= K1_MC, "phase overlap");
+static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 4096 <= K1_GRAM_END, "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
 
@@ -162,37 +164,6 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
                       pack_f16x2(x[6], x[7]));
 }
 
-// Sums each of 16 per-lane values over the warp by recursive halving (16
-// shuffles instead of 80): afterwards lanes 2i and 2i + 1 hold the total of
-// value i.
-__device__ __forceinline__ float warp_sum16_transposed(float (&v)[16], int lane)
-{
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const bool up = lane & 16;
-        const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = lane & 8;
-        const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = lane & 4;
-        const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-        const bool up = lane & 2;
-        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
 __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
@@ -202,7 +173,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
-    __shared__ float nsq[2][2][kC];    // [channel half][q, k][row] partial sums of squares
     __shared__ float rq[kC], rk[kC], bs[kC];
 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
@@ -297,7 +267,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         const float gam0 = __expf(last0), gam1 = __expf(last1);
         if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
-        float sq[16];
         uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4];
         float b0 = pre0, b1 = pre1;
 #pragma unroll
@@ -310,8 +279,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 b1 += gv[j].y;
                 const float e0 = __expf(b0), e1 = __expf(b1), i0 = __expf(-b0), i1 = __expf(-b1);
                 const float q0 = bf_lo(qv[j]), q1 = bf_hi(qv[j]), k0 = bf_lo(kv[j]), k1 = bf_hi(kv[j]);
-                sq[j] = q0 * q0 + q1 * q1;
-                sq[8 + j] = k0 * k0 + k1 * k1;
                 const float kg_0 = k0 * e0, kg_1 = k1 * e1, qg_0 = q0 * e0, qg_1 = q1 * e1;
                 const float kd_0 = k0 * i0, kd_1 = k1 * i1;
                 const uint32_t lo = 2 * lane;
@@ -333,20 +300,22 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             ke0[j2 / 2] = pack_f16x2(kex[0][0], kex[0][1]);
             ke1[j2 / 2] = pack_f16x2(kex[1][0], kex[1][1]);
         }
-        // f16 operand rows d and d + 1, K = rows rb .. rb + 7
-        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(kg0[0], kg0[1], kg0[2], kg0[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_KGT + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(kg1[0], kg1[1], kg1[2], kg1[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(vf0[0], vf0[1], vf0[2], vf0[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_VT + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(vf1[0], vf1[1], vf1[2], vf1[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]);
-        *reinterpret_cast<uint4 *>(sm + K1_KET + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
-        // this half's sums of squares of rows rb .. rb + 7 (q: values 0-7, k: 8-15)
+        // f16 operand rows d and d + 1, K = rows rb .. rb + 7.  Lanes 4-7 of each
+        // quarter-warp store row d + 1 first, so that every store instruction
+        // covers eight distinct rows modulo 8 (conflict-free).
         {
-            const float s = warp_sum16_transposed(sq, lane);
-            if (!(lane & 1)) {
-                const int i = lane >> 1;
-                nsq[p][i >> 3][rb + (i & 7)] = s;
-            }
+            const bool sw = lane & 4;
+            const uint32_t oa = kmaj_off(d + (sw ? 1 : 0), rb, LBO_KIN, SBO_K64);
+            const uint32_t ob = kmaj_off(d + (sw ? 0 : 1), rb, LBO_KIN, SBO_K64);
+#define K1_PAIR_STORE(base, x0, x1)                                                                    \
+    *reinterpret_cast<uint4 *>(sm + (base) + oa) =                                                    \
+        sw ? make_uint4(x1[0], x1[1], x1[2], x1[3]) : make_uint4(x0[0], x0[1], x0[2], x0[3]);         \
+    *reinterpret_cast<uint4 *>(sm + (base) + ob) =                                                    \
+        sw ? make_uint4(x0[0], x0[1], x0[2], x0[3]) : make_uint4(x1[0], x1[1], x1[2], x1[3]);
+            K1_PAIR_STORE(K1_KGT, kg0, kg1)
+            K1_PAIR_STORE(K1_VT, vf0, vf1)
+            K1_PAIR_STORE(K1_KET, ke0, ke1)
+#undef K1_PAIR_STORE
         }
         fence_async_smem();
         fence_before_sync();
@@ -363,10 +332,36 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             mma_commit(&mbar);
         }
     }
-    if (tid < kC) {
-        const int r = tid;
-        rq[r] = r < L ? rsqrtf(nsq[0][0][r] + nsq[1][0][r] + 1e-6f) : 0.f;
-        rk[r] = r < L ? rsqrtf(nsq[0][1][r] + nsq[1][1][r] + 1e-6f) : 0.f;
+    // row norms while the Gram product runs: thread -> row tid / 4, channels
+    // 32 (tid & 3) .. + 31 of q and k (rows this CTA has just read: cache hits)
+    {
+        const int r = tid >> 2, part = tid & 3;
+        float sqq = 0.f, sqk = 0.f;
+        if (r < L) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(qrow + (size_t)r * rstride + 32 * part);
+            const uint4 *kp = reinterpret_cast<const uint4 *>(krow + (size_t)r * rstride + 32 * part);
+            uint4 qa[4], ka[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) { qa[j] = __ldg(qp + j); ka[j] = __ldg(kp + j); }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t qw[4] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w};
+                const uint32_t kw[4] = {ka[j].x, ka[j].y, ka[j].z, ka[j].w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sqq += bf_lo(qw[u]) * bf_lo(qw[u]) + bf_hi(qw[u]) * bf_hi(qw[u]);
+                    sqk += bf_lo(kw[u]) * bf_lo(kw[u]) + bf_hi(kw[u]) * bf_hi(kw[u]);
+                }
+            }
+        }
+        sqq += __shfl_xor_sync(0xffffffffu, sqq, 1);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
+        sqq += __shfl_xor_sync(0xffffffffu, sqq, 2);
+        sqk += __shfl_xor_sync(0xffffffffu, sqk, 2);
+        if (part == 0) {
+            rq[r] = r < L ? rsqrtf(sqq + 1e-6f) : 0.f;
+            rk[r] = r < L ? rsqrtf(sqk + 1e-6f) : 0.f;
+        }
     }
     ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
     fence_after_sync();
@@ -381,6 +376,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     float *Lm = reinterpret_cast<float *>(sm + K1_LM);
     float *Tm = reinterpret_cast<float *>(sm + K1_TM);
     float *Xs = reinterpret_cast<float *>(sm + K1_XS);
+    float *Xw = reinterpret_cast<float *>(sm + K1_XW);
     if (ok) {
         float gq[32];
         tmem_ld32(tm + lane_base + T1_G + 32 * ch, gq);
@@ -391,7 +387,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int col = 32 * ch + i;
-                Lm[r * K1_P + col] = (col < r) ? sr * rk[col] * gq[i] : 0.f;
+                Lm[r * K1_PL + col] = (col < r) ? sr * rk[col] * gq[i] : 0.f;
             }
         } else {
             const int r = row - 64;
@@ -406,20 +402,21 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
     }
     __syncthreads();
-    // 5. T = (I + L)^-1, blocked by 16: diagonal blocks by forward substitution,
-    //    then T_ab = -T_aa * sum_{k=b}^{a-1} L_ak T_kb by block distance.  Each
-    //    thread of the block products computes a 1 x 4 strip (float4 rows).
+    // 5. T = (I + L)^-1.  Diagonal 16 x 16 blocks by forward substitution (one
+    //    column per thread, four partial sums per step), then two doubling
+    //    merges, 16 -> 32 and 32 -> 64: for a lower block pair A (top) and B,
+    //    T_BA = -T_BB (L_BA T_AA).
     if (tid < 64) {
         const int blk = tid >> 4, c = tid & 15, col = 16 * blk + c;
         float tcol[16];
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * blk + rr;
-            float x = (rr == c) ? 1.f : 0.f;
+            float x[4] = {(rr == c) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ii = 0; ii < rr; ++ii)
-                if (ii >= c) x -= Lm[r * K1_P + 16 * blk + ii] * tcol[ii];
-            tcol[rr] = (rr >= c) ? x : 0.f;
+                if (ii >= c) x[ii & 3] -= Lm[r * K1_PL + 16 * blk + ii] * tcol[ii];
+            tcol[rr] = (rr >= c) ? (x[0] + x[1]) + (x[2] + x[3]) : 0.f;
             Tm[r * K1_P + col] = tcol[rr];
         }
     } else {
@@ -430,50 +427,86 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
     }
     __syncthreads();
-    for (int lvl = 1; lvl < 4; ++lvl) {
-        const int nb = 4 - lvl;
-        // X_ab = sum_{k=b}^{a-1} L_ak T_kb   (a = b + lvl), strip (i, 4 j4 .. 4 j4 + 3)
-        if (tid < nb * 64) {
-            const int bb = tid >> 6, i = (tid >> 2) & 15, j4 = (tid & 3) * 4, a = bb + lvl;
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *lrow = Lm + (16 * a + i) * K1_P;
-            for (int m = 16 * bb; m < 16 * a; ++m) {
-                const float l = lrow[m];
-                const float4 t = *reinterpret_cast<const float4 *>(Tm + m * K1_P + 16 * bb + j4);
-                s4.x += l * t.x; s4.y += l * t.y; s4.z += l * t.z; s4.w += l * t.w;
-            }
-            *reinterpret_cast<float4 *>(Xs + (bb * 16 + i) * 16 + j4) = s4;
-        }
-        __syncthreads();
-        // T_ab = -T_aa X_ab
-        if (tid < nb * 64) {
-            const int bb = tid >> 6, i = (tid >> 2) & 15, j4 = (tid & 3) * 4, a = bb + lvl;
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *trow = Tm + (16 * a + i) * K1_P + 16 * a;
+    {   // 16 -> 32, pairs k = 0, 1 (A = block 2k, B = block 2k + 1); thread: pair
+        // k, row i of B, columns j2, j2 + 1
+        const int k2 = tid >> 7, i = (tid >> 3) & 15, j2 = (tid & 7) * 2;
+        const int a0 = 32 * k2, b0 = a0 + 16;
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+        const float *lrow = Lm + (b0 + i) * K1_PL + a0;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float tv = trow[m];
-                const float4 x = *reinterpret_cast<const float4 *>(Xs + (bb * 16 + m) * 16 + j4);
-                s4.x += tv * x.x; s4.y += tv * x.y; s4.z += tv * x.z; s4.w += tv * x.w;
-            }
-            *reinterpret_cast<float4 *>(Tm + (16 * a + i) * K1_P + 16 * bb + j4) =
-                make_float4(-s4.x, -s4.y, -s4.z, -s4.w);
+        for (int m = 0; m < 16; m += 2) {
+            const float2 t0 = *reinterpret_cast<const float2 *>(Tm + (a0 + m) * K1_P + a0 + j2);
+            const float2 t1 = *reinterpret_cast<const float2 *>(Tm + (a0 + m + 1) * K1_P + a0 + j2);
+            const float l0 = lrow[m], l1 = lrow[m + 1];
+            s0.x += l0 * t0.x; s0.y += l0 * t0.y;
+            s1.x += l1 * t1.x; s1.y += l1 * t1.y;
         }
+        *reinterpret_cast<float2 *>(Xs + (k2 * 16 + i) * 16 + j2) = make_float2(s0.x + s1.x, s0.y + s1.y);
         __syncthreads();
+        s0 = make_float2(0.f, 0.f);
+        s1 = s0;
+        const float *trow = Tm + (b0 + i) * K1_P + b0;
+#pragma unroll
+        for (int m = 0; m < 16; m += 2) {
+            const float2 x0 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
+            const float2 x1 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m + 1) * 16 + j2);
+            const float u0 = trow[m], u1 = trow[m + 1];
+            s0.x += u0 * x0.x; s0.y += u0 * x0.y;
+            s1.x += u1 * x1.x; s1.y += u1 * x1.y;
+        }
+        *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-(s0.x + s1.x), -(s0.y + s1.y));
     }
+    __syncthreads();
+    {   // 32 -> 64 (A = rows 0-31, B = rows 32-63); thread: row i of B, columns j4 .. j4 + 3
+        const int i = tid >> 3, j4 = (tid & 7) * 4;
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+        const float *lrow = Lm + (32 + i) * K1_PL;
+#pragma unroll 4
+        for (int m = 0; m < 32; m += 2) {
+            const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
+            const float4 t1 = *reinterpret_cast<const float4 *>(Tm + (m + 1) * K1_P + j4);
+            const float l0 = lrow[m], l1 = lrow[m + 1];
+            s0.x += l0 * t0.x; s0.y += l0 * t0.y; s0.z += l0 * t0.z; s0.w += l0 * t0.w;
+            s1.x += l1 * t1.x; s1.y += l1 * t1.y; s1.z += l1 * t1.z; s1.w += l1 * t1.w;
+        }
+        *reinterpret_cast<float4 *>(Xw + i * 32 + j4) =
+            make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
+        __syncthreads();
+        s0 = make_float4(0.f, 0.f, 0.f, 0.f);
+        s1 = s0;
+        const float *trow = Tm + (32 + i) * K1_P + 32;
+#pragma unroll 4
+        for (int m = 0; m < 32; m += 2) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(Xw + m * 32 + j4);
+            const float4 x1 = *reinterpret_cast<const float4 *>(Xw + (m + 1) * 32 + j4);
+            const float u0 = trow[m], u1 = trow[m + 1];
+            s0.x += u0 * x0.x; s0.y += u0 * x0.y; s0.z += u0 * x0.z; s0.w += u0 * x0.w;
+            s1.x += u1 * x1.x; s1.y += u1 * x1.y; s1.z += u1 * x1.z; s1.w += u1 * x1.w;
+        }
+        *reinterpret_cast<float4 *>(Tm + (32 + i) * K1_P + j4) =
+            make_float4(-(s0.x + s1.x), -(s0.y + s1.y), -(s0.z + s1.z), -(s0.w + s1.w));
+    }
+    __syncthreads();
 
-    // 6. T diag(beta rk) and T diag(beta) -> f16 operands (rows r, K = i):
-    //    thread -> row tid / 4, 16 columns
+    // 6. T diag(beta rk) and T diag(beta) -> f16 operands (rows r, K = i).
+    //    Thread: row r = 8 warp + (tid & 7), columns i0 .. i0 + 15 with
+    //    i0 = 16 ((tid >> 3) & 3): each quarter-warp covers 8 consecutive rows
+    //    (conflict-free float4 reads of T and 16-byte operand stores).
     {
-        const int r = tid >> 2, i0 = (tid & 3) * 16;
+        const int r = 8 * warp + (tid & 7), i0 = 16 * ((tid >> 3) & 3);
 #pragma unroll
         for (int i8 = 0; i8 < 16; i8 += 8) {
             float tk[8], tv[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + i8 + j;
-                tv[j] = i <= r ? Tm[r * K1_P + i] * bs[i] : 0.f;
-                tk[j] = tv[j] * rk[i];
+            for (int j4 = 0; j4 < 8; j4 += 4) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(Tm + r * K1_P + i0 + i8 + j4);
+                const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + i8 + j4 + u;
+                    tv[j4 + u] = i <= r ? tt[u] * bs[i] : 0.f;
+                    tk[j4 + u] = tv[j4 + u] * rk[i];
+                }
             }
             const uint32_t o = kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64);
             *reinterpret_cast<uint4 *>(sm + K1_TBK + o) = pack_f16x8(tk);
@@ -546,6 +579,14 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     if (ok) {
+        // the parked Qg' row of phase 11 (lanes < 16), in flight during phase 10
+        const int r = 16 * q4 + lane;
+        float4 qpk[16];
+        if (lane < 16) {
+            const float4 *src = reinterpret_cast<const float4 *>(qg_park + (size_t)r * kD + 64 * ch);
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) qpk[j4] = __ldcg(src + j4);
+        }
         // 10. A' = -(Ke^T Wk) -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
@@ -560,8 +601,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     pack_f16x8(a + h8);
         }
         // 11. Q' = diag(rq) Qg' - Mc Wk: the M = 64 accumulator puts row r = 16 q4 + l
-        //     in lane 32 q4 + l (l < 16); Qg' comes back from where phase 1 parked it
-        const int r = 16 * q4 + lane;
+        //     in lane 32 q4 + l (l < 16)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
             float a[16];
@@ -569,11 +609,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tmem_ld_wait();
             if (lane < 16) {
                 const float sr = rq[r];
-                const float4 *src = reinterpret_cast<const float4 *>(qg_park + (size_t)r * kD + 64 * ch + c);
                 float qd[16];
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 t = __ldcg(src + j4);
+                    const float4 t = qpk[c / 4 + j4];
                     qd[4 * j4] = sr * t.x - a[4 * j4];
                     qd[4 * j4 + 1] = sr * t.y - a[4 * j4 + 1];
                     qd[4 * j4 + 2] = sr * t.z - a[4 * j4 + 2];
