@@ -16,23 +16,21 @@
 //       T  = (I + L)^-1                            (fp32, blocked, CUDA cores)
 //       Wk = T diag(beta) Kg, Uv = T diag(beta) V   (MMAs)
 //       A' = -Ke^T Wk,  Q' = Qg - Mc Wk             (MMAs)
-//       Bc = Ke^T Uv, Ol = Mc Uv                    (MMAs)
-//   K2  S_next = Diag(gamma) S + A' S + Bc          (fp32 state, one MMA
-//                                                    group on the serial path)
-//       O      = Q' S + Ol
+//   K2  [S_next - Diag(gamma) S | O] = [A' | Ke^T] [S; Uv] , [Q' | Mc] [S; Uv]
+//       as one product per chunk (fp32 state and accumulation)
 // which is W = Uv - Wk S, O = Qg S + Mc W, S_next = Diag(gamma) S + Ke^T W
-// with W eliminated: the serial chain carries one state-dependent MMA per
-// chunk instead of two.
+// with W eliminated: the serial chain carries one state-dependent MMA group
+// per chunk instead of two dependent ones, and the state-independent terms
+// Ke^T Uv and Mc Uv ride in the same accumulator (their K-steps are issued
+// before the state is ready).
 //
 // Precision: fp32 state and accumulation throughout; tensor-core operands are
 // tf32 for the Gram product of K1 and f16 for every other product (values
-// of v and of the state must stay within the f16 range, |x| < 65504).
+// of k, v and of the state must stay within the f16 range, |x| < 65504).
 //
-// K1 writes, per (chunk, head), one record: the operands of K2's two state
-// products (A', Q') already in the tensor-core shared-memory layout
-// (no-swizzle K-major core matrices, moved by one bulk TMA copy), gamma, and
-// the state-independent terms Ke^T Uv and Mc Uv, which K2's state threads
-// read straight from global memory.
+// K1 writes, per (chunk, head), one record holding K2's operand tiles in the
+// tensor-core shared-memory layout (no-swizzle K-major core matrices), moved
+// into K2's shared memory by one bulk TMA copy, and gamma.
 #include "kda_common.cuh"
 #include <algorithm>
 
@@ -51,22 +49,21 @@ constexpr int kC = 64;
 constexpr int kD = 128;
 
 // ------------------------------------------------------------ record layout
-// The first REC_SMEM bytes are copied into K2's shared memory (tensor-core
-// operand tiles, no-swizzle K-major core matrices); the rest is read by K2's
-// state threads straight from global memory.
-// A'   : B operand, rows d (128) x K = d' (128)   LBO 128, SBO 2048   f16
-// Q'   : B operand, rows r (64)  x K = d (128)    LBO 128, SBO 2048   f16
-// gamma: fp32 [128]
-// Bc^T : (Ke^T Uv)^T row-major [e][d]                                  f16
-// Ol^T : (Mc Uv)^T  row-major [e][r]                                   f16
-constexpr uint32_t REC_AP = 0;
+// K2's B operand over K = d' (128): rows 0-127 A'[d][d'], rows 128-191 Q'[r][d];
+// its B operand over K = r (64):    rows 0-127 Ke^T[d][r], rows 128-191 Mc[r][r'];
+// its A operand over K = r:         rows e Uv^T[e][r];  then gamma, fp32 [128].
+// f16, K-major, LBO 128; SBO 2048 for K = 128 and 1024 for K = 64.  With the
+// L2 norms folded into scalars (see K1), the Ke^T rows hold k e^(b_last - b)
+// un-normalised, Mc the rows of Qg Kd^T scaled by the query norm only, and
+// Uv^T the columns of Uv scaled by the key norms: the products are the same.
+constexpr uint32_t REC_AP = 0;          // A' (rows d), then Q' (rows r) at REC_QP
 constexpr uint32_t REC_QP = 32768;
-constexpr uint32_t REC_G = 49152;
-constexpr uint32_t REC_SMEM = 49664;
-constexpr uint32_t REC_BC = REC_SMEM;
-constexpr uint32_t REC_OL = REC_BC + 32768;
-constexpr uint32_t REC_BYTES = REC_OL + 16384;
-static_assert(REC_SMEM % 16 == 0 && REC_BYTES % 256 == 0, "record alignment");
+constexpr uint32_t REC_KM = 49152;      // Ke^T (rows d), then Mc (rows r) at REC_MC
+constexpr uint32_t REC_MC = REC_KM + 16384;
+constexpr uint32_t REC_UV = REC_KM + 24576;
+constexpr uint32_t REC_G = REC_UV + 16384;
+constexpr uint32_t REC_BYTES = REC_G + 512;
+static_assert(REC_BYTES % 256 == 0, "record alignment");
 constexpr uint32_t SBO_K128 = 2048;   // 8-row group stride when K = 128 (K-inner packing)
 constexpr uint32_t SBO_K64 = 1024;    // ... when K = 64
 constexpr uint32_t LBO_KIN = 128;     // K-inner packing: core matrices along K are adjacent
@@ -150,7 +147,7 @@ static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
 
 // TMEM columns (256 allocated)
-constexpr uint32_t T1_G = 0, T1_W1 = 64, T1_W2 = 128, T1_AP = 0, T1_QP = 128, T1_BC = 0, T1_OL = 128;
+constexpr uint32_t T1_G = 0, T1_W1 = 64, T1_W2 = 128, T1_AP = 0, T1_QP = 128;
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
@@ -198,8 +195,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int t0 = tab.cu[n] + lc * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
-    // Qg' in fp32 [r][d] parks in the record's Ke^T Uv area until phase 11
-    float *qg_park = reinterpret_cast<float *>(rec + REC_BC);
+    // Qg' in fp32 [r][d] (32 KB) parks in the record's Ke^T / Mc / Uv^T area
+    // (written last) until phase 11
+    float *qg_park = reinterpret_cast<float *>(rec + REC_KM);
+    static_assert(REC_KM + 32768 <= REC_G, "park area");
 
     // 0. inputs of the first channel half.  Thread: rows rb .. rb + 7 of its
     //    warp, channels 64 p + 2 lane and + 1 of half p (4-byte bf16 pairs,
@@ -625,46 +624,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             }
         }
     }
-    fence_before_sync();
-    __syncthreads();   // the parked Qg' is consumed: its area takes Ke^T Uv next
-    fence_after_sync();
-
-    // 12. Bc^T = Uv^T diag(rk) Ke' (M = 128, N = 128, K = 64); Ol^T = Uv^T diag(rk) Mc'^T (M = 128, N = 64, K = 64)
-    if (tid == 0 && ok) {
-        const uint32_t auv = smem_u32(sm + K1_UVT), bke = smem_u32(sm + K1_KET), bmc = smem_u32(sm + K1_MC);
-        const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(128, 64);
+    if (!ok && tid == 0) record_timeout(st);
+    __syncthreads();   // the parked Qg' is consumed: its area takes the K = r tiles
+    // 12. Ke'^T, Mc' and (diag(rk) Uv)^T are already K2's operand tiles:
+    //     shared memory -> record, 16 bytes per thread and step
+    {
+        const uint4 *ket = reinterpret_cast<const uint4 *>(sm + K1_KET);
+        const uint4 *mc = reinterpret_cast<const uint4 *>(sm + K1_MC);
+        const uint4 *uvt = reinterpret_cast<const uint4 *>(sm + K1_UVT);
+        uint4 *dk = reinterpret_cast<uint4 *>(rec + REC_KM), *dm = reinterpret_cast<uint4 *>(rec + REC_MC);
+        uint4 *du = reinterpret_cast<uint4 *>(rec + REC_UV);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = make_desc(auv + ks * 256, LBO_KIN, SBO_K64);
-            mma_f16(tm + T1_BC, ad, make_desc(bke + ks * 256, LBO_KIN, SBO_K64), id128, ks > 0);
-            mma_f16(tm + T1_OL, ad, make_desc(bmc + ks * 256, LBO_KIN, SBO_K64), id64, ks > 0);
-        }
-        mma_commit(&mbar);
-    }
-    ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
-    fence_after_sync();
-    if (ok) {
-        // row e of Bc^T: columns [64 ch, 64 ch + 64); row e of Ol^T: columns [32 ch, 32 ch + 32)
-#pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-            float a[16];
-            tmem_ld16(tm + lane_base + T1_BC + 64 * ch + c, a);
-            tmem_ld_wait();
-            uint4 *dst = reinterpret_cast<uint4 *>(rec + REC_BC + row * 256 + (64 * ch + c) * 2);
-            dst[0] = pack_f16x8(a);
-            dst[1] = pack_f16x8(a + 8);
+        for (int j = 0; j < 4; ++j) {
+            dk[tid + 256 * j] = ket[tid + 256 * j];
+            du[tid + 256 * j] = uvt[tid + 256 * j];
         }
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-            float a[16];
-            tmem_ld16(tm + lane_base + T1_OL + 32 * ch + c, a);
-            tmem_ld_wait();
-            uint4 *dst = reinterpret_cast<uint4 *>(rec + REC_OL + row * 128 + (32 * ch + c) * 2);
-            dst[0] = pack_f16x8(a);
-            dst[1] = pack_f16x8(a + 8);
-        }
-    } else if (tid == 0) {
-        record_timeout(st);
+        for (int j = 0; j < 2; ++j) dm[tid + 256 * j] = mc[tid + 256 * j];
     }
 
     fence_before_sync();
@@ -675,62 +651,38 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 
 // ============================================================ K2
 // One CTA per (sequence, head), serial over the sequence's chunks.
-//   warps 0-7 : state.  Thread (e = 32 (w & 3) + lane, half = w >> 2) keeps
-//               S[d][e] for d in [64 half, 64 half + 64) in fp32 registers.
-//   warp 8    : copies the records' tensor-core part into a 3-stage ring.
-//   warp 9    : issues the MMAs.
-// Per chunk the state product A' S runs as two independent K-halves
-// (P0: d' < 64, P1: d' >= 64), each fed by the half of the state threads
-// that writes those rows of S^T, so the serial chain per chunk is one
-// 4-instruction MMA group.  O = Q' S is split the same way (Oa, Ob) and
-// double-buffered; it is off the serial path.
+//   16 warps, all on the state: thread (e = 32 (w & 3) + lane, quarter
+//   qd = w >> 2) keeps S[d][e] for d in [32 qd, 32 qd + 32) in fp32 registers
+//   and writes output rows [16 qd, 16 qd + 16) of column e.  One thread also
+//   copies the records' tensor-core part into a 2-stage ring and issues the
+//   MMAs (a separate warp would take the registers the state needs: 16 warps
+//   are the most that keep 128 registers each).
+// Per chunk one product [A' S | Q' S]^T (N = 192: the record keeps the A'
+// and Q' tiles adjacent) accumulates over two K-halves of d', each issued once
+// the state threads owning those rows of S^T have written them.  The state
+// threads read both parts at once, so the next chunk's product overwrites
+// them while this chunk's output is written to memory.
 constexpr int K2_STAGES = 2;
-constexpr uint32_t K2_SOP = K2_STAGES * REC_SMEM;      // f16 S^T [2][rows e x K = d]
-constexpr uint32_t K2_OST = K2_SOP + 2 * 32768;   // bf16 output staging, 2 KB per state warp
-constexpr uint32_t K2_SMEM = K2_OST + 8 * 2048;
-constexpr int K2_STATE_THREADS = 256;
-constexpr int K2_THREADS = K2_STATE_THREADS + 64;
+constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
+constexpr uint32_t K2_SOP = K2_STAGES * REC_BYTES;     // f16 S^T: rows e x K = d
+constexpr uint32_t K2_GAM = K2_SOP + 32768;            // fp32 gamma [kGamSlots][128]
+constexpr int K2_STATE_WARPS = 16;
+constexpr uint32_t K2_SMEM = K2_GAM + kGamSlots * 512;
+constexpr int K2_STATE_THREADS = 32 * K2_STATE_WARPS;
+constexpr int K2_THREADS = K2_STATE_THREADS + 32;
 static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
-// TMEM columns (512 allocated)
-constexpr uint32_t T2_P = 0, T2_O = 128;   // state product (128 columns); O buffers at +0 / +64
-constexpr int kL2Ahead = 4;   // records prefetched into L2 ahead of the one being copied
+// TMEM columns (256 allocated)
+constexpr uint32_t T2_P = 0, T2_O = 128;   // (A' S)^T in columns 0-127, (Q' S)^T in 128-191
 
-__device__ __forceinline__ void write_sop_half(uint8_t *sop, int e, int half, const float (&S)[64])
+__device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, const float (&S)[32])
 {
 #pragma unroll
-    for (int d8 = 0; d8 < 64; d8 += 8)
-        *reinterpret_cast<uint4 *>(sop + kmaj_off(e, 64 * half + d8, LBO_KIN, SBO_K128)) = pack_f16x8(S + d8);
+    for (int d8 = 0; d8 < 32; d8 += 8)
+        *reinterpret_cast<uint4 *>(sop + kmaj_off(e, 32 * qd + d8, LBO_KIN, SBO_K128)) = pack_f16x8(S + d8);
 }
 
-// 16-byte read-only global load kept in program order (volatile), so that a
-// load issued early stays early instead of being moved next to its use.
-__device__ __forceinline__ uint4 ldg_early(const uint4 *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
-__device__ __forceinline__ void ld_rec_bc(const uint8_t *rec, int e, int half, uint4 (&bc)[8])
-{
-    const uint4 *pb = reinterpret_cast<const uint4 *>(rec + REC_BC + e * 256 + 128 * half);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) bc[j] = ldg_early(pb + j);
-}
-
-__device__ __forceinline__ void ld_rec_ol(const uint8_t *rec, int e, int half, uint4 (&ol)[4])
-{
-    const uint4 *po = reinterpret_cast<const uint4 *>(rec + REC_OL + e * 128 + 64 * half);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ol[j] = ldg_early(po + j);
-}
-
-__device__ __forceinline__ float h_lo(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u >> 16))); }
-
-__global__ void __maxnreg__(168)
+__global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
 k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot,
              float *__restrict__ carry, bf16 *__restrict__ out,
@@ -738,7 +690,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
              int64_t capacity, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2], odone[2], ofree[2];
+    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2];
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -767,15 +719,11 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     if (tid == 0) {
         for (int s = 0; s < K2_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + K2_STATE_THREADS);   // MMA commit + every state thread
+            mbar_init(&empty[s], 1 + K2_STATE_THREADS);   // the MMA's commit + every state thread
         }
         mbar_init(&sdone, 1);
         mbar_init(&pread, K2_STATE_THREADS);
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(&sready[j], K2_STATE_THREADS / 2);
-            mbar_init(&odone[j], 1);
-            mbar_init(&ofree[j], K2_STATE_THREADS);
-        }
+        for (int j = 0; j < 2; ++j) mbar_init(&sready[j], K2_STATE_THREADS / 2);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -789,100 +737,146 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const uint32_t tm = tmem_sh;
     volatile int *abort_v = &abort_flag;
 
-    if (warp < 8) {
-        // ---------------------------------------------------------- state role
-        const int q4 = warp & 3, half = warp >> 2;
-        const int e = 32 * q4 + lane;
-        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        float S[64];
+    const int q4 = warp & 3, qd = warp >> 2;
+    const int e = 32 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    // Lane 0 of the last warp drives the record copies and the MMAs.
+    const bool issuer = tid == K2_STATE_THREADS;
+    int copied = 0;
+    auto issue_copy = [&](int c) {   // record c -> stage c % K2_STAGES, once that stage is free
+        const int s = c % K2_STAGES;
+        // the operand tiles into the stage, gamma into its own slot (the stage
+        // is free again once the MMA has read it and every state thread has
+        // seen this copy land; gamma is read later, from its slot)
+        mbar_arrive_expect_tx(&full[s], REC_BYTES);
+        bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_G, &full[s]);
+        bulk_g2s(sm + K2_GAM + (c % kGamSlots) * 512, rec_at(c) + REC_G, 512, &full[s]);
+        copied = c + 1;
+    };
+    // chunk c: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T, in one
+    // accumulator (N = 192 rows of B: d, then r).  The K = r steps (A = Uv^T)
+    // go first, as soon as the record and the accumulator are free; the K = d'
+    // steps (A = S^T) follow half by half as the state threads write S^T.
+    auto issue_mma = [&](int c) -> bool {
+        const int s = c % K2_STAGES;
+        const uint32_t stg = smem_u32(sm + s * REC_BYTES);
+        const uint32_t sop = smem_u32(sm + K2_SOP);
+        const uint32_t idesc = idesc_f16(128, 192);
+        bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v);
+        okw = okw && (c == 0 || wait_or_abort(&pread, (c - 1) & 1, abort_v));
+        if (!okw) return false;
+        fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tm + T2_P, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(stg + REC_KM + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
+        if (!wait_or_abort(&sready[0], c & 1, abort_v)) return false;
+        fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                    make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+        if (!wait_or_abort(&sready[1], c & 1, abort_v)) return false;
+        fence_after_sync();
+#pragma unroll
+        for (int ks = 4; ks < 8; ++ks)
+            mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                    make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+        mma_commit(&sdone);
+        mma_commit(&empty[s]);
+        return true;
+    };
+
+    bool alive = true;
+    if (warp == K2_STATE_WARPS) {
+        // ---------------------------------------------------------- issuer
+        if (issuer) {
+            for (int c = 0; c < min(nch, K2_STAGES); ++c) issue_copy(c);
+            for (int c = 0; c < nch && alive; ++c) {
+                // chunk c's product, then record c + 2 into the stage chunk c
+                // used once that product is complete and seen
+                if (!issue_mma(c)) { alive = false; break; }
+                if (c + K2_STAGES < nch) {
+                    if (!wait_or_abort(&empty[c % K2_STAGES], (c / K2_STAGES) & 1, abort_v)) { alive = false; break; }
+                    issue_copy(c + K2_STAGES);
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- state
+        float S[32];
         const float *src_state = first_seg ? init_state : carry;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-            S[j] = src_state ? src_state[sbase + (size_t)(64 * half + j) * kD + e] : 0.f;
-        write_sop_half(sm + K2_SOP, e, half, S);
+        for (int j = 0; j < 32; ++j)
+            S[j] = src_state ? src_state[sbase + (size_t)(32 * qd + j) * kD + e] : 0.f;
+        write_sop_quarter(sm + K2_SOP, e, qd, S);
         fence_async_smem();
-        mbar_arrive(&sready[half]);
-        uint4 bc[8];
-        if (nch > 0) ld_rec_bc(rec_at(0), e, half, bc);
-        bool alive = true;
-        for (int c = 0; c < nch; ++c) {
-            const int s = c % K2_STAGES, ob = c & 1;
-            uint4 ol[4];   // this chunk's Mc Uv terms, needed at the output step
-            ld_rec_ol(rec_at(c), e, half, ol);
-            // the stage's copy has landed (the MMA thread saw it too; waiting here
-            // makes gamma's bytes visible to this thread as well)
+        mbar_arrive(&sready[qd >> 1]);
+        for (int c = 0; c < nch && alive; ++c) {
+            const int s = c % K2_STAGES;
+            // the stage's copy has landed (waiting here makes gamma's bytes visible
+            // to this thread) and the chunk's product is in TMEM
             if (!wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v) ||
                 !wait_or_abort(&sdone, c & 1, abort_v)) {
                 alive = false;
                 break;
             }
             fence_after_sync();
-            // S = gamma * S + P0 + P1 + Bc, 16 columns at a time (keeps registers low)
-            const float *gam = reinterpret_cast<const float *>(sm + s * REC_SMEM + REC_G) + 64 * half;
-#pragma unroll
-            for (int c32 = 0; c32 < 64; c32 += 32) {
-                float p[32];
-                tmem_ld32(tm + lane_base + T2_P + 64 * half + c32, p);
+            // this thread is past the stage's full phase and the product has read
+            // the stage: it may be refilled (gamma has its own ring)
+            mbar_arrive(&empty[s]);
+            // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16 now and
+            // stored after the state is handed on; then S = gamma * S + P over this
+            // thread's 32 rows d
+            uint32_t ob16[8];
+            {
+                float o[16];
+                tmem_ld16(tm + lane_base + T2_O + 16 * qd, o);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j4 = 0; j4 < 32; j4 += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + c32 + j4);
-                    const uint4 b4 = bc[(c32 + j4) / 8];
-                    const uint32_t w0 = ((j4 & 4) ? b4.z : b4.x), w1 = ((j4 & 4) ? b4.w : b4.y);
-                    const int j = c32 + j4;
-                    S[j] = g4.x * S[j] + p[j4] + h_lo(w0);
-                    S[j + 1] = g4.y * S[j + 1] + p[j4 + 1] + h_hi(w0);
-                    S[j + 2] = g4.z * S[j + 2] + p[j4 + 2] + h_lo(w1);
-                    S[j + 3] = g4.w * S[j + 3] + p[j4 + 3] + h_hi(w1);
+                for (int j = 0; j < 8; ++j) {
+                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+                    ob16[j] = *reinterpret_cast<const uint32_t *>(&v2);
+                }
+            }
+            {
+                const float *gam = reinterpret_cast<const float *>(sm + K2_GAM + (c % kGamSlots) * 512) + 32 * qd;
+#pragma unroll
+                for (int h16 = 0; h16 < 32; h16 += 16) {
+                    float p[16];
+                    tmem_ld16(tm + lane_base + T2_P + 32 * qd + h16, p);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j4 = 0; j4 < 16; j4 += 4) {
+                        const int j = h16 + j4;
+                        const float4 g4 = *reinterpret_cast<const float4 *>(gam + j);
+                        S[j] = fmaf(g4.x, S[j], p[j4]);
+                        S[j + 1] = fmaf(g4.y, S[j + 1], p[j4 + 1]);
+                        S[j + 2] = fmaf(g4.z, S[j + 2], p[j4 + 2]);
+                        S[j + 3] = fmaf(g4.w, S[j + 3], p[j4 + 3]);
+                    }
                 }
             }
             fence_before_sync();
             mbar_arrive(&pread);
-            // the next chunk's Ke^T Uv terms: issued now, used one chunk later
-            if (c + 1 < nch) ld_rec_bc(rec_at(c + 1), e, half, bc);
-            write_sop_half(sm + K2_SOP + ((c + 1) & 1) * 32768, e, half, S);
+            write_sop_quarter(sm + K2_SOP, e, qd, S);
             fence_async_smem();
-            mbar_arrive(&sready[half]);
-            mbar_arrive(&empty[s]);            // done with the stage's gamma
+            mbar_arrive(&sready[qd >> 1]);
 
-            // output rows [32 half, 32 half + 32) of this chunk: O = Oa + Ob + Ol
-            if (!wait_or_abort(&odone[ob], (c >> 1) & 1, abort_v)) { alive = false; break; }
-            fence_after_sync();
+            // this chunk's output, while the next state product runs: straight from
+            // registers (shared memory is busy feeding that product), each warp
+            // store covering 64 contiguous bytes of one row
             const int t0 = seq_t0 + (c_lo + c) * kC;
             const int L = min(kC, seq_t1 - t0);
             {
-                float o[32];
-                tmem_ld32(tm + lane_base + T2_O + 64 * ob + 32 * half, o);
-                tmem_ld_wait();
-                fence_before_sync();
-                mbar_arrive(&ofree[ob]);
-                // this warp's 32 rows x 32 columns, staged [row][lane] in its own 2 KB
-                bf16 *ost = reinterpret_cast<bf16 *>(sm + K2_OST + warp * 2048);
+                unsigned short *orow = reinterpret_cast<unsigned short *>(out) + ((size_t)(t0 + 16 * qd) * H + h) * kD + e;
+                const size_t rs = (size_t)H * kD;
 #pragma unroll
-                for (int j8 = 0; j8 < 32; j8 += 8) {
-                    const uint4 o4 = ol[j8 / 8];
-                    const uint32_t w4[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int rl = j8 + 2 * u;
-                        ost[rl * 32 + lane] = __float2bfloat16_rn(o[rl] + h_lo(w4[u]));
-                        ost[(rl + 1) * 32 + lane] = __float2bfloat16_rn(o[rl + 1] + h_hi(w4[u]));
-                    }
+                for (int rl2 = 0; rl2 < 8; ++rl2) {
+                    if (16 * qd + 2 * rl2 < L) orow[(size_t)(2 * rl2) * rs] = (unsigned short)(ob16[rl2] & 0xFFFFu);
+                    if (16 * qd + 2 * rl2 + 1 < L) orow[(size_t)(2 * rl2 + 1) * rs] = (unsigned short)(ob16[rl2] >> 16);
                 }
             }
-            // the warp writes its valid rows: 64 contiguous bytes per row, 16-byte stores
-            __syncwarp();
-            {
-                const uint4 *ost4 = reinterpret_cast<const uint4 *>(sm + K2_OST + warp * 2048);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int idx = lane + 32 * j, rl = idx >> 2, part = idx & 3;
-                    const int r = 32 * half + rl;
-                    if (r < L)
-                        reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * kD + 32 * q4)[part] = ost4[idx];
-                }
-            }
-            __syncwarp();
             // (output of this chunk done)
             // checkpoint after every `stride` tokens of the sequence
             const int done = (c_lo + c) * kC + L;
@@ -891,82 +885,23 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 if (slot < capacity) {
                     float *dst = ckpts + ((size_t)slot * H + h) * kD * kD + e;
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) dst[(size_t)(64 * half + j) * kD] = S[j];
+                    for (int j = 0; j < 32; ++j) dst[(size_t)(32 * qd + j) * kD] = S[j];
                 }
             }
         }
-        if (!alive) {
-            *abort_v = 1;
-            if (lane == 0) record_timeout(st);
-        } else if (float *dst_state = last_seg ? final_state : carry) {
+        if (alive)
+            if (float *dst_state = last_seg ? final_state : carry) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) dst_state[sbase + (size_t)(64 * half + j) * kD + e] = S[j];
-        }
-    } else if (warp == 8) {
-        // ---------------------------------------------------------- copy role
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % K2_STAGES;
-                if (c >= K2_STAGES && !wait_or_abort(&empty[s], ((c / K2_STAGES) - 1) & 1, abort_v)) {
-                    *abort_v = 1;
-                    record_timeout(st);
-                    break;
-                }
-                if (c == 0)
-                    for (int a = 1; a < min(nch, 1 + kL2Ahead); ++a)
-                        prefetch_l2(rec_at(a), REC_BYTES);
-                else if (c + kL2Ahead < nch)
-                    prefetch_l2(rec_at(c + kL2Ahead), REC_BYTES);
-                mbar_arrive_expect_tx(&full[s], REC_SMEM);
-                bulk_g2s(sm + s * REC_SMEM, rec_at(c), REC_SMEM,
-                         &full[s]);
-                issued = c + 1;
+                for (int j = 0; j < 32; ++j) dst_state[sbase + (size_t)(32 * qd + j) * kD + e] = S[j];
             }
-            // Never leave a copy in flight.
-            for (int c = max(0, issued - K2_STAGES); c < issued; ++c)
+    }
+    if (!alive) {
+        *abort_v = 1;
+        if (lane == 0) record_timeout(st);
+        // never leave a copy in flight
+        if (issuer)
+            for (int c = max(0, copied - K2_STAGES); c < copied; ++c)
                 mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kWaitLimit);
-        }
-    } else {
-        // ---------------------------------------------------------- MMA role
-        if (lane == 0) {
-            const uint32_t id_s = idesc_f16(128, 128), id_o = idesc_f16(128, 64);
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % K2_STAGES, ob = c & 1;
-                const uint32_t stg = smem_u32(sm + s * REC_SMEM);
-                const uint32_t sop = smem_u32(sm + K2_SOP + (c & 1) * 32768);
-                bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v);
-                okw = okw && (c == 0 || wait_or_abort(&pread, (c - 1) & 1, abort_v));
-                // P0 = S^T[:, 0:64] A'[:, 0:64]^T once the first half of S^T is written
-                okw = okw && wait_or_abort(&sready[0], c & 1, abort_v);
-                if (!okw) { *abort_v = 1; record_timeout(st); break; }
-                fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, ks > 0);
-                if (!wait_or_abort(&sready[1], c & 1, abort_v)) { *abort_v = 1; record_timeout(st); break; }
-                fence_after_sync();
-#pragma unroll
-                for (int ks = 4; ks < 8; ++ks)
-                    mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), id_s, 1);
-                mma_commit(&sdone);
-                // O = Q' S in two K-halves, into buffer ob once its previous contents were read
-                if (c >= 2 && !wait_or_abort(&ofree[ob], ((c - 2) >> 1) & 1, abort_v)) {
-                    *abort_v = 1;
-                    record_timeout(st);
-                    break;
-                }
-                fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_f16(tm + T2_O + 64 * ob, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_QP + ks * 256, LBO_KIN, SBO_K128), id_o, ks > 0);
-                mma_commit(&odone[ob]);
-                mma_commit(&empty[s]);
-            }
-        }
     }
 
     fence_before_sync();
