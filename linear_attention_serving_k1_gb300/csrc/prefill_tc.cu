@@ -171,6 +171,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
     __shared__ float rq[kC], rk[kC], bs[kC];
+    __shared__ int wflag[4];           // MMA waits: one thread polls, the barrier releases the rest
 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
     // adjacent 256-byte slices of the same token rows).  G == 0: the item is a
@@ -223,6 +224,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             vv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(vrow + o)) : 0u;
         }
     };
+    const float beta_r = (tid < kC && tid < L) ? __ldg(beta + (size_t)(t0 + tid) * H + h) : 0.f;
     load_half(0);
 
     if (warp == 0) {
@@ -233,7 +235,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         mbar_init(&mbar, 1);
         fence_mbar_init();
     }
-    if (tid < kC) bs[tid] = tid < L ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -254,8 +255,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tot[warp][2 * lane + 1] = c1;
         }
         // the MMA of the previous half has read the operand tiles
-        if (p == 1) ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+        if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+        if (p == 0 && tid < kC) bs[tid] = beta_r;
         __syncthreads();
+        if (p == 1) ok = ok && wflag[0];
         float pre0 = 0.f, pre1 = 0.f, last0 = 0.f, last1 = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
@@ -362,9 +365,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             rk[r] = r < L ? rsqrtf(sqk + 1e-6f) : 0.f;
         }
     }
-    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
-    fence_after_sync();
+    if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
     __syncthreads();   // G' complete and seen by all: the Gram region may be reused; norms visible
+    fence_after_sync();
+    ok = ok && wflag[1];
 
     // 4. read G': lane quarter q4 = warp & 3 holds rows 32 q4 .. +31; warps w and
     //    w + 4 take columns [0, 32) and [32, 64).  Rows < 64: Kg' Kd'^T -> L;
@@ -531,8 +535,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    ok = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    __syncthreads();
     fence_after_sync();
+    ok = ok && wflag[2];
 
     // 8. (diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
@@ -574,8 +580,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    ok = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    if (tid == 0) wflag[3] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    __syncthreads();
     fence_after_sync();
+    ok = ok && wflag[3];
 
     if (ok) {
         // the parked Qg' row of phase 11 (lanes < 16), in flight during phase 10
