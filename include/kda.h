@@ -112,6 +112,14 @@ typedef struct {
 size_t kda_prefill_workspace_size(const kda_prefill_desc *desc);
 
 /*
+ * Number of kernel launches one kda_prefill call with this descriptor
+ * enqueues (a sequence table, then one preparation and one recurrence launch
+ * per segment), or -1 for an invalid descriptor (kda_last_error() says why).
+ * Host-only: touches no device state.
+ */
+int32_t kda_prefill_launch_count(const kda_prefill_desc *desc);
+
+/*
  * Chunked prefill over packed sequences (K1 tensor preparation + K2 blockwise
  * recurrence; page "Kimi K3 reconstructs long-context inference efficiency
  * ...", section "Methodology notes", item "System optimization: FlashKDA";

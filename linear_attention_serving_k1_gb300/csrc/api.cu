@@ -131,6 +131,13 @@ size_t kda_prefill_workspace_size(const kda_prefill_desc *desc)
     return L.total;
 }
 
+int32_t kda_prefill_launch_count(const kda_prefill_desc *desc)
+{
+    Layout L;
+    if (check_desc(desc, &L) != KDA_OK) return -1;
+    return L.plan.nseg > 1 ? 1 + 2 * L.plan.nseg : 3;
+}
+
 kda_status kda_prefill(const void *q, const void *k, const void *v, const float *g,
                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
                        void *out, float *final_state, float *ckpts,

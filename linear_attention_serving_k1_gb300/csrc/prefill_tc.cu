@@ -925,13 +925,13 @@ size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
     // Automatic choice: overlap only when the recurrence (one CTA per chain and
-    // SM) leaves most of the 152 SMs idle; enough chunks per segment that one
-    // K1 launch fills the remaining SMs about four times over (its last wave is
-    // then a small part of it); at most 56 MB per ring slot, so that two slots
-    // stay in the 129 MB L2; at least 4 chunks, so the carry (128 KB per chain
-    // and segment) stays small beside the records (96.5 KB per chunk); at most
-    // 256 segments.
-    constexpr int64_t kSMs = 152, kSlotMax = 56ll << 20, kMaxChains = 96, kMinG = 4, kMaxSegs = 256;
+    // SM) leaves most of the 152 SMs idle; segments long enough that one K1
+    // launch fills the remaining SMs (two K1 CTAs each) about sixteen times over,
+    // so its last partial wave is a small part of it; at least three segments,
+    // so that K1 and K2 overlap for most of the call; at least 4 chunks, so the
+    // carry (128 KB per chain and segment) stays small beside the records
+    // (88.5 KB per chunk); at most 256 segments.
+    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4, kMaxSegs = 256, kWaves = 16;
     const int64_t T = d->total_tokens;
     const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
     const int64_t maxc = (len + d->chunk - 1) / d->chunk;
@@ -942,8 +942,8 @@ SegPlan tc_segment_plan(const kda_prefill_desc *d)
         G = d->segment_chunks;
     } else {
         if (chains > kMaxChains) return p;
-        G = (4 * (kSMs - chains) + chains - 1) / chains;
-        G = std::min<int64_t>(G, kSlotMax / (chains * (int64_t)REC_BYTES));
+        G = (kWaves * 2 * (kSMs - chains) + chains - 1) / chains;
+        G = std::min<int64_t>(G, (maxc + 2) / 3);
         G = std::max<int64_t>(G, kMinG);
         G = std::max<int64_t>(G, (maxc + kMaxSegs - 1) / kMaxSegs);
     }

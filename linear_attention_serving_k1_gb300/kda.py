@@ -21,8 +21,8 @@ STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_status", "kda_decode",
-           "kda_prefill_noalloc", "kda_last_error", "kda_version")
+EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
+           "kda_decode", "kda_prefill_noalloc", "kda_last_error", "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -58,6 +58,8 @@ def load_library(path: Optional[str] = None):
     lib = ctypes.CDLL(path)
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
     lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillDesc)]
+    lib.kda_prefill_launch_count.restype = ctypes.c_int32
+    lib.kda_prefill_launch_count.argtypes = [ctypes.POINTER(PrefillDesc)]
     lib.kda_prefill.restype = ctypes.c_int
     lib.kda_prefill.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp, ctypes.c_size_t, _vp]
     lib.kda_prefill_status.restype = ctypes.c_int
@@ -113,6 +115,14 @@ def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int
 def workspace_size(desc: PrefillDesc) -> int:
     n = load_library().kda_prefill_workspace_size(ctypes.byref(desc))
     if n == 0:
+        raise KDAError(-1, load_library().kda_last_error().decode())
+    return int(n)
+
+
+def launch_count(desc: PrefillDesc) -> int:
+    """Kernel launches one ``kda_prefill`` call with ``desc`` enqueues."""
+    n = load_library().kda_prefill_launch_count(ctypes.byref(desc))
+    if n < 0:
         raise KDAError(-1, load_library().kda_last_error().decode())
     return int(n)
 

@@ -78,12 +78,22 @@ def test_segmented_workspace_is_bounded(lib):
     whole = lib.kda_prefill_workspace_size(ctypes.byref(_desc(segment_chunks=1 << 20, **long)))
     record_bytes = 90624
     assert whole >= 2048 * 32 * record_bytes
-    assert 0 < auto < whole // 8
+    assert 0 < auto < whole // 4
     # explicit segment lengths: ring of 2 x G x H records plus a 64 KB state per head
     for G in (1, 4, 16):
         n = lib.kda_prefill_workspace_size(ctypes.byref(_desc(segment_chunks=G, **long)))
         assert n >= 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4
         assert n < 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4 + 8192
+
+
+def test_launch_count(lib):
+    """Three launches without segments (table, K1, K2); 1 + 2 x segments with."""
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc())) == 3
+    long = dict(T=131072, H=32, D=128, dtype_code=kda.DTYPE_BF16)
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(segment_chunks=1 << 20, **long))) == 3
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(segment_chunks=512, **long))) == 1 + 2 * 4
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(segment_chunks=500, **long))) == 1 + 2 * 5
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(H=0))) == -1
 
 
 def test_prefill_rejects_before_launch(lib):
