@@ -181,7 +181,7 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     a.handoff_bytes = L.carry - L.handoff;
     a.carry = L.plan.nseg > 1 ? (float *)(ws + L.carry) : nullptr;
     a.plan = L.plan;
-    a.seq_cap_chunks = L.plan.nseg > 1 ? L.plan.nseg * L.plan.G : 0;
+    a.seq_cap_chunks = L.plan.nseg > 1 ? L.plan.covered() : 0;
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);

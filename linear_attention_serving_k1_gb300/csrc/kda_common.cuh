@@ -49,13 +49,17 @@ struct SeqTable {
 // segments of G local chunks; the preparation kernel (K1) of segment s + 1
 // runs on the caller's stream while the recurrence kernel (K2) of segment s
 // runs on a side stream, and a segment's K1 -> K2 records occupy one of R ring
-// slots, small enough to stay in L2 between the two.  The state crosses a
-// segment boundary through an fp32 carry buffer.  nseg == 1: one K1 and one K2
-// launch over compactly indexed records (no ring slots, no carry).
+// slots of G chunks per sequence.  The state crosses a segment boundary
+// through an fp32 carry buffer.  nseg == 1: one K1 and one K2 launch over
+// compactly indexed records (no ring slots, no carry).
+constexpr int kMaxSegments = 256;
 struct SegPlan {
-    int G;      // chunks per sequence in one segment
+    int G;      // chunks per sequence in one segment (the last one may hold fewer)
     int nseg;   // number of segments
     int R;      // ring slots
+    int begin(int s) const { return s * G; }
+    int count(int) const { return G; }
+    int covered() const { return nseg * G; }
 };
 
 struct PrefillArgs {

@@ -164,7 +164,7 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
 __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
-             uint8_t *__restrict__ ring, int seg_lo, int G, int slot, DevStatus *st)
+             uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar;
@@ -176,8 +176,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
     // adjacent 256-byte slices of the same token rows).  G == 0: the item is a
     // global chunk index and so is the record's.  G > 0: the item is (sequence
-    // n, chunk seg_lo + i) and its record goes to position (n, i) of ring slot
-    // `slot`.  Exits are uniform and come before any allocation.
+    // n, chunk seg_lo + i), i < G, and its record goes to position (n, i) of
+    // ring slot `slot` (`slot_chunks` records per sequence).  Exits are uniform
+    // and come before any allocation.
     const int h = (int)(blockIdx.x % (unsigned)H), item = (int)(blockIdx.x / (unsigned)H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int n, lc;
@@ -191,7 +192,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         n = item / G;
         lc = seg_lo + item % G;
         if (lc >= tab.chunk_off[n + 1] - tab.chunk_off[n]) return;
-        ri = ((size_t)slot * N + n) * G + item % G;
+        ri = ((size_t)slot * N + n) * slot_chunks + item % G;
     }
     const int t0 = tab.cu[n] + lc * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
@@ -692,7 +693,7 @@ __device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, c
 
 __global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
 k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
-             const uint8_t *__restrict__ ring, int seg_lo, int G, int slot,
+             const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
              float *__restrict__ carry, bf16 *__restrict__ out,
              float *__restrict__ final_state, float *__restrict__ ckpts, int stride,
              int64_t capacity, DevStatus *st)
@@ -714,7 +715,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
     const bool first_seg = c_lo == 0, last_seg = G == 0 || seg_lo + G >= nch_seq;
     const size_t sbase = ((size_t)n * H + h) * kD * kD;
-    const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * G;
+    const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * slot_chunks;
     if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
         if (first_seg && nch_seq == 0 && final_state)
             for (int i = tid; i < kD * kD; i += blockDim.x)
@@ -925,13 +926,15 @@ size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
     // Automatic choice: overlap only when the recurrence (one CTA per chain and
-    // SM) leaves most of the 152 SMs idle; segments long enough that one K1
-    // launch fills the remaining SMs (two K1 CTAs each) about sixteen times over,
-    // so its last partial wave is a small part of it; at least three segments,
-    // so that K1 and K2 overlap for most of the call; at least 4 chunks, so the
-    // carry (128 KB per chain and segment) stays small beside the records
-    // (88.5 KB per chunk); at most 256 segments.
-    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4, kMaxSegs = 256, kWaves = 16;
+    // SM) leaves most of the 152 SMs idle.  Uniform segments of G chunks (the
+    // last one takes the remainder): G long enough that one K1 launch fills the
+    // remaining SMs (two K1 CTAs each) about sixteen times over, so its last
+    // partial wave is a small part of it, and at most 3/8 of the sequence, so
+    // that K1 and K2 overlap for most of the call and the last K2, which
+    // nothing overlaps, is short.  At least 4 chunks (the carry, 128 KB per
+    // chain and segment, stays small beside the records, 88.5 KB per chunk);
+    // at most kMaxSegments segments.
+    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4, kWaves = 16;
     const int64_t T = d->total_tokens;
     const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
     const int64_t maxc = (len + d->chunk - 1) / d->chunk;
@@ -943,9 +946,9 @@ SegPlan tc_segment_plan(const kda_prefill_desc *d)
     } else {
         if (chains > kMaxChains) return p;
         G = (kWaves * 2 * (kSMs - chains) + chains - 1) / chains;
-        G = std::min<int64_t>(G, (maxc + 2) / 3);
+        G = std::min<int64_t>(G, (3 * maxc + 7) / 8);
         G = std::max<int64_t>(G, kMinG);
-        G = std::max<int64_t>(G, (maxc + kMaxSegs - 1) / kMaxSegs);
+        G = std::max<int64_t>(G, (maxc + kMaxSegments - 1) / kMaxSegments);
     }
     if (G >= maxc) return p;
     p.G = (int)G;
@@ -1023,14 +1026,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if (p.nseg <= 1) {   // one K1 over every chunk, then one K2 over every sequence
         if (a.max_chunks > 0) {
             k1_tc_kernel<<<(unsigned)((size_t)a.max_chunks * a.H), K1_THREADS, K1_SMEM, a.stream>>>(
-                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, a.status);
+                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.status);
             if ((e = cudaGetLastError()) != cudaSuccess) {
                 note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
                 return e;
             }
         }
         k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
-            a.init_state, a.N, a.H, a.tab, ring, 0, 0, 0, nullptr, (bf16 *)a.out, a.final_state,
+            a.init_state, a.N, a.H, a.tab, ring, 0, 0, 0, 0, nullptr, (bf16 *)a.out, a.final_state,
             a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
         return e;
@@ -1042,12 +1045,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if ((e = side_ctx(&c)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(c->fork, a.stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(c->side, c->fork, 0)) != cudaSuccess) return e;
-    const unsigned k1_grid = (unsigned)((size_t)a.N * p.G * a.H);
     for (int s = 0; s < p.nseg && e == cudaSuccess; ++s) {
-        const int slot = s % p.R;
+        const int slot = s % p.R, lo = p.begin(s), cnt = p.count(s);
+        const unsigned k1_grid = (unsigned)((size_t)a.N * cnt * a.H);
         if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
         k1_tc_kernel<<<k1_grid, K1_THREADS, K1_SMEM, a.stream>>>(
-            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, s * p.G, p.G, slot, a.status);
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
             break;
@@ -1055,7 +1058,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(c->side, c->k1[slot], 0)) != cudaSuccess) break;
         k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, c->side>>>(
-            a.init_state, a.N, a.H, a.tab, ring, s * p.G, p.G, slot, a.carry, (bf16 *)a.out,
+            a.init_state, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out,
             a.final_state, a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
