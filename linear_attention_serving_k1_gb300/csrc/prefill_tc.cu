@@ -673,6 +673,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 // them while this chunk's output is written to memory.
 constexpr int K2_STAGES = 2;
 constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
+constexpr int kL2Ahead = 3;   // records pulled into L2 this many chunks ahead
 constexpr uint32_t K2_SOP = K2_STAGES * REC_BYTES;     // f16 S^T: rows e x K = d
 constexpr uint32_t K2_GAM = K2_SOP + 32768;            // fp32 gamma [kGamSlots][128]
 constexpr int K2_STATE_WARPS = 16;
@@ -680,8 +681,9 @@ constexpr uint32_t K2_SMEM = K2_GAM + kGamSlots * 512;
 constexpr int K2_STATE_THREADS = 32 * K2_STATE_WARPS;
 constexpr int K2_THREADS = K2_STATE_THREADS + 32;
 static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
-// TMEM columns (256 allocated)
-constexpr uint32_t T2_P = 0, T2_O = 128;   // (A' S)^T in columns 0-127, (Q' S)^T in 128-191
+// TMEM columns (512 allocated): accumulator buffer b at 256 b, (A' S)^T in its
+// columns 0-127 and (Q' S)^T in 128-191
+constexpr uint32_t T2_P = 0, T2_O = 128;
 
 __device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, const float (&S)[32])
 {
@@ -699,7 +701,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
              int64_t capacity, DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], sdone, pread, sready[2];
+    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], gfull[kGamSlots], sdone, pread[2], sready[2];
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -728,16 +730,17 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     if (tid == 0) {
         for (int s = 0; s < K2_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + K2_STATE_THREADS);   // the MMA's commit + every state thread
+            mbar_init(&empty[s], 1);   // the MMA's commit: the state threads read gamma from its own ring
         }
+        for (int j = 0; j < kGamSlots; ++j) mbar_init(&gfull[j], 1);
         mbar_init(&sdone, 1);
-        mbar_init(&pread, K2_STATE_THREADS);
+        for (int j = 0; j < 2; ++j) mbar_init(&pread[j], K2_STATE_THREADS);   // per accumulator buffer
         for (int j = 0; j < 2; ++j) mbar_init(&sready[j], K2_STATE_THREADS / 2);
         abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_sh, 256);
+        tmem_alloc(&tmem_sh, 512);
         tmem_relinquish();
     }
     fence_before_sync();
@@ -754,42 +757,51 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     int copied = 0;
     auto issue_copy = [&](int c) {   // record c -> stage c % K2_STAGES, once that stage is free
         const int s = c % K2_STAGES;
-        // the operand tiles into the stage, gamma into its own slot (the stage
-        // is free again once the MMA has read it and every state thread has
-        // seen this copy land; gamma is read later, from its slot)
-        mbar_arrive_expect_tx(&full[s], REC_BYTES);
+        // the operand tiles into the stage (free again as soon as the MMA has
+        // read it), gamma into its own slot with its own barrier (the state
+        // threads read it later)
+        mbar_arrive_expect_tx(&full[s], REC_G);
         bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_G, &full[s]);
-        bulk_g2s(sm + K2_GAM + (c % kGamSlots) * 512, rec_at(c) + REC_G, 512, &full[s]);
+        mbar_arrive_expect_tx(&gfull[c % kGamSlots], 512);
+        bulk_g2s(sm + K2_GAM + (c % kGamSlots) * 512, rec_at(c) + REC_G, 512, &gfull[c % kGamSlots]);
         copied = c + 1;
     };
-    // chunk c: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T, in one
-    // accumulator (N = 192 rows of B: d, then r).  The K = r steps (A = Uv^T)
-    // go first, as soon as the record and the accumulator are free; the K = d'
-    // steps (A = S^T) follow half by half as the state threads write S^T.
-    auto issue_mma = [&](int c) -> bool {
+    // chunk c: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T, in
+    // TMEM buffer c & 1 (N = 192 rows of B: d, then r).  The K = r steps
+    // (A = Uv^T) do not involve the state: they are issued as soon as the
+    // record has landed and the buffer's previous contents (chunk c - 2) were
+    // read, so they run while the state threads still work on chunk c - 1; the
+    // K = d' steps (A = S^T) follow half by half as the state threads write S^T.
+    auto issue_rpart = [&](int c) -> bool {
         const int s = c % K2_STAGES;
-        const uint32_t stg = smem_u32(sm + s * REC_BYTES);
-        const uint32_t sop = smem_u32(sm + K2_SOP);
+        const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
         const uint32_t idesc = idesc_f16(128, 192);
         bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v);
-        okw = okw && (c == 0 || wait_or_abort(&pread, (c - 1) & 1, abort_v));
+        okw = okw && (c < 2 || wait_or_abort(&pread[c & 1], ((c >> 1) - 1) & 1, abort_v));
         if (!okw) return false;
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tm + T2_P, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
+            mma_f16(acc, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
                     make_desc(stg + REC_KM + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
+        return true;
+    };
+    auto issue_dpart = [&](int c) -> bool {
+        const int s = c % K2_STAGES;
+        const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
+        const uint32_t sop = smem_u32(sm + K2_SOP);
+        const uint32_t idesc = idesc_f16(128, 192);
         if (!wait_or_abort(&sready[0], c & 1, abort_v)) return false;
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+            mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
                     make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
         if (!wait_or_abort(&sready[1], c & 1, abort_v)) return false;
         fence_after_sync();
 #pragma unroll
         for (int ks = 4; ks < 8; ++ks)
-            mma_f16(tm + T2_P, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+            mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
                     make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
         mma_commit(&sdone);
         mma_commit(&empty[s]);
@@ -801,14 +813,17 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         // ---------------------------------------------------------- issuer
         if (issuer) {
             for (int c = 0; c < min(nch, K2_STAGES); ++c) issue_copy(c);
+            alive = issue_rpart(0);
             for (int c = 0; c < nch && alive; ++c) {
-                // chunk c's product, then record c + 2 into the stage chunk c
-                // used once that product is complete and seen
-                if (!issue_mma(c)) { alive = false; break; }
+                // chunk c's state-dependent steps; then record c + 2 into the
+                // stage chunk c used, once its product is complete; then the
+                // state-independent steps of chunk c + 1
+                if (!issue_dpart(c)) { alive = false; break; }
                 if (c + K2_STAGES < nch) {
                     if (!wait_or_abort(&empty[c % K2_STAGES], (c / K2_STAGES) & 1, abort_v)) { alive = false; break; }
                     issue_copy(c + K2_STAGES);
                 }
+                if (c + 1 < nch && !issue_rpart(c + 1)) { alive = false; break; }
             }
         }
     } else {
@@ -822,25 +837,28 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         fence_async_smem();
         mbar_arrive(&sready[qd >> 1]);
         for (int c = 0; c < nch && alive; ++c) {
-            const int s = c % K2_STAGES;
-            // the stage's copy has landed (waiting here makes gamma's bytes visible
-            // to this thread) and the chunk's product is in TMEM
-            if (!wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v) ||
+            // gamma has landed (its slot's barrier cannot run ahead: slot c % 4 is
+            // refilled only after the product of chunk c + 2, which needs this
+            // thread's S^T of chunk c + 1) and the chunk's product is in TMEM;
+            // records a few chunks ahead are pulled into L2 meanwhile
+            if (c + kL2Ahead < nch) {
+                const uint8_t *pre = rec_at(c + kL2Ahead);
+                for (uint32_t off = (uint32_t)tid * 128; off < REC_G; off += K2_STATE_THREADS * 128)
+                    prefetch_l2_line(pre + off);
+            }
+            if (!wait_or_abort(&gfull[c % kGamSlots], (c / kGamSlots) & 1, abort_v) ||
                 !wait_or_abort(&sdone, c & 1, abort_v)) {
                 alive = false;
                 break;
             }
             fence_after_sync();
-            // this thread is past the stage's full phase and the product has read
-            // the stage: it may be refilled (gamma has its own ring)
-            mbar_arrive(&empty[s]);
             // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16 now and
             // stored after the state is handed on; then S = gamma * S + P over this
             // thread's 32 rows d
             uint32_t ob16[8];
             {
                 float o[16];
-                tmem_ld16(tm + lane_base + T2_O + 16 * qd, o);
+                tmem_ld16(tm + lane_base + T2_O + 256 * (c & 1) + 16 * qd, o);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -853,7 +871,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
 #pragma unroll
                 for (int h16 = 0; h16 < 32; h16 += 16) {
                     float p[16];
-                    tmem_ld16(tm + lane_base + T2_P + 32 * qd + h16, p);
+                    tmem_ld16(tm + lane_base + T2_P + 256 * (c & 1) + 32 * qd + h16, p);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j4 = 0; j4 < 16; j4 += 4) {
@@ -867,7 +885,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 }
             }
             fence_before_sync();
-            mbar_arrive(&pread);
+            mbar_arrive(&pread[c & 1]);
             write_sop_quarter(sm + K2_SOP, e, qd, S);
             fence_async_smem();
             mbar_arrive(&sready[qd >> 1]);
@@ -916,7 +934,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 }  // namespace

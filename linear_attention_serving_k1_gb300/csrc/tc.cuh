@@ -85,6 +85,12 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Pulls one 128-byte line into L2 (no register result, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_line(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads)
 {
