@@ -58,6 +58,8 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     if (d->ckpt_capacity < 0) return fail(KDA_ERR_INVALID_ARG, "ckpt_capacity must be >= 0");
     if (d->max_seq_len < 0) return fail(KDA_ERR_INVALID_ARG, "max_seq_len must be >= 0");
     if (d->segment_chunks < 0) return fail(KDA_ERR_INVALID_ARG, "segment_chunks must be >= 0");
+    if (d->scalar_gate != 0 && d->scalar_gate != 1)
+        return fail(KDA_ERR_INVALID_ARG, "scalar_gate must be 0 or 1 (got %d)", d->scalar_gate);
     const int64_t maxc = d->total_tokens / d->chunk + d->num_seqs;
     if (maxc * d->num_heads > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many chunks x heads");
     Layout L;
@@ -162,8 +164,10 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     if (out && (out == q || out == k || out == v))
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
     if (kda::use_tc_path(desc->dtype, desc->head_dim_k, desc->chunk) &&
-        ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out) & 15) != 0 || ((uintptr_t)g & 7) != 0))
-        return fail(KDA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned and g 8-byte aligned");
+        ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out) & 15) != 0 ||
+         ((uintptr_t)g & (desc->scalar_gate ? 3 : 7)) != 0))
+        return fail(KDA_ERR_INVALID_ARG,
+                    "q, k, v and out must be 16-byte aligned and g 8-byte aligned (4 with scalar_gate)");
 
     char *ws = (char *)workspace;
     kda::PrefillArgs a;
@@ -182,6 +186,7 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     a.carry = L.plan.nseg > 1 ? (float *)(ws + L.carry) : nullptr;
     a.plan = L.plan;
     a.seq_cap_chunks = L.plan.nseg > 1 ? L.plan.covered() : 0;
+    a.scalar_gate = desc->scalar_gate != 0;
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);

@@ -81,6 +81,7 @@ struct PrefillArgs {
     float *carry;                // [N, H, D, D] state between segments (plan.nseg > 1)
     SegPlan plan;
     int seq_cap_chunks;          // chunks any sequence may have (0 = unbounded)
+    bool scalar_gate;            // g is [T, H] (one decay per head), else [T, H, Dk]
     cudaStream_t stream;
 };
 

@@ -97,7 +97,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, int N, int H,
-               SeqTable tab, float *__restrict__ handoff)
+               SeqTable tab, float *__restrict__ handoff, int scalar_gate)
 {
     constexpr int P = D + 1;   // padded row pitch (bank-conflict free columns)
     extern __shared__ float smem[];
@@ -147,7 +147,7 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
         const int d = tid;
         float b = 0.f;
         for (int r = 0; r < kC; ++r) {
-            if (r < L) b += g[((size_t)(t0 + r) * H + h) * D + d];
+            if (r < L) b += scalar_gate ? g[(size_t)(t0 + r) * H + h] : g[((size_t)(t0 + r) * H + h) * D + d];
             const float e = expf(b), ei = expf(-b);
             const float kh = Kg[r * P + d];
             Qg[r * P + d] *= e;
@@ -334,7 +334,7 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
         dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
         k1_simt_kernel<D, T><<<g1, kThreads, sm1, a.stream>>>(
             (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.N, a.H, a.tab,
-            (float *)a.handoff);
+            (float *)a.handoff, a.scalar_gate ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned g2 = (unsigned)((size_t)a.N * a.H * (D / kBV));

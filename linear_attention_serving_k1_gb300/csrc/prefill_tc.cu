@@ -164,7 +164,8 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
 __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
-             uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, DevStatus *st)
+             uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
+             DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar;
@@ -208,7 +209,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int rb = 8 * warp;
     const bf16 *qrow = q + ((size_t)t0 * H + h) * kD, *krow = k + ((size_t)t0 * H + h) * kD;
     const bf16 *vrow = v + ((size_t)t0 * H + h) * kD;
-    const float *grow = g + ((size_t)t0 * H + h) * kD;
+    // the gate: a decay per key channel ([T, H, Dk]) or one per row shared by
+    // every channel ([T, H], then the same value fills both lanes of gv)
+    const float *grow = g + ((size_t)t0 * H + h) * (scalar_gate ? 1 : kD);
     const size_t rstride = (size_t)H * kD;
     float2 gv[8];
     uint32_t qv[8], kv[8], vv[8];
@@ -219,7 +222,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const int r = rb + j;
             const bool valid = r < L;
             const size_t o = (size_t)r * rstride + d;
-            gv[j] = valid ? __ldg(reinterpret_cast<const float2 *>(grow + o)) : make_float2(0.f, 0.f);
+            if (scalar_gate) {
+                const float gs = valid ? __ldg(grow + (size_t)r * H) : 0.f;
+                gv[j] = make_float2(gs, gs);
+            } else {
+                gv[j] = valid ? __ldg(reinterpret_cast<const float2 *>(grow + o)) : make_float2(0.f, 0.f);
+            }
             qv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(qrow + o)) : 0u;
             kv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(krow + o)) : 0u;
             vv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(vrow + o)) : 0u;
@@ -1044,7 +1052,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if (p.nseg <= 1) {   // one K1 over every chunk, then one K2 over every sequence
         if (a.max_chunks > 0) {
             k1_tc_kernel<<<(unsigned)((size_t)a.max_chunks * a.H), K1_THREADS, K1_SMEM, a.stream>>>(
-                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.status);
+                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.scalar_gate ? 1 : 0, a.status);
             if ((e = cudaGetLastError()) != cudaSuccess) {
                 note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
                 return e;
@@ -1068,7 +1076,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         const unsigned k1_grid = (unsigned)((size_t)a.N * cnt * a.H);
         if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
         k1_tc_kernel<<<k1_grid, K1_THREADS, K1_SMEM, a.stream>>>(
-            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.status);
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.scalar_gate ? 1 : 0, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
             break;

@@ -40,7 +40,7 @@ class PrefillDesc(ctypes.Structure):
                 ("head_dim_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
                 ("ckpt_capacity", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
-                ("segment_chunks", ctypes.c_int32)]
+                ("segment_chunks", ctypes.c_int32), ("scalar_gate", ctypes.c_int32)]
 
 
 _lib = None
@@ -107,9 +107,9 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
               ckpt_stride: int = 0, ckpt_capacity: int = 0, max_seq_len: int = 0,
-              segment_chunks: int = 0) -> PrefillDesc:
+              segment_chunks: int = 0, scalar_gate: bool = False) -> PrefillDesc:
     return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity,
-                       max_seq_len, segment_chunks)
+                       max_seq_len, segment_chunks, int(bool(scalar_gate)))
 
 
 def workspace_size(desc: PrefillDesc) -> int:
@@ -141,7 +141,8 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
             max_seq_len: int = 0, segment_chunks: int = 0):
     """Chunked KDA prefill through ``kda_prefill``.
 
-    q, k, g: [T, H, D]; v: [T, H, D]; beta: [T, H]; init_state: [N, H, D, D] fp32 or
+    q, k: [T, H, D]; v: [T, H, D]; g: [T, H, D] (a decay per key channel) or
+    [T, H] (one per head: the scalar-gate form); beta: [T, H]; init_state: [N, H, D, D] fp32 or
     None; cu_seqlens: [N + 1] int32 on the device, or None with ``num_seqs``
     equal-length sequences (default 1).  ``max_seq_len`` (0 = unknown) bounds
     every sequence's length; ``segment_chunks`` (0 = automatic) sets the
@@ -158,7 +159,8 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
         cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
-    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
+                     scalar_gate=g.dim() == 2)
     if workspace is None:
         workspace = alloc_workspace(desc, dev)
     code = load_library().kda_prefill(
@@ -188,7 +190,8 @@ def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_s
         cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
-    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks)
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
+                     scalar_gate=g.dim() == 2)
     code = load_library().kda_prefill_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
         _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _stream(stream))

@@ -41,10 +41,14 @@ def test_version(lib):
 
 
 def _desc(**kw):
+    raw_gate = kw.pop("raw_scalar_gate", None)
     d = dict(T=256, H=2, D=64, num_seqs=1, dtype_code=kda.DTYPE_FP32, chunk=64, ckpt_stride=0,
              ckpt_capacity=0)
     d.update(kw)
-    return kda.make_desc(**d)
+    desc = kda.make_desc(**d)
+    if raw_gate is not None:   # a value the binding would not produce
+        desc.scalar_gate = raw_gate
+    return desc
 
 
 def test_workspace_size(lib):
@@ -57,7 +61,7 @@ def test_workspace_size(lib):
 @pytest.mark.parametrize("kw,code", [
     (dict(D=96), -2), (dict(chunk=32), -2), (dict(num_seqs=0), -1), (dict(T=-1), -1),
     (dict(H=0), -1), (dict(dtype_code=7), -1), (dict(ckpt_stride=100), -1),
-    (dict(max_seq_len=-1), -1), (dict(segment_chunks=-2), -1),
+    (dict(max_seq_len=-1), -1), (dict(segment_chunks=-2), -1), (dict(raw_scalar_gate=2), -1),
 ])
 def test_invalid_desc(lib, kw, code):
     d = _desc(**kw)
