@@ -207,6 +207,21 @@ kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, cons
                                const int32_t *cu_seqlens, void *out, float *final_state,
                                float *ckpts, const kda_prefill_desc *desc, kda_stream_t stream);
 
+/*
+ * kda_decode over a pool of states: the state of sequence n is slot
+ * slot_ids[n] of state_pool [pool_slots, H, Dk, Dv] fp32 (updated in place),
+ * so that a serving loop keeps sequences in fixed slots while its batch
+ * changes (continuous batching; a prefill can write a sequence's slot as its
+ * final_state, or resume from a checkpoint copied into a slot).  slot_ids is
+ * int32 [N] on the device; a slot outside [0, pool_slots) marks a padding
+ * row: its state is not touched and its output row is zero.  Slots of one call
+ * must be distinct.  Everything else as kda_decode.
+ */
+kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state_pool, int64_t pool_slots,
+                            const int32_t *slot_ids, void *out, int32_t N, int32_t H, int32_t Dk,
+                            int32_t Dv, kda_dtype dtype, kda_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *kda_last_error(void);
 

@@ -220,9 +220,10 @@ kda_status kda_prefill_status(void *workspace, kda_stream_t stream)
     return fail((kda_status)code, "device reported status %d", code);
 }
 
-kda_status kda_decode(const void *q, const void *k, const void *v, const float *g,
-                      const float *beta, float *state, void *out, int32_t N, int32_t H,
-                      int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+namespace {
+kda_status decode_common(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                         float *state, const int32_t *slots, int64_t pool, void *out, int32_t N,
+                         int32_t H, int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
 {
     if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
     if (Dk != Dv) return fail(KDA_ERR_UNSUPPORTED, "Dk (%d) != Dv (%d)", Dk, Dv);
@@ -236,10 +237,29 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
     if (((uintptr_t)state & 15) != 0) return fail(KDA_ERR_INVALID_ARG, "state must be 16-byte aligned");
     if (out == q || out == k || out == v || out == (void *)state)
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
-    cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype,
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype, slots, pool,
                                        (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     return KDA_OK;
+}
+}  // namespace
+
+kda_status kda_decode(const void *q, const void *k, const void *v, const float *g,
+                      const float *beta, float *state, void *out, int32_t N, int32_t H,
+                      int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+{
+    return decode_common(q, k, v, g, beta, state, nullptr, 0, out, N, H, Dk, Dv, dtype, stream);
+}
+
+kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state_pool, int64_t pool_slots,
+                            const int32_t *slot_ids, void *out, int32_t N, int32_t H, int32_t Dk,
+                            int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+{
+    if (pool_slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
+    if (N > 0 && H > 0 && !slot_ids) return fail(KDA_ERR_INVALID_ARG, "slot_ids is NULL");
+    return decode_common(q, k, v, g, beta, state_pool, slot_ids, pool_slots, out, N, H, Dk, Dv, dtype,
+                         stream);
 }
 
 }  // extern "C"

@@ -25,7 +25,8 @@ template <int D, typename T, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
-              float *__restrict__ state, T *__restrict__ out)
+              float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
+              int H, int64_t pool)
 {
     constexpr int C4 = D / 4;            // float4 groups per state row
     constexpr int RPI = THREADS / C4;    // rows covered per pass of the CTA
@@ -38,7 +39,19 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const int c4 = tid % C4;
     const int r0 = tid / C4;
 
-    float4 *S = reinterpret_cast<float4 *>(state + head * (size_t)D * D);
+    // The state of (sequence n, head h) is block `head` of `state`, or, with a
+    // slot table, block (slots[n], h) of a pool of `pool` slots; a slot outside
+    // [0, pool) marks a padding row: no state access, a zero output row.
+    size_t sblock = head;
+    if (slots) {
+        const int64_t sl = slots[head / (size_t)H];
+        if (sl < 0 || sl >= pool) {
+            if (tid < D) out[head * D + tid] = from_f32<T>(0.f);
+            return;
+        }
+        sblock = (size_t)sl * H + head % (size_t)H;
+    }
+    float4 *S = reinterpret_cast<float4 *>(state + sblock * (size_t)D * D);
 
     // Issue every state load first: RPT independent 16-byte loads per thread.
     float4 s[RPT];
@@ -125,12 +138,13 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
 template <int D, typename T>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
-                     const float *beta, float *state, void *out, int N, int H, cudaStream_t st)
+                     const float *beta, float *state, void *out, int N, int H,
+                     const int32_t *slots, int64_t pool, cudaStream_t st)
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
     decode_kernel<D, T, THREADS><<<blocks, THREADS, 0, st>>>(
-        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out);
+        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool);
     return cudaGetLastError();
 }
 
@@ -138,16 +152,16 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
-                          kda_dtype dtype, cudaStream_t stream)
+                          kda_dtype dtype, const int32_t *slots, int64_t pool, cudaStream_t stream)
 {
     if ((size_t)N * H == 0) return cudaSuccess;
     if (D == 128)
         return dtype == KDA_DTYPE_BF16
-                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, stream)
-                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, stream);
+                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, stream)
+                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, stream);
     return dtype == KDA_DTYPE_BF16
-               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, stream)
-               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, stream);
+               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, stream)
+               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, stream);
 }
 
 }  // namespace kda

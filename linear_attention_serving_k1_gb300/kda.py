@@ -22,7 +22,7 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
-           "kda_decode", "kda_prefill_noalloc", "kda_last_error", "kda_version")
+           "kda_decode", "kda_decode_paged", "kda_prefill_noalloc", "kda_last_error", "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -66,6 +66,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_prefill_status.argtypes = [_vp, _vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_decode_paged.restype = ctypes.c_int
+    lib.kda_decode_paged.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
     lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_noalloc.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp]
     lib.kda_last_error.restype = ctypes.c_char_p
@@ -211,5 +213,20 @@ def decode(q, k, v, g, beta, state, out=None, stream=None):
         out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
     code = load_library().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                                      _ptr(out), N, H, D, v.shape[2], _dtype_code(q), _stream(stream))
+    _check(code)
+    return out
+
+
+def decode_paged(q, k, v, g, beta, state_pool, slot_ids, out=None, stream=None):
+    """One decode step through ``kda_decode_paged``: sequence n reads and
+    updates slot ``slot_ids[n]`` of ``state_pool`` [P, H, D, D] (int32 ids on
+    the device; an id outside [0, P) marks a padding row with a zero output)."""
+    N, H, D = q.shape
+    if out is None:
+        out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
+    code = load_library().kda_decode_paged(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool),
+        ctypes.c_int64(state_pool.shape[0]), _ptr(slot_ids), _ptr(out), N, H, D, v.shape[2],
+        _dtype_code(q), _stream(stream))
     _check(code)
     return out

@@ -140,3 +140,20 @@ def test_decode_rejects_before_launch(lib):
     assert lib.kda_decode(p, p, p, p, p, p, p, 2, 2, 64, 64, 0, None) == -1     # out aliases q
     assert lib.kda_decode(p, p, p, p, p, p, o, 2, 2, 64, 64, 5, None) == -1     # dtype
     assert lib.kda_decode(p, p, p, p, p, p, o, 0, 2, 64, 64, 0, None) == 0      # empty: nothing to do
+
+
+def test_decode_paged_rejects_before_launch(lib):
+    p = ctypes.c_void_p(4096)
+    args = [p] * 6
+    # NULL slot ids with rows to decode
+    assert lib.kda_decode_paged(*args, ctypes.c_int64(8), None, ctypes.c_void_p(8192), 2, 2, 128, 128,
+                                kda.DTYPE_BF16, None) == -1
+    # negative pool size
+    assert lib.kda_decode_paged(*args, ctypes.c_int64(-1), p, ctypes.c_void_p(8192), 2, 2, 128, 128,
+                                kda.DTYPE_BF16, None) == -1
+    # unsupported head dim
+    assert lib.kda_decode_paged(*args, ctypes.c_int64(8), p, ctypes.c_void_p(8192), 2, 2, 96, 96,
+                                kda.DTYPE_BF16, None) == -2
+    # nothing to do
+    assert lib.kda_decode_paged(*args, ctypes.c_int64(8), None, ctypes.c_void_p(8192), 0, 2, 128, 128,
+                                kda.DTYPE_BF16, None) == 0

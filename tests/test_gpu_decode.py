@@ -63,3 +63,31 @@ def test_workload3_64_steps_sampled():
     print(f"workload 3: output {worst_o:.3e} state {worst_s:.3e}")
     assert worst_o <= TOL_OUT_BF16
     assert worst_s <= TOL_STATE
+
+
+@pytest.mark.parametrize("D,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_paged_decode_matches_gathered_states(D, dtype):
+    """Decode over a state pool through slot ids: the same bits as decoding the
+    gathered states; padding rows (slot -1) output zeros; other slots untouched."""
+    gen = torch.Generator(device="cpu").manual_seed(77)
+    N, H, P = 5, 4, 7
+    slots = torch.tensor([3, 0, -1, 6, 2], dtype=torch.int32)
+    pool = (0.05 * torch.randn(P, H, D, D, generator=gen)).cuda()
+    q = torch.randn(N, H, D, generator=gen).to(dtype).cuda()
+    k = torch.randn(N, H, D, generator=gen).to(dtype).cuda()
+    v = torch.randn(N, H, D, generator=gen).to(dtype).cuda()
+    g = (-torch.exp(torch.empty(N, H, D).uniform_(-5, -1, generator=gen))).cuda()
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).cuda()
+    valid = [i for i in range(N) if slots[i] >= 0]
+    gathered = pool[slots[valid].long()].clone()
+    out_ref = kda.decode(q[valid].contiguous(), k[valid].contiguous(), v[valid].contiguous(),
+                         g[valid].contiguous(), beta[valid].contiguous(), gathered)
+    pool2 = pool.clone()
+    out = kda.decode_paged(q, k, v, g, beta, pool2, slots.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out[valid], out_ref)
+    assert torch.count_nonzero(out[2]) == 0
+    for j, i in enumerate(valid):
+        assert torch.equal(pool2[slots[i]], gathered[j])
+    for s in (1, 4, 5):
+        assert torch.equal(pool2[s], pool[s])
