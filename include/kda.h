@@ -222,6 +222,24 @@ kda_status kda_decode_paged(const void *q, const void *k, const void *v, const f
                             const int32_t *slot_ids, void *out, int32_t N, int32_t H, int32_t Dk,
                             int32_t Dv, kda_dtype dtype, kda_stream_t stream);
 
+/*
+ * Multi-token decode (a speculative-decoding verify step): each sequence runs
+ * m tokens through the recurrence one after another with its state kept on
+ * chip.  q, k, g: [N, m, H, Dk]; v, out: [N, m, H, Dv]; beta: [N, m, H].  The
+ * state is dense [N, H, Dk, Dv] (slot_ids NULL, pool_slots ignored) or slot
+ * slot_ids[n] of a pool as in kda_decode_paged.  commit_len (int32 [N] on the
+ * device, or NULL for m) says after how many of its tokens each sequence's
+ * state is written back (0 = not at all): a verify call computes the outputs
+ * of all drafted tokens and commits the accepted prefix of the previous
+ * step's drafts, or commits nothing and a second call commits the accepted
+ * tokens.  Outputs of every token are written.  m = 1 with commit_len NULL is
+ * kda_decode (kda_decode_paged with slots).
+ */
+kda_status kda_decode_multi(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state, int64_t pool_slots, const int32_t *slot_ids,
+                            const int32_t *commit_len, void *out, int32_t N, int32_t m, int32_t H,
+                            int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *kda_last_error(void);
 

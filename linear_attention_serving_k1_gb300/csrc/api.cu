@@ -222,23 +222,24 @@ kda_status kda_prefill_status(void *workspace, kda_stream_t stream)
 
 namespace {
 kda_status decode_common(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                         float *state, const int32_t *slots, int64_t pool, void *out, int32_t N,
-                         int32_t H, int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+                         float *state, const int32_t *slots, int64_t pool, int32_t m,
+                         const int32_t *commit, void *out, int32_t N, int32_t H, int32_t Dk, int32_t Dv,
+                         kda_dtype dtype, kda_stream_t stream)
 {
-    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
+    if (N < 0 || H < 0 || m < 0) return fail(KDA_ERR_INVALID_ARG, "N, m and H must be >= 0");
+    if ((int64_t)N * m * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N*m*H too large");
     if (Dk != Dv) return fail(KDA_ERR_UNSUPPORTED, "Dk (%d) != Dv (%d)", Dk, Dv);
     if (Dk != 64 && Dk != 128) return fail(KDA_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", Dk);
     if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32)
         return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if ((size_t)N * H == 0) return KDA_OK;
-    if ((size_t)N * H > (size_t)INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N*H too large");
+    if ((size_t)N * H * m == 0) return KDA_OK;
     if (!q || !k || !v || !g || !beta || !state || !out)
         return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta, state and out must be non-NULL");
     if (((uintptr_t)state & 15) != 0) return fail(KDA_ERR_INVALID_ARG, "state must be 16-byte aligned");
     if (out == q || out == k || out == v || out == (void *)state)
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
-    cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype, slots, pool,
-                                       (cudaStream_t)stream);
+    cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype, slots, pool, m,
+                                       commit, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     return KDA_OK;
 }
@@ -248,7 +249,7 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
                       const float *beta, float *state, void *out, int32_t N, int32_t H,
                       int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
 {
-    return decode_common(q, k, v, g, beta, state, nullptr, 0, out, N, H, Dk, Dv, dtype, stream);
+    return decode_common(q, k, v, g, beta, state, nullptr, 0, 1, nullptr, out, N, H, Dk, Dv, dtype, stream);
 }
 
 kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,
@@ -258,8 +259,18 @@ kda_status kda_decode_paged(const void *q, const void *k, const void *v, const f
 {
     if (pool_slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
     if (N > 0 && H > 0 && !slot_ids) return fail(KDA_ERR_INVALID_ARG, "slot_ids is NULL");
-    return decode_common(q, k, v, g, beta, state_pool, slot_ids, pool_slots, out, N, H, Dk, Dv, dtype,
-                         stream);
+    return decode_common(q, k, v, g, beta, state_pool, slot_ids, pool_slots, 1, nullptr, out, N, H, Dk, Dv,
+                         dtype, stream);
+}
+
+kda_status kda_decode_multi(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state, int64_t pool_slots, const int32_t *slot_ids,
+                            const int32_t *commit_len, void *out, int32_t N, int32_t m, int32_t H,
+                            int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+{
+    if (slot_ids && pool_slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
+    return decode_common(q, k, v, g, beta, state, slot_ids, slot_ids ? pool_slots : 0, m, commit_len, out,
+                         N, H, Dk, Dv, dtype, stream);
 }
 
 }  // extern "C"

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(THREADS)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
-              int H, int64_t pool)
+              int H, int64_t pool, int m, const int32_t *__restrict__ commit)
 {
     constexpr int C4 = D / 4;            // float4 groups per state row
     constexpr int RPI = THREADS / C4;    // rows covered per pass of the CTA
@@ -34,23 +34,28 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     static_assert(THREADS % C4 == 0 && D % RPI == 0, "shape");
     constexpr int NW = THREADS / 32;
 
-    const size_t head = blockIdx.x;
+    const size_t head = blockIdx.x;      // (sequence n, head h) = n H + h
+    const size_t n = head / (size_t)H, hh = head % (size_t)H;
     const int tid = threadIdx.x;
     const int c4 = tid % C4;
     const int r0 = tid / C4;
 
     // The state of (sequence n, head h) is block `head` of `state`, or, with a
     // slot table, block (slots[n], h) of a pool of `pool` slots; a slot outside
-    // [0, pool) marks a padding row: no state access, a zero output row.
+    // [0, pool) marks a padding row: no state access, zero output rows.
     size_t sblock = head;
     if (slots) {
-        const int64_t sl = slots[head / (size_t)H];
+        const int64_t sl = slots[n];
         if (sl < 0 || sl >= pool) {
-            if (tid < D) out[head * D + tid] = from_f32<T>(0.f);
+            for (int t = 0; t < m; ++t)
+                if (tid < D) out[((n * m + t) * H + hh) * D + tid] = from_f32<T>(0.f);
             return;
         }
-        sblock = (size_t)sl * H + head % (size_t)H;
+        sblock = (size_t)sl * H + hh;
     }
+    // The sequence's m tokens run one after another with the state in
+    // registers; the state after `ncommit` of them is written back.
+    const int ncommit = commit ? min(max(commit[n], 0), m) : m;
     float4 *S = reinterpret_cast<float4 *>(state + sblock * (size_t)D * D);
 
     // Issue every state load first: RPT independent 16-byte loads per thread.
@@ -63,88 +68,94 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     __shared__ float4 red_k[RPI][C4];
     __shared__ float4 red_q[RPI][C4];
 
-    // Token vectors and the two L2 norms (fp32).
-    float qv = 0.f, kv = 0.f;
-    if (tid < D) {
-        qv = to_f32(q[head * D + tid]);
-        kv = to_f32(k[head * D + tid]);
-        sh_a[tid] = expf(g[head * D + tid]);
-    }
-    float pq = warp_sum(qv * qv), pk = warp_sum(kv * kv), pqk = warp_sum(qv * kv);
-    if ((tid & 31) == 0) {
-        sh_part[0][tid >> 5] = pq;
-        sh_part[1][tid >> 5] = pk;
-        sh_part[2][tid >> 5] = pqk;
-    }
-    __syncthreads();
-    float nq = 0.f, nk = 0.f, nqk = 0.f;
-#pragma unroll
-    for (int w = 0; w < (D + 31) / 32; ++w) {
-        nq += sh_part[0][w];
-        nk += sh_part[1][w];
-        nqk += sh_part[2][w];
-    }
-    const float rq = rsqrtf(nq + 1e-6f), rk = rsqrtf(nk + 1e-6f);
-    const float b = beta[head];
-    if (tid < D) {
-        sh_qh[tid] = qv * rq;
-        sh_kh[tid] = kv * rk;
-    }
-    __syncthreads();
-
-    // Decay in registers and accumulate S'^T kh and S'^T qh.
-    float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), aq = ak;
-#pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-        const int i = r0 + j * RPI;
-        const float a = sh_a[i], kh = sh_kh[i], qh = sh_qh[i];
-        s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
-        ak.x += kh * s[j].x; ak.y += kh * s[j].y; ak.z += kh * s[j].z; ak.w += kh * s[j].w;
-        aq.x += qh * s[j].x; aq.y += qh * s[j].y; aq.z += qh * s[j].z; aq.w += qh * s[j].w;
-    }
-    red_k[r0][c4] = ak;
-    red_q[r0][c4] = aq;
-    __syncthreads();
-
-    if (tid < D) {
-        const float *rk_ = reinterpret_cast<const float *>(&red_k[0][0]);
-        const float *rq_ = reinterpret_cast<const float *>(&red_q[0][0]);
-        float sk = 0.f, sq = 0.f;
-#pragma unroll
-        for (int r = 0; r < RPI; ++r) {
-            sk += rk_[r * D + tid];
-            sq += rq_[r * D + tid];
+    for (int t = 0; t < m; ++t) {
+        const size_t tok = (n * m + t) * H + hh;   // token-head row of q, k, v, g, beta, out
+        // Token vectors and the two L2 norms (fp32).
+        float qv = 0.f, kv = 0.f;
+        if (tid < D) {
+            qv = to_f32(q[tok * D + tid]);
+            kv = to_f32(k[tok * D + tid]);
+            sh_a[tid] = expf(g[tok * D + tid]);
         }
-        const float u = to_f32(v[head * D + tid]) - sk;
-        sh_u[tid] = u;
-        const float kq = nqk * rq * rk;   // kh . qh
-        out[head * D + tid] = from_f32<T>(sq + b * kq * u);
-    }
-    __syncthreads();
-
-    const float4 u4 = reinterpret_cast<const float4 *>(sh_u)[c4];
+        float pq = warp_sum(qv * qv), pk = warp_sum(kv * kv), pqk = warp_sum(qv * kv);
+        if ((tid & 31) == 0) {
+            sh_part[0][tid >> 5] = pq;
+            sh_part[1][tid >> 5] = pk;
+            sh_part[2][tid >> 5] = pqk;
+        }
+        __syncthreads();
+        float nq = 0.f, nk = 0.f, nqk = 0.f;
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-        const int i = r0 + j * RPI;
-        const float bk = b * sh_kh[i];
-        float4 o;
-        o.x = s[j].x + bk * u4.x;
-        o.y = s[j].y + bk * u4.y;
-        o.z = s[j].z + bk * u4.z;
-        o.w = s[j].w + bk * u4.w;
-        __stcs(S + (size_t)i * C4 + c4, o);
+        for (int w = 0; w < (D + 31) / 32; ++w) {
+            nq += sh_part[0][w];
+            nk += sh_part[1][w];
+            nqk += sh_part[2][w];
+        }
+        const float rq = rsqrtf(nq + 1e-6f), rk = rsqrtf(nk + 1e-6f);
+        const float b = beta[tok];
+        if (tid < D) {
+            sh_qh[tid] = qv * rq;
+            sh_kh[tid] = kv * rk;
+        }
+        __syncthreads();
+
+        // Decay in registers and accumulate S'^T kh and S'^T qh.
+        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), aq = ak;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int i = r0 + j * RPI;
+            const float a = sh_a[i], kh = sh_kh[i], qh = sh_qh[i];
+            s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
+            ak.x += kh * s[j].x; ak.y += kh * s[j].y; ak.z += kh * s[j].z; ak.w += kh * s[j].w;
+            aq.x += qh * s[j].x; aq.y += qh * s[j].y; aq.z += qh * s[j].z; aq.w += qh * s[j].w;
+        }
+        red_k[r0][c4] = ak;
+        red_q[r0][c4] = aq;
+        __syncthreads();
+
+        if (tid < D) {
+            const float *rk_ = reinterpret_cast<const float *>(&red_k[0][0]);
+            const float *rq_ = reinterpret_cast<const float *>(&red_q[0][0]);
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int r = 0; r < RPI; ++r) {
+                sk += rk_[r * D + tid];
+                sq += rq_[r * D + tid];
+            }
+            const float u = to_f32(v[tok * D + tid]) - sk;
+            sh_u[tid] = u;
+            const float kq = nqk * rq * rk;   // kh . qh
+            out[tok * D + tid] = from_f32<T>(sq + b * kq * u);
+        }
+        __syncthreads();
+
+        const float4 u4 = reinterpret_cast<const float4 *>(sh_u)[c4];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int i = r0 + j * RPI;
+            const float bk = b * sh_kh[i];
+            s[j].x += bk * u4.x;
+            s[j].y += bk * u4.y;
+            s[j].z += bk * u4.z;
+            s[j].w += bk * u4.w;
+        }
+        if (t + 1 == ncommit) {
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) __stcs(S + (size_t)(r0 + j * RPI) * C4 + c4, s[j]);
+        }
+        __syncthreads();   // shared vectors are rewritten by the next token
     }
 }
 
 template <int D, typename T>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, float *state, void *out, int N, int H,
-                     const int32_t *slots, int64_t pool, cudaStream_t st)
+                     const int32_t *slots, int64_t pool, int m, const int32_t *commit, cudaStream_t st)
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
     decode_kernel<D, T, THREADS><<<blocks, THREADS, 0, st>>>(
-        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool);
+        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit);
     return cudaGetLastError();
 }
 
@@ -152,16 +163,17 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
-                          kda_dtype dtype, const int32_t *slots, int64_t pool, cudaStream_t stream)
+                          kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
+                          const int32_t *commit, cudaStream_t stream)
 {
-    if ((size_t)N * H == 0) return cudaSuccess;
+    if ((size_t)N * H == 0 || m == 0) return cudaSuccess;
     if (D == 128)
         return dtype == KDA_DTYPE_BF16
-                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, stream)
-                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, stream);
+                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream)
+                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream);
     return dtype == KDA_DTYPE_BF16
-               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, stream)
-               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, stream);
+               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream)
+               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream);
 }
 
 }  // namespace kda

@@ -114,6 +114,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a);
 const char *launch_failure_detail();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
-                          kda_dtype dtype, const int32_t *slots, int64_t pool, cudaStream_t stream);
+                          kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
+                          const int32_t *commit, cudaStream_t stream);
 
 }  // namespace kda

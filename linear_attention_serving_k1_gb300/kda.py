@@ -22,7 +22,8 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
-           "kda_decode", "kda_decode_paged", "kda_prefill_noalloc", "kda_last_error", "kda_version")
+           "kda_decode", "kda_decode_paged", "kda_decode_multi", "kda_prefill_noalloc", "kda_last_error",
+           "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -68,6 +69,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
     lib.kda_decode_paged.restype = ctypes.c_int
     lib.kda_decode_paged.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_decode_multi.restype = ctypes.c_int
+    lib.kda_decode_multi.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
     lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_noalloc.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp]
     lib.kda_last_error.restype = ctypes.c_char_p
@@ -228,5 +231,21 @@ def decode_paged(q, k, v, g, beta, state_pool, slot_ids, out=None, stream=None):
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool),
         ctypes.c_int64(state_pool.shape[0]), _ptr(slot_ids), _ptr(out), N, H, D, v.shape[2],
         _dtype_code(q), _stream(stream))
+    _check(code)
+    return out
+
+
+def decode_multi(q, k, v, g, beta, state, commit_len=None, slot_ids=None, out=None, stream=None):
+    """m tokens per sequence through ``kda_decode_multi``: q, k, g [N, m, H, D],
+    v [N, m, H, D], beta [N, m, H]; ``state`` dense [N, H, D, D] or, with
+    ``slot_ids``, a pool [P, H, D, D]; ``commit_len`` int32 [N] on the device
+    (None: all m tokens) sets after how many tokens each state is written."""
+    N, m, H, D = q.shape
+    if out is None:
+        out = torch.empty(N, m, H, v.shape[3], dtype=q.dtype, device=q.device)
+    pool = state.shape[0] if slot_ids is not None else 0
+    code = load_library().kda_decode_multi(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.c_int64(pool),
+        _ptr(slot_ids), _ptr(commit_len), _ptr(out), N, m, H, D, v.shape[3], _dtype_code(q), _stream(stream))
     _check(code)
     return out

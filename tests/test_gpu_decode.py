@@ -91,3 +91,48 @@ def test_paged_decode_matches_gathered_states(D, dtype):
         assert torch.equal(pool2[slots[i]], gathered[j])
     for s in (1, 4, 5):
         assert torch.equal(pool2[s], pool[s])
+
+
+@pytest.mark.parametrize("D,dtype,tol", [(128, torch.bfloat16, TOL_OUT_BF16), (64, torch.float32, TOL_OUT_FP32)])
+def test_multi_token_decode_against_oracle(D, dtype, tol):
+    """m tokens per sequence in one call: every output follows the token
+    recurrence from the given state, and each state is written after its own
+    commit length (0 = untouched, m = all)."""
+    gen = torch.Generator(device="cpu").manual_seed(78)
+    N, m, H = 4, 5, 3
+    s0 = 0.05 * torch.randn(N, H, D, D, generator=gen, dtype=torch.float64)
+    q = torch.randn(N, m, H, D, generator=gen).to(dtype)
+    k = torch.randn(N, m, H, D, generator=gen).to(dtype)
+    v = torch.randn(N, m, H, D, generator=gen).to(dtype)
+    g = -torch.exp(torch.empty(N, m, H, D).uniform_(-5, -1, generator=gen))
+    beta = torch.sigmoid(torch.randn(N, m, H, generator=gen))
+    commit = torch.tensor([0, 2, 5, 1], dtype=torch.int32)
+    st = s0.float().cuda()
+    out = kda.decode_multi(q.cuda(), k.cuda(), v.cuda(), g.cuda(), beta.cuda(), st, commit.cuda())
+    torch.cuda.synchronize()
+    flat = lambda x: x.reshape(N * m, *x.shape[2:])
+    cu = np.arange(N + 1, dtype=np.int64) * m
+    o_r, _, _ = oracle.prefill(flat(q), flat(k), flat(v), flat(g), flat(beta), s0, cu)
+    assert out_err(to_np(out).reshape(N * m, H, D), o_r) <= tol
+    for n in range(N):
+        c = int(commit[n])
+        if c == 0:
+            assert torch.equal(st[n].cpu(), s0[n].float())   # untouched
+            continue
+        _, f_r, _ = oracle.prefill(q[n, :c], k[n, :c], v[n, :c], g[n, :c], beta[n, :c], s0[n:n + 1], None)
+        assert state_err(to_np(st[n]), f_r[0]) <= TOL_STATE
+
+
+def test_single_token_multi_decode_is_decode():
+    gen = torch.Generator(device="cpu").manual_seed(79)
+    N, H, D = 3, 4, 128
+    st = (0.05 * torch.randn(N, H, D, D, generator=gen)).cuda()
+    q, k, v = (torch.randn(N, H, D, generator=gen).to(torch.bfloat16).cuda() for _ in range(3))
+    g = (-torch.exp(torch.empty(N, H, D).uniform_(-5, -1, generator=gen))).cuda()
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).cuda()
+    st1, st2 = st.clone(), st.clone()
+    o1 = kda.decode(q, k, v, g, beta, st1)
+    o2 = kda.decode_multi(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None], st2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2[:, 0])
+    assert torch.equal(st1, st2)
