@@ -136,13 +136,15 @@ constexpr uint32_t K1_LM = 0;            // fp32 [64][65]  L (strict lower)
 constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
 constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][16] scratch of the 16 -> 32 merge
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
-constexpr uint32_t K1_XW = 46080;        // fp32 [32][32] scratch of the 32 -> 64 merge
+constexpr uint32_t K1_XW = 46080;        // fp32 [32][36] scratch of the 32 -> 64 merge
+constexpr int K1_XWP = 36;               // its row pitch (conflict-free float4 stores by 32 rows)
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
 constexpr uint32_t K1_UVT = 16384;       // f16 (diag(rk) Uv)^T: rows e x K = r
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_UVT + 16384 <= K1_MC, "later phases must fit the Gram region");
-static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 4096 <= K1_GRAM_END, "phase overlap");
+static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
+              "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
 
@@ -440,7 +442,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     }
     __syncthreads();
     {   // 16 -> 32, pairs k = 0, 1 (A = block 2k, B = block 2k + 1); thread: pair
-        // k, row i of B, columns j2, j2 + 1
+        // k, row i of B, columns j2, j2 + 1 (packed fp32 pairs)
         const int k2 = tid >> 7, i = (tid >> 3) & 15, j2 = (tid & 7) * 2;
         const int a0 = 32 * k2, b0 = a0 + 16;
         float2 s0 = make_float2(0.f, 0.f), s1 = s0;
@@ -450,53 +452,63 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const float2 t0 = *reinterpret_cast<const float2 *>(Tm + (a0 + m) * K1_P + a0 + j2);
             const float2 t1 = *reinterpret_cast<const float2 *>(Tm + (a0 + m + 1) * K1_P + a0 + j2);
             const float l0 = lrow[m], l1 = lrow[m + 1];
-            s0.x += l0 * t0.x; s0.y += l0 * t0.y;
-            s1.x += l1 * t1.x; s1.y += l1 * t1.y;
+            s0 = __ffma2_rn(make_float2(l0, l0), t0, s0);
+            s1 = __ffma2_rn(make_float2(l1, l1), t1, s1);
         }
-        *reinterpret_cast<float2 *>(Xs + (k2 * 16 + i) * 16 + j2) = make_float2(s0.x + s1.x, s0.y + s1.y);
+        *reinterpret_cast<float2 *>(Xs + (k2 * 16 + i) * 16 + j2) = __fadd2_rn(s0, s1);
         __syncthreads();
+        // T_BB is unit lower triangular: its row i ends at column i
         s0 = make_float2(0.f, 0.f);
-        s1 = s0;
         const float *trow = Tm + (b0 + i) * K1_P + b0;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            const float2 x0 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
-            const float2 x1 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m + 1) * 16 + j2);
-            const float u0 = trow[m], u1 = trow[m + 1];
-            s0.x += u0 * x0.x; s0.y += u0 * x0.y;
-            s1.x += u1 * x1.x; s1.y += u1 * x1.y;
+        for (int m = 0; m <= i; ++m) {
+            const float2 x = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
+            s0 = __ffma2_rn(make_float2(trow[m], trow[m]), x, s0);
         }
-        *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-(s0.x + s1.x), -(s0.y + s1.y));
+        *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-s0.x, -s0.y);
     }
     __syncthreads();
-    {   // 32 -> 64 (A = rows 0-31, B = rows 32-63); thread: row i of B, columns j4 .. j4 + 3
-        const int i = tid >> 3, j4 = (tid & 7) * 4;
-        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-        const float *lrow = Lm + (32 + i) * K1_PL;
-#pragma unroll 4
-        for (int m = 0; m < 32; m += 2) {
-            const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
-            const float4 t1 = *reinterpret_cast<const float4 *>(Tm + (m + 1) * K1_P + j4);
-            const float l0 = lrow[m], l1 = lrow[m + 1];
-            s0.x += l0 * t0.x; s0.y += l0 * t0.y; s0.z += l0 * t0.z; s0.w += l0 * t0.w;
-            s1.x += l1 * t1.x; s1.y += l1 * t1.y; s1.z += l1 * t1.z; s1.w += l1 * t1.w;
+    {   // 32 -> 64 (A = rows 0-31, B = rows 32-63).
+        // X = L_BA T_AA: thread = row i (lane), columns j4 .. j4 + 3 (warp): T_AA
+        // is lower triangular, so the sum starts at row j4 of T_AA, warp-uniformly
+        {
+            const int i = tid & 31, j4 = 4 * warp;
+            float2 s01 = make_float2(0.f, 0.f), s23 = s01, u01 = s01, u23 = s01;
+            const float *lrow = Lm + (32 + i) * K1_PL;
+            int m = j4;
+            for (; m + 1 < 32; m += 2) {
+                const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
+                const float4 t1 = *reinterpret_cast<const float4 *>(Tm + (m + 1) * K1_P + j4);
+                const float2 l0 = make_float2(lrow[m], lrow[m]), l1 = make_float2(lrow[m + 1], lrow[m + 1]);
+                s01 = __ffma2_rn(l0, make_float2(t0.x, t0.y), s01);
+                s23 = __ffma2_rn(l0, make_float2(t0.z, t0.w), s23);
+                u01 = __ffma2_rn(l1, make_float2(t1.x, t1.y), u01);
+                u23 = __ffma2_rn(l1, make_float2(t1.z, t1.w), u23);
+            }
+            if (m < 32) {
+                const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
+                const float2 l0 = make_float2(lrow[m], lrow[m]);
+                s01 = __ffma2_rn(l0, make_float2(t0.x, t0.y), s01);
+                s23 = __ffma2_rn(l0, make_float2(t0.z, t0.w), s23);
+            }
+            s01 = __fadd2_rn(s01, u01);
+            s23 = __fadd2_rn(s23, u23);
+            *reinterpret_cast<float4 *>(Xw + i * K1_XWP + j4) = make_float4(s01.x, s01.y, s23.x, s23.y);
         }
-        *reinterpret_cast<float4 *>(Xw + i * 32 + j4) =
-            make_float4(s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w);
         __syncthreads();
-        s0 = make_float4(0.f, 0.f, 0.f, 0.f);
-        s1 = s0;
-        const float *trow = Tm + (32 + i) * K1_P + 32;
-#pragma unroll 4
-        for (int m = 0; m < 32; m += 2) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(Xw + m * 32 + j4);
-            const float4 x1 = *reinterpret_cast<const float4 *>(Xw + (m + 1) * 32 + j4);
-            const float u0 = trow[m], u1 = trow[m + 1];
-            s0.x += u0 * x0.x; s0.y += u0 * x0.y; s0.z += u0 * x0.z; s0.w += u0 * x0.w;
-            s1.x += u1 * x1.x; s1.y += u1 * x1.y; s1.z += u1 * x1.z; s1.w += u1 * x1.w;
+        // T_BA = -T_BB X: thread = row i, columns j4 .. j4 + 3; T_BB's row i ends
+        // at column i
+        {
+            const int i = tid >> 3, j4 = (tid & 7) * 4;
+            float2 s01 = make_float2(0.f, 0.f), s23 = s01;
+            const float *trow = Tm + (32 + i) * K1_P + 32;
+            for (int m = 0; m <= i; ++m) {
+                const float4 x = *reinterpret_cast<const float4 *>(Xw + m * K1_XWP + j4);
+                const float2 tv = make_float2(trow[m], trow[m]);
+                s01 = __ffma2_rn(tv, make_float2(x.x, x.y), s01);
+                s23 = __ffma2_rn(tv, make_float2(x.z, x.w), s23);
+            }
+            *reinterpret_cast<float4 *>(Tm + (32 + i) * K1_P + j4) = make_float4(-s01.x, -s01.y, -s23.x, -s23.y);
         }
-        *reinterpret_cast<float4 *>(Tm + (32 + i) * K1_P + j4) =
-            make_float4(-(s0.x + s1.x), -(s0.y + s1.y), -(s0.z + s1.z), -(s0.w + s1.w));
     }
     __syncthreads();
 
