@@ -173,7 +173,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
-    __shared__ float rq[kC], rk[kC], bs[kC];
+    // (16-byte aligned: read as float2 / float4)
+    __shared__ __align__(16) float rq[kC];
+    __shared__ __align__(16) float rk[kC];
+    __shared__ __align__(16) float bs[kC];
     __shared__ int wflag[4];           // MMA waits: one thread polls, the barrier releases the rest
 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
@@ -281,30 +284,32 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const float gam0 = __expf(last0), gam1 = __expf(last1);
         if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
         uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4];
-        float b0 = pre0, b1 = pre1;
+        // the two channels of a thread as packed fp32 pairs
+        float2 bb = make_float2(pre0, pre1);
+        const float2 gam2 = make_float2(gam0, gam1);
 #pragma unroll
         for (int j2 = 0; j2 < 8; j2 += 2) {
             float kgx[2][2], vx[2][2], kex[2][2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int j = j2 + u, r = rb + j;
-                b0 += gv[j].x;
-                b1 += gv[j].y;
-                const float e0 = __expf(b0), e1 = __expf(b1), i0 = __expf(-b0), i1 = __expf(-b1);
-                const float q0 = bf_lo(qv[j]), q1 = bf_hi(qv[j]), k0 = bf_lo(kv[j]), k1 = bf_hi(kv[j]);
-                const float kg_0 = k0 * e0, kg_1 = k1 * e1, qg_0 = q0 * e0, qg_1 = q1 * e1;
-                const float kd_0 = k0 * i0, kd_1 = k1 * i1;
+                bb = __fadd2_rn(bb, gv[j]);
+                const float2 e = make_float2(__expf(bb.x), __expf(bb.y));
+                const float2 ei = make_float2(__expf(-bb.x), __expf(-bb.y));
+                const float2 qq = make_float2(bf_lo(qv[j]), bf_hi(qv[j])), kk = make_float2(bf_lo(kv[j]), bf_hi(kv[j]));
+                const float2 kg = __fmul2_rn(kk, e), qg = __fmul2_rn(qq, e), kd = __fmul2_rn(kk, ei);
+                const float2 ke = __fmul2_rn(kd, gam2);   // k' e^(b_last - b)
                 const uint32_t lo = 2 * lane;
                 *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(kg_0), round_tf32(kg_1));
+                    make_float2(round_tf32(kg.x), round_tf32(kg.y));
                 *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(64 + r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(qg_0), round_tf32(qg_1));
+                    make_float2(round_tf32(qg.x), round_tf32(qg.y));
                 *reinterpret_cast<float2 *>(sm + K1_KD + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(kd_0), round_tf32(kd_1));
-                *reinterpret_cast<float2 *>(qg_park + (size_t)r * kD + d) = make_float2(qg_0, qg_1);
-                kgx[0][u] = kg_0; kgx[1][u] = kg_1;
+                    make_float2(round_tf32(kd.x), round_tf32(kd.y));
+                *reinterpret_cast<float2 *>(qg_park + (size_t)r * kD + d) = qg;
+                kgx[0][u] = kg.x; kgx[1][u] = kg.y;
                 vx[0][u] = bf_lo(vv[j]); vx[1][u] = bf_hi(vv[j]);
-                kex[0][u] = kd_0 * gam0; kex[1][u] = kd_1 * gam1;   // k' e^(b_last - b)
+                kex[0][u] = ke.x; kex[1][u] = ke.y;
             }
             kg0[j2 / 2] = pack_f16x2(kgx[0][0], kgx[0][1]);
             kg1[j2 / 2] = pack_f16x2(kgx[1][0], kgx[1][1]);
@@ -398,10 +403,14 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         if (row < 64) {
             const int r = row;
             const float sr = bs[r] * rk[r];
+            const float2 sr2 = make_float2(sr, sr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 32; i += 2) {
                 const int col = 32 * ch + i;
-                Lm[r * K1_PL + col] = (col < r) ? sr * rk[col] * gq[i] : 0.f;
+                const float2 lv = __fmul2_rn(__fmul2_rn(sr2, *reinterpret_cast<const float2 *>(rk + col)),
+                                             make_float2(gq[i], gq[i + 1]));
+                Lm[r * K1_PL + col] = (col < r) ? lv.x : 0.f;
+                Lm[r * K1_PL + col + 1] = (col + 1 < r) ? lv.y : 0.f;
             }
         } else {
             const int r = row - 64;
@@ -525,11 +534,19 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int j4 = 0; j4 < 8; j4 += 4) {
                 const float4 t4 = *reinterpret_cast<const float4 *>(Tm + r * K1_P + i0 + i8 + j4);
                 const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+                const int ib = i0 + i8 + j4;
+                const float4 b4 = *reinterpret_cast<const float4 *>(bs + ib);
+                const float4 k4 = *reinterpret_cast<const float4 *>(rk + ib);
+                const float2 v01 = __fmul2_rn(make_float2(tt[0], tt[1]), make_float2(b4.x, b4.y));
+                const float2 v23 = __fmul2_rn(make_float2(tt[2], tt[3]), make_float2(b4.z, b4.w));
+                const float2 k01 = __fmul2_rn(v01, make_float2(k4.x, k4.y));
+                const float2 k23 = __fmul2_rn(v23, make_float2(k4.z, k4.w));
+                const float vv4[4] = {v01.x, v01.y, v23.x, v23.y}, kk4[4] = {k01.x, k01.y, k23.x, k23.y};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + i8 + j4 + u;
-                    tv[j4 + u] = i <= r ? tt[u] * bs[i] : 0.f;
-                    tk[j4 + u] = tv[j4 + u] * rk[i];
+                    const bool in = ib + u <= r;
+                    tv[j4 + u] = in ? vv4[u] : 0.f;
+                    tk[j4 + u] = in ? kk4[u] : 0.f;
                 }
             }
             const uint32_t o = kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64);
@@ -571,10 +588,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tmem_ld16(tm + lane_base + T1_W2 + 32 * ch + c, u);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float s = rk[32 * ch + c + j];
-                w[j] *= s;
-                u[j] *= s;
+            for (int j = 0; j < 16; j += 2) {
+                const float2 s2 = *reinterpret_cast<const float2 *>(rk + 32 * ch + c + j);
+                const float2 w2 = __fmul2_rn(make_float2(w[j], w[j + 1]), s2);
+                const float2 u2 = __fmul2_rn(make_float2(u[j], u[j + 1]), s2);
+                w[j] = w2.x; w[j + 1] = w2.y;
+                u[j] = u2.x; u[j + 1] = u2.y;
             }
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8) {
@@ -897,10 +916,11 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                     for (int j4 = 0; j4 < 16; j4 += 4) {
                         const int j = h16 + j4;
                         const float4 g4 = *reinterpret_cast<const float4 *>(gam + j);
-                        S[j] = fmaf(g4.x, S[j], p[j4]);
-                        S[j + 1] = fmaf(g4.y, S[j + 1], p[j4 + 1]);
-                        S[j + 2] = fmaf(g4.z, S[j + 2], p[j4 + 2]);
-                        S[j + 3] = fmaf(g4.w, S[j + 3], p[j4 + 3]);
+                        const float2 s01 = __ffma2_rn(make_float2(g4.x, g4.y), make_float2(S[j], S[j + 1]),
+                                                      make_float2(p[j4], p[j4 + 1]));
+                        const float2 s23 = __ffma2_rn(make_float2(g4.z, g4.w), make_float2(S[j + 2], S[j + 3]),
+                                                      make_float2(p[j4 + 2], p[j4 + 3]));
+                        S[j] = s01.x; S[j + 1] = s01.y; S[j + 2] = s23.x; S[j + 3] = s23.y;
                     }
                 }
             }
