@@ -354,7 +354,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // 32 (tid & 3) .. + 31 of q and k (rows this CTA has just read: cache hits)
     {
         const int r = tid >> 2, part = tid & 3;
-        float sqq = 0.f, sqk = 0.f;
+        float2 sqk2 = make_float2(0.f, 0.f);   // (sum of q^2, sum of k^2)
         if (r < L) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(qrow + (size_t)r * rstride + 32 * part);
             const uint4 *kp = reinterpret_cast<const uint4 *>(krow + (size_t)r * rstride + 32 * part);
@@ -367,11 +367,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 const uint32_t kw[4] = {ka[j].x, ka[j].y, ka[j].z, ka[j].w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    sqq += bf_lo(qw[u]) * bf_lo(qw[u]) + bf_hi(qw[u]) * bf_hi(qw[u]);
-                    sqk += bf_lo(kw[u]) * bf_lo(kw[u]) + bf_hi(kw[u]) * bf_hi(kw[u]);
+                    const float2 lo = make_float2(bf_lo(qw[u]), bf_lo(kw[u])), hi = make_float2(bf_hi(qw[u]), bf_hi(kw[u]));
+                    sqk2 = __ffma2_rn(lo, lo, sqk2);
+                    sqk2 = __ffma2_rn(hi, hi, sqk2);
                 }
             }
         }
+        float sqq = sqk2.x, sqk = sqk2.y;
         sqq += __shfl_xor_sync(0xffffffffu, sqq, 1);
         sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
         sqq += __shfl_xor_sync(0xffffffffu, sqq, 2);
@@ -578,7 +580,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
     ok = ok && wflag[2];
 
-    // 8. (diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
+    // 8. (-diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
 #pragma unroll
@@ -590,7 +592,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
                 const float2 s2 = *reinterpret_cast<const float2 *>(rk + 32 * ch + c + j);
-                const float2 w2 = __fmul2_rn(make_float2(w[j], w[j + 1]), s2);
+                // Wk's tile carries -rk: the products of phase 9 come out as A'
+                // and -Mc Wk directly
+                const float2 w2 = __fmul2_rn(make_float2(w[j], w[j + 1]), make_float2(-s2.x, -s2.y));
                 const float2 u2 = __fmul2_rn(make_float2(u[j], u[j + 1]), s2);
                 w[j] = w2.x; w[j + 1] = w2.y;
                 u[j] = u2.x; u[j + 1] = u2.y;
@@ -608,7 +612,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // 9. A'acc = Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); Q'acc = Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
+    // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); -Mc Wk = -Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
     if (tid == 0 && ok) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
@@ -634,36 +638,33 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) qpk[j4] = __ldcg(src + j4);
         }
-        // 10. A' = -(Ke^T Wk) -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
+        // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
             float a[16];
             tmem_ld16(tm + lane_base + T1_AP + 64 * ch + c, a);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) a[j] = -a[j];
-#pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8)
                 *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
                     pack_f16x8(a + h8);
         }
-        // 11. Q' = diag(rq) Qg' - Mc Wk: the M = 64 accumulator puts row r = 16 q4 + l
-        //     in lane 32 q4 + l (l < 16)
+        // 11. Q' = diag(rq) Qg' + (-Mc Wk): the M = 64 accumulator puts row
+        //     r = 16 q4 + l in lane 32 q4 + l (l < 16)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
             float a[16];
             tmem_ld16(tm + lane_base + T1_QP + 64 * ch + c, a);
             tmem_ld_wait();
             if (lane < 16) {
-                const float sr = rq[r];
+                const float2 sr2 = make_float2(rq[r], rq[r]);
                 float qd[16];
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4) {
                     const float4 t = qpk[c / 4 + j4];
-                    qd[4 * j4] = sr * t.x - a[4 * j4];
-                    qd[4 * j4 + 1] = sr * t.y - a[4 * j4 + 1];
-                    qd[4 * j4 + 2] = sr * t.z - a[4 * j4 + 2];
-                    qd[4 * j4 + 3] = sr * t.w - a[4 * j4 + 3];
+                    const float2 lo = __ffma2_rn(sr2, make_float2(t.x, t.y), make_float2(a[4 * j4], a[4 * j4 + 1]));
+                    const float2 hi = __ffma2_rn(sr2, make_float2(t.z, t.w), make_float2(a[4 * j4 + 2], a[4 * j4 + 3]));
+                    qd[4 * j4] = lo.x; qd[4 * j4 + 1] = lo.y; qd[4 * j4 + 2] = hi.x; qd[4 * j4 + 3] = hi.y;
                 }
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8)
