@@ -137,6 +137,7 @@ constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
 constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][16] scratch of the 16 -> 32 merge
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
 constexpr uint32_t K1_XW = 46080;        // fp32 [32][36] scratch of the 32 -> 64 merge
+constexpr uint32_t K1_RQD = 46080;       // f16 diag(rq): rows i x K = r (64 x 64), over XW after the inverse
 constexpr int K1_XWP = 36;               // its row pitch (conflict-free float4 stores by 32 rows)
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
@@ -170,7 +171,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
              DevStatus *st)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t mbar;
+    __shared__ uint64_t mbar, qbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
     // (16-byte aligned: read as float2 / float4)
@@ -203,10 +204,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int t0 = tab.cu[n] + lc * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
-    // Qg' in fp32 [r][d] (32 KB) parks in the record's Ke^T / Mc / Uv^T area
-    // (written last) until phase 11
-    float *qg_park = reinterpret_cast<float *>(rec + REC_KM);
-    static_assert(REC_KM + 32768 <= REC_G, "park area");
+    // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in the record's
+    // Ke^T area (written last) until phase 9 copies it back into shared memory
+    uint8_t *qg_park = rec + REC_KM;
+    static_assert(REC_KM + 16384 <= REC_G, "park area");
 
     // 0. inputs of the first channel half.  Thread: rows rb .. rb + 7 of its
     //    warp, channels 64 p + 2 lane and + 1 of half p (4-byte bf16 pairs,
@@ -247,6 +248,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     }
     if (tid == 0) {
         mbar_init(&mbar, 1);
+        mbar_init(&qbar, 1);
         fence_mbar_init();
     }
     fence_before_sync();
@@ -283,13 +285,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         const float gam0 = __expf(last0), gam1 = __expf(last1);
         if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
-        uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4];
+        uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4], qp0[4], qp1[4];
         // the two channels of a thread as packed fp32 pairs
         float2 bb = make_float2(pre0, pre1);
         const float2 gam2 = make_float2(gam0, gam1);
 #pragma unroll
         for (int j2 = 0; j2 < 8; j2 += 2) {
-            float kgx[2][2], vx[2][2], kex[2][2];
+            float kgx[2][2], vx[2][2], kex[2][2], qgx[2][2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int j = j2 + u, r = rb + j;
@@ -306,11 +308,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     make_float2(round_tf32(qg.x), round_tf32(qg.y));
                 *reinterpret_cast<float2 *>(sm + K1_KD + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
                     make_float2(round_tf32(kd.x), round_tf32(kd.y));
-                *reinterpret_cast<float2 *>(qg_park + (size_t)r * kD + d) = qg;
+                qgx[0][u] = qg.x; qgx[1][u] = qg.y;
                 kgx[0][u] = kg.x; kgx[1][u] = kg.y;
                 vx[0][u] = bf_lo(vv[j]); vx[1][u] = bf_hi(vv[j]);
                 kex[0][u] = ke.x; kex[1][u] = ke.y;
             }
+            qp0[j2 / 2] = pack_f16x2(qgx[0][0], qgx[0][1]);
+            qp1[j2 / 2] = pack_f16x2(qgx[1][0], qgx[1][1]);
             kg0[j2 / 2] = pack_f16x2(kgx[0][0], kgx[0][1]);
             kg1[j2 / 2] = pack_f16x2(kgx[1][0], kgx[1][1]);
             vf0[j2 / 2] = pack_f16x2(vx[0][0], vx[0][1]);
@@ -335,6 +339,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             K1_PAIR_STORE(K1_KET, ke0, ke1)
 #undef K1_PAIR_STORE
         }
+        // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
+        *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
+        *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
+        fence_async_global();   // the bulk copy of phase 8 reads these through the async proxy
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -580,6 +588,20 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
     ok = ok && wflag[2];
 
+    // the Kg'^T tile is dead: the parked Qg'^T tile comes back into its place
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(&qbar, 16384);
+        bulk_g2s(sm + K1_KGT, qg_park, 16384, &qbar);
+    }
+    // diag(rq) as an f16 operand tile (rows i, K = r; 64 x 64) for Q' = diag(rq) Qg' - Mc Wk
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int idx = tid + K1_THREADS * h, i = idx >> 3, kg = idx & 7;
+        float dv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dv[j] = (8 * kg + j == i) ? rq[i] : 0.f;
+        *reinterpret_cast<uint4 *>(sm + K1_RQD + kmaj_off(i, 8 * kg, LBO_KIN, SBO_K64)) = pack_f16x8(dv);
+    }
     // 8. (-diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
@@ -613,8 +635,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); -Mc Wk = -Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
-    if (tid == 0 && ok) {
+    if (tid == 0 && ok && mbar_wait_bounded(&qbar, 0, kWaitLimit)) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
+        const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_KGT);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -622,6 +645,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             mma_f16(tm + T1_AP, make_desc(ake + ks * 256, LBO_KIN, SBO_K64), bd, id128, ks > 0);
             mma_f16(tm + T1_QP, make_desc(amc + ks * 256, LBO_KIN, SBO_K64), bd, id64, ks > 0);
         }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tm + T1_QP, make_desc(ard + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(bq + ks * 256, LBO_KIN, SBO_K64), id64, 1);
         mma_commit(&mbar);
     }
     if (tid == 0) wflag[3] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
@@ -630,14 +657,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     ok = ok && wflag[3];
 
     if (ok) {
-        // the parked Qg' row of phase 11 (lanes < 16), in flight during phase 10
         const int r = 16 * q4 + lane;
-        float4 qpk[16];
-        if (lane < 16) {
-            const float4 *src = reinterpret_cast<const float4 *>(qg_park + (size_t)r * kD + 64 * ch);
-#pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) qpk[j4] = __ldcg(src + j4);
-        }
         // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
@@ -649,27 +669,18 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
                     pack_f16x8(a + h8);
         }
-        // 11. Q' = diag(rq) Qg' + (-Mc Wk): the M = 64 accumulator puts row
-        //     r = 16 q4 + l in lane 32 q4 + l (l < 16)
+        // 11. Q' -> record: the M = 64 accumulator puts row r = 16 q4 + l in lane
+        //     32 q4 + l (l < 16)
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
             float a[16];
             tmem_ld16(tm + lane_base + T1_QP + 64 * ch + c, a);
             tmem_ld_wait();
             if (lane < 16) {
-                const float2 sr2 = make_float2(rq[r], rq[r]);
-                float qd[16];
-#pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 t = qpk[c / 4 + j4];
-                    const float2 lo = __ffma2_rn(sr2, make_float2(t.x, t.y), make_float2(a[4 * j4], a[4 * j4 + 1]));
-                    const float2 hi = __ffma2_rn(sr2, make_float2(t.z, t.w), make_float2(a[4 * j4 + 2], a[4 * j4 + 3]));
-                    qd[4 * j4] = lo.x; qd[4 * j4 + 1] = lo.y; qd[4 * j4 + 2] = hi.x; qd[4 * j4 + 3] = hi.y;
-                }
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8)
                     *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
-                        pack_f16x8(qd + h8);
+                        pack_f16x8(a + h8);
             }
         }
     }

@@ -85,6 +85,13 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Orders this thread's earlier generic-proxy global writes before later
+// async-proxy (bulk copy) reads of them.
+__device__ __forceinline__ void fence_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Pulls one 128-byte line into L2 (no register result, no completion to wait for).
 __device__ __forceinline__ void prefetch_l2_line(const void *p)
 {
