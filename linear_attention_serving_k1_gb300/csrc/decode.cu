@@ -21,13 +21,14 @@
 namespace kda {
 namespace {
 
-template <int D, typename T, int THREADS>
+template <int D, typename T, int THREADS, bool MULTI>
 __global__ void __launch_bounds__(THREADS)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
-              int H, int64_t pool, int m, const int32_t *__restrict__ commit)
+              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit)
 {
+    const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
     constexpr int RPI = THREADS / C4;    // rows covered per pass of the CTA
     constexpr int RPT = D / RPI;         // rows per thread
@@ -55,7 +56,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     }
     // The sequence's m tokens run one after another with the state in
     // registers; the state after `ncommit` of them is written back.
-    const int ncommit = commit ? min(max(commit[n], 0), m) : m;
+    const int ncommit = (MULTI && commit) ? min(max(commit[n], 0), m) : m;
     float4 *S = reinterpret_cast<float4 *>(state + sblock * (size_t)D * D);
 
     // Issue every state load first: RPT independent 16-byte loads per thread.
@@ -154,8 +155,12 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
-    decode_kernel<D, T, THREADS><<<blocks, THREADS, 0, st>>>(
-        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit);
+    if (m == 1 && !commit)
+        decode_kernel<D, T, THREADS, false><<<blocks, THREADS, 0, st>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr);
+    else
+        decode_kernel<D, T, THREADS, true><<<blocks, THREADS, 0, st>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit);
     return cudaGetLastError();
 }
 
