@@ -342,7 +342,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
         *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
         *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
-        fence_async_global();   // the bulk copy of phase 8 reads these through the async proxy
+        if (p == 1) fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
