@@ -115,8 +115,8 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 //   Ke^T Wk = Ke'^T diag(rk) Wk,  Mc Wk = Mc' diag(rk) Wk  (Mc' = diag(rq) G'_qk)
 //   Ke^T Uv = Ke'^T diag(rk) Uv,  Mc Uv = Mc' diag(rk) Uv,   Qg = diag(rq) Qg'
 // so the operands are built in one pass over the inputs, in two halves of the
-// key channels (the Gram product accumulates over both), and the norms are
-// reduced while the Gram product runs.  Un-normalised f16 operands require |k| < 65504.
+// key channels (the Gram product accumulates over both), and the squared row
+// norms are summed from the same registers.  Un-normalised f16 operands require |k| < 65504.
 //
 // Shared memory map (bytes).  [0, 55296) holds one key-channel half of the
 // tf32 Gram operands and is reused by the later phases.
@@ -142,8 +142,7 @@ constexpr int K1_XWP = 36;               // its row pitch (conflict-free float4 
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
-constexpr uint32_t K1_UVT = 16384;       // f16 (diag(rk) Uv)^T: rows e x K = r
-static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_UVT + 16384 <= K1_MC, "later phases must fit the Gram region");
+static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
 static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
@@ -205,9 +204,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
     // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in the record's
-    // Ke^T area (written last) until phase 9 copies it back into shared memory
-    uint8_t *qg_park = rec + REC_KM;
-    static_assert(REC_KM + 16384 <= REC_G, "park area");
+    // A' area (written once the product that reads it back is complete) until
+    // phase 9 copies it into shared memory
+    uint8_t *qg_park = rec + REC_AP;
+    static_assert(REC_AP + 16384 <= REC_QP, "park area");
 
     // 0. inputs of the first channel half.  Thread: rows rb .. rb + 7 of its
     //    warp, channels 64 p + 2 lane and + 1 of half p (4-byte bf16 pairs,
@@ -222,7 +222,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     float2 gv[8];
     uint32_t qv[8], kv[8], vv[8];
     auto load_half = [&](int p) {
-        const int d = 64 * p + 2 * lane;
+        int d = 64 * p + 2 * lane;
+        asm volatile("" : "+r"(d));   // keeps the second half's loads after its barrier (registers)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int r = rb + j;
@@ -256,11 +257,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
     const uint32_t tm = tmem_sh;
     bool ok = true;
+    float nsq = 0.f;   // squared row norm of value lane >> 1 (q rows rb .. rb + 7, then k rows)
 
     // 1-3. per channel half p: cumulative gates, decayed operands, partial row
     //      norms; then the half's share of G' = [Kg'; Qg'] Kd'^T (tf32, M = 128,
     //      N = 64, K = 64: 8 instructions of K = 8, accumulating over the halves)
-#pragma unroll 1
+#pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int d = 64 * p + 2 * lane;
         {
@@ -286,6 +288,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const float gam0 = __expf(last0), gam1 = __expf(last1);
         if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
         uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4], qp0[4], qp1[4];
+        // this half's squared row norms, summed over the warp's 32 lanes by
+        // halving exchanges: the exchange across lane bit 4 leaves q of row
+        // rb + j (bit 4 clear) or k (set) in sq[j], bit 3 keeps four of those
+        // rows, and so on, so that lanes 2i and 2i + 1 end with value i (q rows
+        // rb .. rb + 7, then k rows)
+        float sq[8];
+        const bool up16 = lane & 16;
         // the two channels of a thread as packed fp32 pairs
         float2 bb = make_float2(pre0, pre1);
         const float2 gam2 = make_float2(gam0, gam1);
@@ -299,6 +308,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 const float2 e = make_float2(__expf(bb.x), __expf(bb.y));
                 const float2 ei = make_float2(__expf(-bb.x), __expf(-bb.y));
                 const float2 qq = make_float2(bf_lo(qv[j]), bf_hi(qv[j])), kk = make_float2(bf_lo(kv[j]), bf_hi(kv[j]));
+                const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
+                const float2 s2 = __ffma2_rn(qk1, qk1, __fmul2_rn(qk0, qk0));
+                sq[j] = (up16 ? s2.y : s2.x) + __shfl_xor_sync(0xffffffffu, up16 ? s2.x : s2.y, 16);
                 const float2 kg = __fmul2_rn(kk, e), qg = __fmul2_rn(qq, e), kd = __fmul2_rn(kk, ei);
                 const float2 ke = __fmul2_rn(kd, gam2);   // k' e^(b_last - b)
                 const uint32_t lo = 2 * lane;
@@ -342,7 +354,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
         *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
         *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
-        if (p == 1) fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1) {
+            const bool up = lane & (2 * w);
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const float send = up ? sq[i] : sq[i + w], keep = up ? sq[i + w] : sq[i];
+                sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            }
+        }
+        nsq += sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
+        if (p == 1) {
+            fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
+            if ((lane & 1) == 0) {
+                const int i = lane >> 1, r = rb + (i & 7);
+                (i < 8 ? rq : rk)[r] = r < L ? rsqrtf(nsq + 1e-6f) : 0.f;
+            }
+        }
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -358,41 +386,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             mma_commit(&mbar);
         }
     }
-    // row norms while the Gram product runs: thread -> row tid / 4, channels
-    // 32 (tid & 3) .. + 31 of q and k (rows this CTA has just read: cache hits)
-    {
-        const int r = tid >> 2, part = tid & 3;
-        float2 sqk2 = make_float2(0.f, 0.f);   // (sum of q^2, sum of k^2)
-        if (r < L) {
-            const uint4 *qp = reinterpret_cast<const uint4 *>(qrow + (size_t)r * rstride + 32 * part);
-            const uint4 *kp = reinterpret_cast<const uint4 *>(krow + (size_t)r * rstride + 32 * part);
-            uint4 qa[4], ka[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) { qa[j] = __ldg(qp + j); ka[j] = __ldg(kp + j); }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t qw[4] = {qa[j].x, qa[j].y, qa[j].z, qa[j].w};
-                const uint32_t kw[4] = {ka[j].x, ka[j].y, ka[j].z, ka[j].w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 lo = make_float2(bf_lo(qw[u]), bf_lo(kw[u])), hi = make_float2(bf_hi(qw[u]), bf_hi(kw[u]));
-                    sqk2 = __ffma2_rn(lo, lo, sqk2);
-                    sqk2 = __ffma2_rn(hi, hi, sqk2);
-                }
-            }
-        }
-        float sqq = sqk2.x, sqk = sqk2.y;
-        sqq += __shfl_xor_sync(0xffffffffu, sqq, 1);
-        sqk += __shfl_xor_sync(0xffffffffu, sqk, 1);
-        sqq += __shfl_xor_sync(0xffffffffu, sqq, 2);
-        sqk += __shfl_xor_sync(0xffffffffu, sqk, 2);
-        if (part == 0) {
-            rq[r] = r < L ? rsqrtf(sqq + 1e-6f) : 0.f;
-            rk[r] = r < L ? rsqrtf(sqk + 1e-6f) : 0.f;
-        }
-    }
     if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
-    __syncthreads();   // G' complete and seen by all: the Gram region may be reused; norms visible
+    __syncthreads();   // G' complete and seen by all: the Gram region may be reused
     fence_after_sync();
     ok = ok && wflag[1];
 
@@ -453,10 +448,16 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             Tm[r * K1_P + col] = tcol[rr];
         }
     } else {
-        for (int idx = tid - 64; idx < 64 * 16; idx += K1_THREADS - 64) {
-            const int r = idx >> 4, j4 = (idx & 15) * 4;
-            if ((j4 >> 4) > (r >> 4))
-                *reinterpret_cast<float4 *>(Tm + r * K1_P + j4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        // meanwhile Ke'^T and Mc', already K2's operand tiles, go to the record
+        // (Ke'^T then Mc' are contiguous there: 1536 16-byte pieces)
+        const uint4 *ket = reinterpret_cast<const uint4 *>(sm + K1_KET);
+        const uint4 *mc = reinterpret_cast<const uint4 *>(sm + K1_MC);
+        uint4 *dkm = reinterpret_cast<uint4 *>(rec + REC_KM);
+        static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = tid - 64 + (K1_THREADS - 64) * j;
+            dkm[i] = i < 1024 ? ket[i] : mc[i - 1024];
         }
     }
     __syncthreads();
@@ -515,7 +516,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         __syncthreads();
         // T_BA = -T_BB X: thread = row i, columns j4 .. j4 + 3; T_BB's row i ends
-        // at column i
+        // at column i.  The entries go straight into the f16 operands
+        // T diag(beta rk) and T diag(beta) (rows r, K = i), which overwrite L.
         {
             const int i = tid >> 3, j4 = (tid & 7) * 4;
             float2 s01 = make_float2(0.f, 0.f), s23 = s01;
@@ -526,40 +528,42 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 s01 = __ffma2_rn(tv, make_float2(x.x, x.y), s01);
                 s23 = __ffma2_rn(tv, make_float2(x.z, x.w), s23);
             }
-            *reinterpret_cast<float4 *>(Tm + (32 + i) * K1_P + j4) = make_float4(-s01.x, -s01.y, -s23.x, -s23.y);
+            const float4 b4 = *reinterpret_cast<const float4 *>(bs + j4);
+            const float4 k4 = *reinterpret_cast<const float4 *>(rk + j4);
+            const float2 v01 = __fmul2_rn(make_float2(-s01.x, -s01.y), make_float2(b4.x, b4.y));
+            const float2 v23 = __fmul2_rn(make_float2(-s23.x, -s23.y), make_float2(b4.z, b4.w));
+            const float2 k01 = __fmul2_rn(v01, make_float2(k4.x, k4.y));
+            const float2 k23 = __fmul2_rn(v23, make_float2(k4.z, k4.w));
+            const uint32_t o = kmaj_off(32 + i, j4, LBO_KIN, SBO_K64);
+            *reinterpret_cast<uint2 *>(sm + K1_TBK + o) = make_uint2(pack_f16x2(k01.x, k01.y), pack_f16x2(k23.x, k23.y));
+            *reinterpret_cast<uint2 *>(sm + K1_TBV + o) = make_uint2(pack_f16x2(v01.x, v01.y), pack_f16x2(v23.x, v23.y));
         }
-    }
-    __syncthreads();
-
-    // 6. T diag(beta rk) and T diag(beta) -> f16 operands (rows r, K = i).
-    //    Thread: row r = 8 warp + (tid & 7), columns i0 .. i0 + 15 with
-    //    i0 = 16 ((tid >> 3) & 3): each quarter-warp covers 8 consecutive rows
-    //    (conflict-free float4 reads of T and 16-byte operand stores).
-    {
-        const int r = 8 * warp + (tid & 7), i0 = 16 * ((tid >> 3) & 3);
-#pragma unroll
-        for (int i8 = 0; i8 < 16; i8 += 8) {
+        // 6. the other blocks of T (T_AA, T_BB, final since the 16 -> 32 merge,
+        //    and the zeros above the diagonal) -> the same operands: 384 pieces
+        //    of 8 columns; pieces 0-255 are rows 0-31 (warp = column piece),
+        //    pieces 256-383 rows 32-63, column pieces 4-7
+        for (int gi = tid; gi < 384; gi += K1_THREADS) {
+            const int r = (gi < 256 ? 0 : 32) + (gi & 31), c0 = 8 * ((gi < 256 ? 0 : 4) + ((gi & 255) >> 5));
             float tk[8], tv[8];
 #pragma unroll
             for (int j4 = 0; j4 < 8; j4 += 4) {
-                const float4 t4 = *reinterpret_cast<const float4 *>(Tm + r * K1_P + i0 + i8 + j4);
-                const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
-                const int ib = i0 + i8 + j4;
+                const int ib = c0 + j4;
+                const float4 t4 = *reinterpret_cast<const float4 *>(Tm + r * K1_P + ib);
                 const float4 b4 = *reinterpret_cast<const float4 *>(bs + ib);
                 const float4 k4 = *reinterpret_cast<const float4 *>(rk + ib);
-                const float2 v01 = __fmul2_rn(make_float2(tt[0], tt[1]), make_float2(b4.x, b4.y));
-                const float2 v23 = __fmul2_rn(make_float2(tt[2], tt[3]), make_float2(b4.z, b4.w));
+                const float2 v01 = __fmul2_rn(make_float2(t4.x, t4.y), make_float2(b4.x, b4.y));
+                const float2 v23 = __fmul2_rn(make_float2(t4.z, t4.w), make_float2(b4.z, b4.w));
                 const float2 k01 = __fmul2_rn(v01, make_float2(k4.x, k4.y));
                 const float2 k23 = __fmul2_rn(v23, make_float2(k4.z, k4.w));
                 const float vv4[4] = {v01.x, v01.y, v23.x, v23.y}, kk4[4] = {k01.x, k01.y, k23.x, k23.y};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const bool in = ib + u <= r;
+                    const bool in = ib + u <= r;   // T is lower triangular; above it lies stale data
                     tv[j4 + u] = in ? vv4[u] : 0.f;
                     tk[j4 + u] = in ? kk4[u] : 0.f;
                 }
             }
-            const uint32_t o = kmaj_off(r, i0 + i8, LBO_KIN, SBO_K64);
+            const uint32_t o = kmaj_off(r, c0, LBO_KIN, SBO_K64);
             *reinterpret_cast<uint4 *>(sm + K1_TBK + o) = pack_f16x8(tk);
             *reinterpret_cast<uint4 *>(sm + K1_TBV + o) = pack_f16x8(tv);
         }
@@ -602,7 +606,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         for (int j = 0; j < 8; ++j) dv[j] = (8 * kg + j == i) ? rq[i] : 0.f;
         *reinterpret_cast<uint4 *>(sm + K1_RQD + kmaj_off(i, 8 * kg, LBO_KIN, SBO_K64)) = pack_f16x8(dv);
     }
-    // 8. (-diag(rk) Wk)^T and (diag(rk) Uv)^T -> smem operands (rows d / e, K = r).
+    // 8. (-diag(rk) Wk)^T -> smem operand and (diag(rk) Uv)^T -> record (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
 #pragma unroll
@@ -625,7 +629,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int h8 = 0; h8 < 16; h8 += 8) {
                 const int kk = 32 * ch + c + h8;
                 *reinterpret_cast<uint4 *>(sm + K1_WKT + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(w + h8);
-                *reinterpret_cast<uint4 *>(sm + K1_UVT + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(u + h8);
+                *reinterpret_cast<uint4 *>(rec + REC_UV + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(u + h8);
             }
         }
     }
@@ -685,24 +689,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
     }
     if (!ok && tid == 0) record_timeout(st);
-    __syncthreads();   // the parked Qg' is consumed: its area takes the K = r tiles
-    // 12. Ke'^T, Mc' and (diag(rk) Uv)^T are already K2's operand tiles:
-    //     shared memory -> record, 16 bytes per thread and step
-    {
-        const uint4 *ket = reinterpret_cast<const uint4 *>(sm + K1_KET);
-        const uint4 *mc = reinterpret_cast<const uint4 *>(sm + K1_MC);
-        const uint4 *uvt = reinterpret_cast<const uint4 *>(sm + K1_UVT);
-        uint4 *dk = reinterpret_cast<uint4 *>(rec + REC_KM), *dm = reinterpret_cast<uint4 *>(rec + REC_MC);
-        uint4 *du = reinterpret_cast<uint4 *>(rec + REC_UV);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            dk[tid + 256 * j] = ket[tid + 256 * j];
-            du[tid + 256 * j] = uvt[tid + 256 * j];
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) dm[tid + 256 * j] = mc[tid + 256 * j];
-    }
-
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
