@@ -442,23 +442,17 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const int r = 16 * blk + rr;
             float x[4] = {(rr == c) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ii = 0; ii < rr; ++ii)
-                if (ii >= c) x[ii & 3] -= Lm[r * K1_PL + 16 * blk + ii] * tcol[ii];
+            for (int ii = 0; ii < rr; ++ii)   // tcol[ii] = 0 for ii < c: no lane-dependent predicate
+                x[ii & 3] -= Lm[r * K1_PL + 16 * blk + ii] * tcol[ii];
             tcol[rr] = (rr >= c) ? (x[0] + x[1]) + (x[2] + x[3]) : 0.f;
             Tm[r * K1_P + col] = tcol[rr];
         }
-    } else {
-        // meanwhile Ke'^T and Mc', already K2's operand tiles, go to the record
-        // (Ke'^T then Mc' are contiguous there: 1536 16-byte pieces)
-        const uint4 *ket = reinterpret_cast<const uint4 *>(sm + K1_KET);
-        const uint4 *mc = reinterpret_cast<const uint4 *>(sm + K1_MC);
-        uint4 *dkm = reinterpret_cast<uint4 *>(rec + REC_KM);
-        static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = tid - 64 + (K1_THREADS - 64) * j;
-            dkm[i] = i < 1024 ? ket[i] : mc[i - 1024];
-        }
+    } else if (tid < 192) {
+        // zeros in the 16 x 16 blocks above the diagonal of T_AA and T_BB
+        // (rows 0-15 x columns 16-31, rows 32-47 x columns 48-63): the merges
+        // below then run over whole blocks, without triangular bounds
+        const int z = tid - 64, r = (z >> 2) + (z >= 64 ? 16 : 0), c4 = 16 + 4 * (z & 3) + (z >= 64 ? 32 : 0);
+        *reinterpret_cast<float4 *>(Tm + r * K1_P + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
     {   // 16 -> 32, pairs k = 0, 1 (A = block 2k, B = block 2k + 1); thread: pair
@@ -477,25 +471,30 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         *reinterpret_cast<float2 *>(Xs + (k2 * 16 + i) * 16 + j2) = __fadd2_rn(s0, s1);
         __syncthreads();
-        // T_BB is unit lower triangular: its row i ends at column i
+        // T_BB is unit lower triangular (zeros above its diagonal)
         s0 = make_float2(0.f, 0.f);
+        s1 = s0;
         const float *trow = Tm + (b0 + i) * K1_P + b0;
-        for (int m = 0; m <= i; ++m) {
-            const float2 x = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
-            s0 = __ffma2_rn(make_float2(trow[m], trow[m]), x, s0);
+#pragma unroll
+        for (int m = 0; m < 16; m += 2) {
+            const float2 x0 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
+            const float2 x1 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m + 1) * 16 + j2);
+            s0 = __ffma2_rn(make_float2(trow[m], trow[m]), x0, s0);
+            s1 = __ffma2_rn(make_float2(trow[m + 1], trow[m + 1]), x1, s1);
         }
+        s0 = __fadd2_rn(s0, s1);
         *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-s0.x, -s0.y);
     }
     __syncthreads();
     {   // 32 -> 64 (A = rows 0-31, B = rows 32-63).
-        // X = L_BA T_AA: thread = row i (lane), columns j4 .. j4 + 3 (warp): T_AA
-        // is lower triangular, so the sum starts at row j4 of T_AA, warp-uniformly
+        // X = L_BA T_AA: thread = row i (lane), columns j4 .. j4 + 3 (warp), over
+        // all 32 rows of T_AA (zeros above its diagonal)
         {
             const int i = tid & 31, j4 = 4 * warp;
             float2 s01 = make_float2(0.f, 0.f), s23 = s01, u01 = s01, u23 = s01;
             const float *lrow = Lm + (32 + i) * K1_PL;
-            int m = j4;
-            for (; m + 1 < 32; m += 2) {
+#pragma unroll
+            for (int m = 0; m < 32; m += 2) {
                 const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
                 const float4 t1 = *reinterpret_cast<const float4 *>(Tm + (m + 1) * K1_P + j4);
                 const float2 l0 = make_float2(lrow[m], lrow[m]), l1 = make_float2(lrow[m + 1], lrow[m + 1]);
@@ -504,30 +503,30 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 u01 = __ffma2_rn(l1, make_float2(t1.x, t1.y), u01);
                 u23 = __ffma2_rn(l1, make_float2(t1.z, t1.w), u23);
             }
-            if (m < 32) {
-                const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
-                const float2 l0 = make_float2(lrow[m], lrow[m]);
-                s01 = __ffma2_rn(l0, make_float2(t0.x, t0.y), s01);
-                s23 = __ffma2_rn(l0, make_float2(t0.z, t0.w), s23);
-            }
             s01 = __fadd2_rn(s01, u01);
             s23 = __fadd2_rn(s23, u23);
             *reinterpret_cast<float4 *>(Xw + i * K1_XWP + j4) = make_float4(s01.x, s01.y, s23.x, s23.y);
         }
         __syncthreads();
-        // T_BA = -T_BB X: thread = row i, columns j4 .. j4 + 3; T_BB's row i ends
-        // at column i.  The entries go straight into the f16 operands
+        // T_BA = -T_BB X: thread = row i, columns j4 .. j4 + 3, over all 32
+        // columns of T_BB (zeros above its diagonal).  The entries go straight into the f16 operands
         // T diag(beta rk) and T diag(beta) (rows r, K = i), which overwrite L.
         {
             const int i = tid >> 3, j4 = (tid & 7) * 4;
-            float2 s01 = make_float2(0.f, 0.f), s23 = s01;
+            float2 s01 = make_float2(0.f, 0.f), s23 = s01, u01 = s01, u23 = s01;
             const float *trow = Tm + (32 + i) * K1_P + 32;
-            for (int m = 0; m <= i; ++m) {
-                const float4 x = *reinterpret_cast<const float4 *>(Xw + m * K1_XWP + j4);
-                const float2 tv = make_float2(trow[m], trow[m]);
-                s01 = __ffma2_rn(tv, make_float2(x.x, x.y), s01);
-                s23 = __ffma2_rn(tv, make_float2(x.z, x.w), s23);
+#pragma unroll
+            for (int m = 0; m < 32; m += 2) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(Xw + m * K1_XWP + j4);
+                const float4 x1 = *reinterpret_cast<const float4 *>(Xw + (m + 1) * K1_XWP + j4);
+                const float2 t0 = make_float2(trow[m], trow[m]), t1 = make_float2(trow[m + 1], trow[m + 1]);
+                s01 = __ffma2_rn(t0, make_float2(x0.x, x0.y), s01);
+                s23 = __ffma2_rn(t0, make_float2(x0.z, x0.w), s23);
+                u01 = __ffma2_rn(t1, make_float2(x1.x, x1.y), u01);
+                u23 = __ffma2_rn(t1, make_float2(x1.z, x1.w), u23);
             }
+            s01 = __fadd2_rn(s01, u01);
+            s23 = __fadd2_rn(s23, u23);
             const float4 b4 = *reinterpret_cast<const float4 *>(bs + j4);
             const float4 k4 = *reinterpret_cast<const float4 *>(rk + j4);
             const float2 v01 = __fmul2_rn(make_float2(-s01.x, -s01.y), make_float2(b4.x, b4.y));
@@ -573,6 +572,14 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
+    // Ke'^T and Mc', already K2's operand tiles, go to the record by bulk copies
+    // (waited for before the CTA exits; neither tile is overwritten)
+    if (tid == 0) {
+        static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
+        bulk_s2g(rec + REC_KM, sm + K1_KET, 16384);
+        bulk_s2g(rec + REC_MC, sm + K1_MC, 8192);
+        bulk_commit();
+    }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
         const uint32_t idesc = idesc_f16(128, 64);
@@ -689,6 +696,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
     }
     if (!ok && tid == 0) record_timeout(st);
+    if (tid == 0) bulk_wait_all();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();

@@ -79,6 +79,27 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 1-D bulk copy shared -> global (TMA engine), tracked by the issuing thread's
+// bulk async-group.  Addresses 16-byte aligned, bytes % 16 == 0.  The source
+// must have been made visible to the async proxy (fence_async_smem).
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk copy committed by this thread has completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Hint: bring [src, src + bytes) into L2 (bulk prefetch; no completion).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
 {
