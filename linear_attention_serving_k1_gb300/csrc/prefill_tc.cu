@@ -242,6 +242,16 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     };
     const float beta_r = (tid < kC && tid < L) ? __ldg(beta + (size_t)(t0 + tid) * H + h) : 0.f;
     load_half(0);
+    // L2 prefetch of the second channel half of this chunk's rows (bulk, one
+    // row slice per thread), so that its loads after the first half hit L2
+    {
+        const int r = tid & 63, which = tid >> 6;   // q, k, v, g
+        const char *base = which == 0 ? (const char *)q : which == 1 ? (const char *)k
+                         : which == 2 ? (const char *)v : (const char *)g;
+        const uint32_t esz = which == 3 ? 4u : 2u;
+        if (r < L && (which < 3 || !scalar_gate))
+            prefetch_l2(base + (((size_t)(t0 + r) * H + h) * kD + 64) * esz, 64 * esz);
+    }
 
     if (warp == 0) {
         tmem_alloc(&tmem_sh, 256);
@@ -718,7 +728,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 // them while this chunk's output is written to memory.
 constexpr int K2_STAGES = 2;
 constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
-constexpr int kL2Ahead = 3;   // records pulled into L2 this many chunks ahead
 constexpr uint32_t K2_SOP = K2_STAGES * REC_BYTES;     // f16 S^T: rows e x K = d
 constexpr uint32_t K2_GAM = K2_SOP + 32768;            // fp32 gamma [kGamSlots][128]
 constexpr int K2_STATE_WARPS = 16;
@@ -884,13 +893,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         for (int c = 0; c < nch && alive; ++c) {
             // gamma has landed (its slot's barrier cannot run ahead: slot c % 4 is
             // refilled only after the product of chunk c + 2, which needs this
-            // thread's S^T of chunk c + 1) and the chunk's product is in TMEM;
-            // records a few chunks ahead are pulled into L2 meanwhile
-            if (c + kL2Ahead < nch) {
-                const uint8_t *pre = rec_at(c + kL2Ahead);
-                for (uint32_t off = (uint32_t)tid * 128; off < REC_G; off += K2_STATE_THREADS * 128)
-                    prefetch_l2_line(pre + off);
-            }
+            // thread's S^T of chunk c + 1) and the chunk's product is in TMEM
             if (!wait_or_abort(&gfull[c % kGamSlots], (c / kGamSlots) & 1, abort_v) ||
                 !wait_or_abort(&sdone, c & 1, abort_v)) {
                 alive = false;

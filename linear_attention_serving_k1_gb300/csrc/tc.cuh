@@ -113,12 +113,6 @@ __device__ __forceinline__ void fence_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Pulls one 128-byte line into L2 (no register result, no completion to wait for).
-__device__ __forceinline__ void prefetch_l2_line(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads)
 {
