@@ -84,7 +84,8 @@ typedef enum {
  *                  kda_prefill_status and its tail is not computed.
  *   segment_chunks 0 = chosen by the library (from num_seqs x num_heads and
  *                  the sequence bound); otherwise the number of chunks per
- *                  sequence in one segment.  A tuning knob only: the
+ *                  sequence in one segment, raised where needed so that
+ *                  there are at most 256 segments.  A tuning knob only: the
  *                  results are bit-identical for every value, since the
  *                  state crosses a segment boundary in fp32 unchanged.
  *   scalar_gate    0: g is [T, H, Dk], one log-decay per key channel (KDA).

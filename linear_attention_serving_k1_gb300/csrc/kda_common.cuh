@@ -54,12 +54,13 @@ struct SeqTable {
 // compactly indexed records (no ring slots, no carry).
 constexpr int kMaxSegments = 256;
 struct SegPlan {
-    int G;      // chunks per sequence in one segment (the last one may hold fewer)
+    int G;      // ring slot capacity: chunks per sequence of the longest segment
     int nseg;   // number of segments
     int R;      // ring slots
-    int begin(int s) const { return s * G; }
-    int count(int) const { return G; }
-    int covered() const { return nseg * G; }
+    int lo[kMaxSegments + 1];   // segment s: local chunks [lo[s], lo[s + 1]) of every sequence
+    int begin(int s) const { return lo[s]; }
+    int count(int s) const { return lo[s + 1] - lo[s]; }
+    int covered() const { return lo[nseg]; }
 };
 
 struct PrefillArgs {

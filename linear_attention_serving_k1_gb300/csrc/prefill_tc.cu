@@ -993,35 +993,60 @@ size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
     // Automatic choice: overlap only when the recurrence (one CTA per chain and
-    // SM) leaves most of the 152 SMs idle.  Uniform segments of G chunks (the
-    // last one takes the remainder): G long enough that one K1 launch fills the
-    // remaining SMs (two K1 CTAs each) about sixteen times over, so its last
-    // partial wave is a small part of it, and at most 3/8 of the sequence, so
-    // that K1 and K2 overlap for most of the call and the last K2, which
-    // nothing overlaps, is short.  At least 4 chunks (the carry, 128 KB per
-    // chain and segment, stays small beside the records, 88.5 KB per chunk);
-    // at most kMaxSegments segments.
-    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4, kWaves = 16;
+    // SM) leaves most of the 152 SMs idle.  Segment lengths are whole K1 waves
+    // (two K1 CTAs per SM; a wave covers 2 x SMs / chains chunks of every
+    // sequence): the first segment, which K1 runs on all SMs before any K2,
+    // four waves; then, on the SMs K2 leaves, segments of 16 waves, shrinking
+    // towards the end (16, 13, 9, 6, 4, 2 waves) so that each K2 is shorter
+    // than the K1 running beside it and the last K2, which nothing overlaps,
+    // covers two waves only.  The segment just after the first takes the
+    // remainder.  At most kMaxSegments segments (else uniform, as for an
+    // explicit segment_chunks, which is raised to that bound where needed).
+    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4;
     const int64_t T = d->total_tokens;
     const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
     const int64_t maxc = (len + d->chunk - 1) / d->chunk;
     const int64_t chains = (int64_t)d->num_seqs * d->num_heads;
-    SegPlan p{0, 1, 1};
-    int64_t G;
-    if (d->segment_chunks > 0) {
-        G = d->segment_chunks;
-    } else {
-        if (chains > kMaxChains) return p;
-        G = (kWaves * 2 * (kSMs - chains) + chains - 1) / chains;
-        G = std::min<int64_t>(G, (3 * maxc + 7) / 8);
-        G = std::max<int64_t>(G, kMinG);
-        G = std::max<int64_t>(G, (maxc + kMaxSegments - 1) / kMaxSegments);
+    SegPlan p{0, 1, 1, {}};
+    auto finish = [&]() {
+        p.G = 0;
+        for (int s = 0; s < p.nseg; ++s) p.G = std::max(p.G, p.count(s));
+        p.R = std::min(2, p.nseg);
+        return p;
+    };
+    if (d->segment_chunks == 0) {
+        if (chains > kMaxChains || chains <= 0) return p;
+        const double wave_all = 2.0 * kSMs / chains, wave = 2.0 * (kSMs - chains) / chains;
+        const int64_t first = std::max<int64_t>(kMinG, std::llround(4 * wave_all));
+        if (first >= maxc) return p;
+        static const int kTailWaves[] = {2, 4, 6, 9, 13, 16};
+        int64_t tail[kMaxSegments], sum = 0;
+        int nt = 0;
+        while (first + sum < maxc && nt < kMaxSegments - 1) {
+            const int w = nt < 6 ? kTailWaves[nt] : 16;
+            tail[nt] = std::max<int64_t>(kMinG, std::llround(w * wave));
+            sum += tail[nt++];
+        }
+        if (first + sum >= maxc) {
+            // the earliest tail segment gives back the overshoot; one shorter than
+            // kMinG joins the first segment instead
+            int64_t head = first;
+            tail[nt - 1] -= first + sum - maxc;
+            if (tail[nt - 1] < kMinG) head += tail[--nt];
+            p.nseg = 1 + nt;
+            p.lo[0] = 0;
+            p.lo[1] = (int)head;
+            for (int s = 1; s < p.nseg; ++s) p.lo[s + 1] = p.lo[s] + (int)tail[nt - s];
+            return finish();
+        }
     }
+    // uniform segments of G chunks (the last may reach past the sequence)
+    int64_t G = d->segment_chunks > 0 ? d->segment_chunks : 1;
+    G = std::max<int64_t>(G, (maxc + kMaxSegments - 1) / kMaxSegments);
     if (G >= maxc) return p;
-    p.G = (int)G;
     p.nseg = (int)((maxc + G - 1) / G);
-    p.R = std::min(2, p.nseg);
-    return p;
+    for (int s = 0; s <= p.nseg; ++s) p.lo[s] = (int)(s * G);
+    return finish();
 }
 
 namespace {

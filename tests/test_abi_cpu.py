@@ -83,11 +83,13 @@ def test_segmented_workspace_is_bounded(lib):
     record_bytes = 90624
     assert whole >= 2048 * 32 * record_bytes
     assert 0 < auto < whole // 4
-    # explicit segment lengths: ring of 2 x G x H records plus a 64 KB state per head
+    # explicit segment lengths: ring of 2 x G x H records plus a 64 KB state per
+    # head, G raised to 2048 / 256 chunks (at most 256 segments)
     for G in (1, 4, 16):
+        Ge = max(G, 2048 // 256)
         n = lib.kda_prefill_workspace_size(ctypes.byref(_desc(segment_chunks=G, **long)))
-        assert n >= 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4
-        assert n < 2 * G * 32 * record_bytes + 32 * 128 * 128 * 4 + 8192
+        assert n >= 2 * Ge * 32 * record_bytes + 32 * 128 * 128 * 4
+        assert n < 2 * Ge * 32 * record_bytes + 32 * 128 * 128 * 4 + 8192
 
 
 def test_launch_count(lib):
@@ -98,6 +100,11 @@ def test_launch_count(lib):
     assert lib.kda_prefill_launch_count(ctypes.byref(_desc(segment_chunks=512, **long))) == 1 + 2 * 4
     assert lib.kda_prefill_launch_count(ctypes.byref(_desc(segment_chunks=500, **long))) == 1 + 2 * 5
     assert lib.kda_prefill_launch_count(ctypes.byref(_desc(H=0))) == -1
+    # automatic plan: segments of whole K1 waves, 4 on all SMs first, a 2-wave
+    # tail: workload 2 (8192 tokens x 32 heads) -> 38, 45, 30, 15 chunks;
+    # workload 4 (131072 tokens) -> 21 segments
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(T=8192, H=32, D=128, dtype_code=kda.DTYPE_BF16))) == 1 + 2 * 4
+    assert lib.kda_prefill_launch_count(ctypes.byref(_desc(**long))) == 1 + 2 * 21
 
 
 def test_prefill_rejects_before_launch(lib):
