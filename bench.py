@@ -8,8 +8,10 @@ checkpoint writer) over the chosen prefill workload, default "prefill B1 H32
 T8192 D128 bf16".  Decode (state GB/s) is timed in the same run over the
 decode workload "decode N256 H32 D128 bf16", 64 consecutive steps, and
 reported under "decode".  Inputs are seeded synthetic draws (see
-linear_attention_serving_k1_gb300/workloads.py) made on the device; L2 is
-flushed (a 512 MiB write) before every timed step.
+linear_attention_serving_k1_gb300/workloads.py) made on the device; every
+timed prefill step starts from an idle device and L2 is flushed (a 512 MiB
+write) before it.  (Back to back, without the synchronisation between steps,
+a workload-2 call measures about 5% longer.)
 
 Rank 0 prints one JSON line.  With --impl reference the float64 CPU oracle is
 timed instead, on the same workload (or its first heads when it is large).
@@ -190,6 +192,9 @@ def time_steps(fn, steps, warmup, flush_buf, stream):
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
+        # each timed step starts from an idle device: the previous step has
+        # finished (synchronize) and L2 holds only the flush buffer's lines
+        torch.cuda.synchronize()
         flush_buf.fill_(1.0)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -392,7 +397,7 @@ def run_ours(args):
             "data": "synthetic (seeded, on device)",
             "config": {"workload": w.name, "tokens_per_step": w.total_tokens, "heads": w.H,
                        "head_dim": w.D, "chunk": 64, "ckpt_stride": w.ckpt_stride,
-                       "l2": "flushed (512 MiB write) before every timed step; inputs also exceed L2",
+                       "l2": "flushed (512 MiB write) before every timed step, each step started from an idle device; inputs also exceed L2",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "e2e": ({"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -31,6 +31,7 @@
 // K1 writes, per (chunk, head), one record holding K2's operand tiles in the
 // tensor-core shared-memory layout (no-swizzle K-major core matrices), moved
 // into K2's shared memory by one bulk TMA copy, and gamma.
+#include <atomic>
 #include "kda_common.cuh"
 #include <algorithm>
 
@@ -626,12 +627,16 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // 8. (-diag(rk) Wk)^T -> smem operand and (diag(rk) Uv)^T -> record (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
+        float wu[4][16];   // Wk^T and Uv^T, columns c and c + 16: all four loads before one wait
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            tmem_ld16(tm + lane_base + T1_W1 + 32 * ch + 16 * c2, wu[2 * c2]);
+            tmem_ld16(tm + lane_base + T1_W2 + 32 * ch + 16 * c2, wu[2 * c2 + 1]);
+        }
+        tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; c += 16) {
-            float w[16], u[16];
-            tmem_ld16(tm + lane_base + T1_W1 + 32 * ch + c, w);
-            tmem_ld16(tm + lane_base + T1_W2 + 32 * ch + c, u);
-            tmem_ld_wait();
+            float (&w)[16] = wu[c / 8], (&u)[16] = wu[c / 8 + 1];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
                 const float2 s2 = *reinterpret_cast<const float2 *>(rk + 32 * ch + c + j);
@@ -679,29 +684,34 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 
     if (ok) {
         const int r = 16 * q4 + lane;
-        // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64)
+        // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64), all
+        //     four 16-column loads in flight before one wait
+        {
+            float a[4][16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-            float a[16];
-            tmem_ld16(tm + lane_base + T1_AP + 64 * ch + c, a);
+            for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_AP + 64 * ch + 16 * q, a[q]);
             tmem_ld_wait();
 #pragma unroll
-            for (int h8 = 0; h8 < 16; h8 += 8)
-                *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
-                    pack_f16x8(a + h8);
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int h8 = 0; h8 < 16; h8 += 8)
+                    *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
+                        pack_f16x8(a[q] + h8);
         }
         // 11. Q' -> record: the M = 64 accumulator puts row r = 16 q4 + l in lane
         //     32 q4 + l (l < 16)
+        {
+            float a[4][16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
-            float a[16];
-            tmem_ld16(tm + lane_base + T1_QP + 64 * ch + c, a);
+            for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_QP + 64 * ch + 16 * q, a[q]);
             tmem_ld_wait();
             if (lane < 16) {
 #pragma unroll
-                for (int h8 = 0; h8 < 16; h8 += 8)
-                    *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + c + h8, LBO_KIN, SBO_K128)) =
-                        pack_f16x8(a + h8);
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int h8 = 0; h8 < 16; h8 += 8)
+                        *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
+                            pack_f16x8(a[q] + h8);
             }
         }
     }
@@ -1106,10 +1116,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
 {
     cudaError_t e;
     g_detail[0] = 0;
-    e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
-    if (e != cudaSuccess) return e;
+    // the kernels' shared-memory opt-in, once per device rather than on every call
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit, std::memory_order_release);
+    }
     const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
     uint8_t *ring = (uint8_t *)a.handoff;
     const unsigned chains = (unsigned)((size_t)a.N * a.H);
