@@ -205,8 +205,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int L = min(kC, tab.cu[n + 1] - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
     // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in the record's
-    // A' area (written once the product that reads it back is complete) until
-    // phase 9 copies it into shared memory
+    // A' area (written once the product that reads it back is complete) until a
+    // bulk copy brings it back into shared memory for the products of phase 9
     uint8_t *qg_park = rec + REC_AP;
     static_assert(REC_AP + 16384 <= REC_QP, "park area");
 
