@@ -140,11 +140,13 @@ int32_t kda_prefill_launch_count(const kda_prefill_desc *desc)
     return L.plan.nseg > 1 ? 1 + 2 * L.plan.nseg : 3;
 }
 
-kda_status kda_prefill(const void *q, const void *k, const void *v, const float *g,
-                       const float *beta, const float *init_state, const int32_t *cu_seqlens,
-                       void *out, float *final_state, float *ckpts,
-                       const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
-                       kda_stream_t stream)
+}  // extern "C"
+
+namespace kda {
+kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                        const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
+                        float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                        kda_stream_t stream, bool use_graph)
 {
     Layout L;
     kda_status s = check_desc(desc, &L);
@@ -189,14 +191,31 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     a.scalar_gate = desc->scalar_gate != 0;
     a.stream = (cudaStream_t)stream;
 
-    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream);
-    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    cudaError_t e;
+    if (kda::use_tc_path(a.dtype, a.D, a.C)) {
+        e = use_graph ? kda::launch_prefill_tc_graph(a) : kda::enqueue_prefill_tc(a, a.stream);
+        if (e != cudaSuccess)
+            return fail(KDA_ERR_CUDA, "prefill kernels: %s %s", cudaGetErrorString(e), kda::launch_failure_detail());
+        return KDA_OK;
+    }
+    if ((e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream)) != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
-    e = kda::use_tc_path(a.dtype, a.D, a.C) ? kda::launch_prefill_tc(a) : kda::launch_prefill_simt(a);
-    if (e != cudaSuccess)
-        return fail(KDA_ERR_CUDA, "prefill kernels: %s %s", cudaGetErrorString(e),
-                    kda::use_tc_path(a.dtype, a.D, a.C) ? kda::launch_failure_detail() : "");
+    if ((e = kda::launch_prefill_simt(a)) != cudaSuccess)
+        return fail(KDA_ERR_CUDA, "prefill kernels: %s", cudaGetErrorString(e));
     return KDA_OK;
+}
+}  // namespace kda
+
+extern "C" {
+
+kda_status kda_prefill(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                       void *out, float *final_state, float *ckpts,
+                       const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                       kda_stream_t stream)
+{
+    return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc, workspace,
+                             workspace_bytes, stream, true);
 }
 
 kda_status kda_prefill_status(void *workspace, kda_stream_t stream)

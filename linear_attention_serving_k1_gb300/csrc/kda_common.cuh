@@ -105,12 +105,22 @@ SegPlan tc_segment_plan(const kda_prefill_desc *desc);
 // Validates `desc` and returns the workspace bytes kda_prefill needs for it
 // (on error: the status, with the thread-local message set).
 kda_status prefill_workspace_bytes(const kda_prefill_desc *desc, size_t *bytes);
+// kda_prefill's body; use_graph = false launches every kernel directly (no
+// CUDA graph is captured or instantiated: the no-allocation entry point)
+kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                        const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
+                        float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                        kda_stream_t stream, bool use_graph);
 // Sets the thread-local message that kda_last_error() returns; returns `s`.
 kda_status fail_with_message(kda_status s, const char *fmt, ...);
 
 cudaError_t launch_seq_table(const PrefillArgs &a);
 cudaError_t launch_prefill_simt(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a);
+// The whole tensor-core call (status reset, sequence table, K1/K2 segments) on
+// `stream`, and the same call replayed from a cached CUDA graph.
+cudaError_t enqueue_prefill_tc(PrefillArgs a, cudaStream_t stream);
+cudaError_t launch_prefill_tc_graph(const PrefillArgs &a);
 // Kernel attributes noted by the last failed tensor-core launch on this thread ("" if none).
 const char *launch_failure_detail();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,

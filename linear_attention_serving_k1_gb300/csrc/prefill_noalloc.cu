@@ -73,6 +73,6 @@ extern "C" kda_status kda_prefill_noalloc(const void *q, const void *k, const vo
     if (e != cudaSuccess)
         return kda::fail_with_message(KDA_ERR_CUDA, "kda_prefill_noalloc: scratch address: %s",
                                       cudaGetErrorString(e));
-    return kda_prefill(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc,
-                       scratch, kScratchBytes, stream);
+    return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc,
+                             scratch, kScratchBytes, stream, false);
 }

@@ -1108,18 +1108,13 @@ cudaError_t side_ctx(SideCtx **out)
     *out = &c;
     return cudaSuccess;
 }
-}  // namespace
-
-const char *launch_failure_detail() { return g_detail; }
-
-cudaError_t launch_prefill_tc(const PrefillArgs &a)
+// The kernels' shared-memory opt-in, once per device rather than on every call.
+cudaError_t tc_kernel_attributes()
 {
-    cudaError_t e;
-    g_detail[0] = 0;
-    // the kernels' shared-memory opt-in, once per device rather than on every call
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(attr_done.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
@@ -1128,6 +1123,93 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_release);
     }
+    return cudaSuccess;
+}
+
+// Per thread and device: a private stream on which a call's launches are
+// captured, and the executable graph they were last replayed from.
+struct GraphCtx {
+    int device = -1;
+    cudaStream_t cap = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+thread_local GraphCtx g_graph[kMaxDevices];
+}  // namespace
+
+const char *launch_failure_detail() { return g_detail; }
+
+cudaError_t enqueue_prefill_tc(PrefillArgs a, cudaStream_t stream)
+{
+    a.stream = stream;
+    cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_seq_table(a)) != cudaSuccess) return e;
+    return launch_prefill_tc(a);
+}
+
+cudaError_t launch_prefill_tc_graph(const PrefillArgs &a)
+{
+    // Everything a graph capture must not create is made first (the side
+    // stream, its events, the kernels' attributes); then the call is captured
+    // on this thread's private stream, the cached executable graph takes the
+    // new launch parameters (or is instantiated again when the launch
+    // structure changed) and is launched on the caller's stream.  When that
+    // stream is itself being captured, or a graph call fails, the launches go
+    // to the caller's stream directly.
+    cudaError_t e;
+    if ((e = tc_kernel_attributes()) != cudaSuccess) return e;
+    SideCtx *c = nullptr;
+    if ((e = side_ctx(&c)) != cudaSuccess) return e;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(a.stream, &cs)) != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return enqueue_prefill_tc(a, a.stream);
+    GraphCtx &g = g_graph[c->device];
+    if (g.device != c->device) {
+        if (cudaStreamCreateWithFlags(&g.cap, cudaStreamNonBlocking) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return enqueue_prefill_tc(a, a.stream);
+        }
+        g.device = c->device;
+    }
+    if (cudaStreamBeginCapture(g.cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return enqueue_prefill_tc(a, a.stream);
+    }
+    e = enqueue_prefill_tc(a, g.cap);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(g.cap, &graph);
+    if (e != cudaSuccess || ec != cudaSuccess || graph == nullptr) {
+        if (graph) cudaGraphDestroy(graph);
+        (void)cudaGetLastError();
+        return e != cudaSuccess ? e : enqueue_prefill_tc(a, a.stream);
+    }
+    cudaError_t r = cudaErrorInvalidValue;
+    if (g.exec) {
+        cudaGraphExecUpdateResultInfo info;
+        r = cudaGraphExecUpdate(g.exec, graph, &info);
+        if (r != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphExecDestroy(g.exec);
+            g.exec = nullptr;
+        }
+    }
+    if (!g.exec) {
+        r = cudaGraphInstantiate(&g.exec, graph, 0);
+        if (r != cudaSuccess) g.exec = nullptr;
+    }
+    cudaGraphDestroy(graph);
+    if (r != cudaSuccess) {
+        (void)cudaGetLastError();
+        return enqueue_prefill_tc(a, a.stream);
+    }
+    return cudaGraphLaunch(g.exec, a.stream);
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a)
+{
+    cudaError_t e;
+    g_detail[0] = 0;
+    if ((e = tc_kernel_attributes()) != cudaSuccess) return e;
     const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
     uint8_t *ring = (uint8_t *)a.handoff;
     const unsigned chains = (unsigned)((size_t)a.N * a.H);
