@@ -1161,7 +1161,10 @@ cudaError_t launch_prefill_tc_graph(const PrefillArgs &a)
     SideCtx *c = nullptr;
     if ((e = side_ctx(&c)) != cudaSuccess) return e;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if ((e = cudaStreamIsCapturing(a.stream, &cs)) != cudaSuccess) return e;
+    if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return enqueue_prefill_tc(a, a.stream);
+    }
     if (cs != cudaStreamCaptureStatusNone) return enqueue_prefill_tc(a, a.stream);
     GraphCtx &g = g_graph[c->device];
     if (g.device != c->device) {
