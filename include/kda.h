@@ -18,12 +18,13 @@
  *   - All pointers are DEVICE pointers into contiguous, row-major buffers
  *     that the caller owns and allocates (the library allocates no buffer;
  *     the tensor-core prefill creates, once per host thread and device, a
- *     side stream, a few events and a capture stream, and keeps one
- *     executable CUDA graph of its last call: each kda_prefill call is
- *     captured on that stream and replayed from the graph, its launch
- *     parameters updated in place, which shortens the gaps between its
- *     kernels; inside a caller's own stream capture, and in
- *     kda_prefill_noalloc, the kernels are launched directly).
+ *     side stream, a few events and a capture stream, and keeps up to 8
+ *     executable CUDA graphs, one per launch structure (number of
+ *     segments): each kda_prefill call is captured on that stream and
+ *     replayed from the graph of its structure, its launch parameters
+ *     updated in place, which shortens the gaps between its kernels; inside
+ *     a caller's own stream capture, and in kda_prefill_noalloc, the kernels
+ *     are launched directly).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  No entry point synchronises the stream.
  *   - Arguments are validated on the host before anything is launched; an

@@ -1127,11 +1127,15 @@ cudaError_t tc_kernel_attributes()
 }
 
 // Per thread and device: a private stream on which a call's launches are
-// captured, and the executable graph they were last replayed from.
+// captured, and a few executable graphs, one per launch structure (the number
+// of segments, and whether K1 runs at all), reused least recently first.
+constexpr int kGraphCache = 8;
 struct GraphCtx {
     int device = -1;
     cudaStream_t cap = nullptr;
-    cudaGraphExec_t exec = nullptr;
+    int key[kGraphCache] = {};
+    cudaGraphExec_t exec[kGraphCache] = {};
+    uint64_t used[kGraphCache] = {}, tick = 0;
 };
 thread_local GraphCtx g_graph[kMaxDevices];
 }  // namespace
@@ -1186,26 +1190,36 @@ cudaError_t launch_prefill_tc_graph(const PrefillArgs &a)
         (void)cudaGetLastError();
         return e != cudaSuccess ? e : enqueue_prefill_tc(a, a.stream);
     }
-    cudaError_t r = cudaErrorInvalidValue;
-    if (g.exec) {
-        cudaGraphExecUpdateResultInfo info;
-        r = cudaGraphExecUpdate(g.exec, graph, &info);
-        if (r != cudaSuccess) {
-            (void)cudaGetLastError();
-            cudaGraphExecDestroy(g.exec);
-            g.exec = nullptr;
-        }
+    // the cached graph of this launch structure takes the new parameters; a
+    // structure not cached replaces the least recently used graph
+    const int key = 2 * a.plan.nseg + (a.max_chunks > 0 ? 1 : 0);
+    int slot = -1, lru = 0;
+    for (int i = 0; i < kGraphCache; ++i) {
+        if (g.exec[i] && g.key[i] == key) slot = i;
+        if (g.used[i] < g.used[lru]) lru = i;
     }
-    if (!g.exec) {
-        r = cudaGraphInstantiate(&g.exec, graph, 0);
-        if (r != cudaSuccess) g.exec = nullptr;
+    cudaError_t r = cudaErrorInvalidValue;
+    if (slot >= 0) {
+        cudaGraphExecUpdateResultInfo info;
+        r = cudaGraphExecUpdate(g.exec[slot], graph, &info);
+        if (r != cudaSuccess) (void)cudaGetLastError();
+    } else {
+        slot = lru;
+    }
+    if (r != cudaSuccess) {
+        if (g.exec[slot]) cudaGraphExecDestroy(g.exec[slot]);
+        g.exec[slot] = nullptr;
+        r = cudaGraphInstantiate(&g.exec[slot], graph, 0);
+        if (r != cudaSuccess) g.exec[slot] = nullptr;
+        g.key[slot] = key;
     }
     cudaGraphDestroy(graph);
     if (r != cudaSuccess) {
         (void)cudaGetLastError();
         return enqueue_prefill_tc(a, a.stream);
     }
-    return cudaGraphLaunch(g.exec, a.stream);
+    g.used[slot] = ++g.tick;
+    return cudaGraphLaunch(g.exec[slot], a.stream);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a)
