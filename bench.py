@@ -4,10 +4,13 @@
                     [--workload 2|4|5] [--no-decode] [--no-cpu-baseline]
 
 A step is one chunked prefill (sequence table, K1 preparation, K2 recurrence,
-checkpoint writer) over the chosen prefill workload, default "prefill B1 H32
-T8192 D128 bf16".  Decode (state GB/s) is timed in the same run over the
-decode workload "decode N256 H32 D128 bf16", 64 consecutive steps, and
-reported under "decode".  Inputs are seeded synthetic draws (see
+checkpoint writer) over the chosen prefill workload, default the largest one
+that fits one GPU, "varlen prefill 16 seqs U[1024,32768] H32 D128 bf16"
+(274,076 tokens).  The other prefill workloads ("prefill B1 H32 T8192 D128
+bf16" and the 131,072-token prefill with four 32K-token snapshots) are timed
+in the same run with fewer steps and reported under "prefill_other".  Decode
+(state GB/s) is timed over the decode workload "decode N256 H32 D128 bf16",
+64 consecutive steps, and reported under "decode".  Inputs are seeded synthetic draws (see
 linear_attention_serving_k1_gb300/workloads.py) made on the device; every
 timed prefill step starts from an idle device and L2 is flushed (a 512 MiB
 write) before it.  (Back to back, without the synchronisation between steps,
@@ -208,7 +211,7 @@ def time_steps(fn, steps, warmup, flush_buf, stream):
 
 
 # ------------------------------------------------------------------ our arm
-def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True):
+def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True, graph=True):
     inp = workloads.make_prefill(w, device=dev)
     q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
     s0, cu = inp["init_state"], inp["cu_seqlens"]
@@ -239,6 +242,8 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True):
     # shorter gaps between kernels; reported beside the eager number
     graph_ms = None
     try:
+        if not graph:
+            raise RuntimeError("not requested")
         cap = torch.cuda.Stream(device=dev)
         cap.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -249,7 +254,8 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True):
         graph_ms = time_steps(graph.replay, steps, warmup, flush_buf, stream)
         assert kda.prefill_status(ws) == 0
     except RuntimeError as e:   # capture unsupported here: report the eager number only
-        print(f"graph replay skipped: {e}", file=sys.stderr)
+        if graph:
+            print(f"graph replay skipped: {e}", file=sys.stderr)
     barrier(world)
 
     if not e2e:
@@ -347,7 +353,7 @@ def bench_decode(steps_total, dev, flush_buf, warmup=3):
     return w, ms
 
 
-def cpu_baseline_prefill(w, max_token_heads=16_000_000):
+def cpu_baseline_prefill(w, max_token_heads=4_000_000):
     """Times the float64 oracle (OpenMP over sequence x head) on the prefill
     workload: the whole workload when it has at most max_token_heads
     token-heads, else its first heads.  Returns the dict of the JSON line."""
@@ -379,6 +385,16 @@ def run_ours(args):
     clk.start()
     ms, e2e_ms, h2d, d2h, launches, graph_ms = bench_prefill(w, args.steps, args.warmup, dev, flush_buf,
                                                              world, not args.no_e2e)
+    others = []
+    if not args.no_other:
+        for wi in (2, 4, 5):
+            if wi == args.workload:
+                continue
+            wo = workloads.workload(wi)
+            o_ms, _, _, _, o_launch, _ = bench_prefill(wo, max(3, args.steps // 2), args.warmup, dev, flush_buf,
+                                                        world, e2e=False, graph=False)
+            others.append((wo, wi, o_ms, o_launch))
+            torch.cuda.empty_cache()
     dec = None
     if not args.no_decode:
         dec_w, dec_ms = bench_decode(64, dev, flush_buf)
@@ -436,6 +452,19 @@ def run_ours(args):
             "graph_replay": graph,
             "clocks": clocks,
             "decode": dec}
+    if others:
+        line["prefill_other"] = []
+        for wo, wi, o_ms, o_launch in others:
+            o_mean = max_over_ranks(sum(o_ms) / len(o_ms), world)
+            o_bytes = prefill_algorithmic_bytes(wo)
+            o_gbs = o_bytes / (o_mean / 1e3) / 1e9
+            line["prefill_other"].append({
+                "workload": wo.name, "ms_per_step": round(o_mean, 4), "steps": len(o_ms),
+                "value": round(job_throughput(wo.total_tokens, sum(o_ms) / len(o_ms), world), 1),
+                "unit": "tokens/s", "gpu_launches": o_launch * len(o_ms),
+                "roofline": {"bound": "hbm", "achieved": round(o_gbs, 1), "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": round(o_gbs / peaks["hbm_gbs"], 4),
+                             "traffic": load_traffic(f"prefill_w{wi}"), "algorithmic_bytes_per_launch": o_bytes}})
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(w)
     if rank == 0:
@@ -495,8 +524,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 4, 5])
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 4, 5])
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     args = ap.parse_args()

@@ -7,9 +7,18 @@
 
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kda_common.cuh"
 
 namespace {
+
+// An NVTX range around one entry point (visible in a timeline profiler;
+// without a tool attached the calls return at once).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 thread_local std::string g_last_error;
 
@@ -146,7 +155,7 @@ namespace kda {
 kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
                         const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
                         float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
-                        kda_stream_t stream, bool use_graph)
+                        kda_stream_t stream, bool use_graph, const PoolArgs *pool)
 {
     Layout L;
     kda_status s = check_desc(desc, &L);
@@ -157,8 +166,17 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     if (!cu_seqlens && T % desc->num_seqs != 0)
         return fail(KDA_ERR_INVALID_ARG, "total_tokens %lld not a multiple of num_seqs %d (cu_seqlens NULL)",
                     (long long)T, desc->num_seqs);
-    if (desc->ckpt_stride > 0 && !ckpts && desc->ckpt_capacity > 0)
+    if (pool) {
+        if (pool->slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
+        if (!pool->pool && (pool->init_slots || pool->final_slots || pool->ckpt_slots))
+            return fail(KDA_ERR_INVALID_ARG, "state_pool is NULL but a slot table is given");
+        if (desc->ckpt_stride > 0 && desc->ckpt_capacity > 0 && !pool->ckpt_slots)
+            return fail(KDA_ERR_INVALID_ARG, "ckpt_slots is NULL but ckpt_capacity > 0");
+        if (pool->pool && ((uintptr_t)pool->pool & 15) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "state_pool must be 16-byte aligned");
+    } else if (desc->ckpt_stride > 0 && !ckpts && desc->ckpt_capacity > 0) {
         return fail(KDA_ERR_INVALID_ARG, "ckpts is NULL but ckpt_capacity > 0");
+    }
     if (!workspace) return fail(KDA_ERR_WORKSPACE, "workspace is NULL");
     if (workspace_bytes < L.total)
         return fail(KDA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
@@ -189,6 +207,18 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     a.plan = L.plan;
     a.seq_cap_chunks = L.plan.nseg > 1 ? L.plan.covered() : 0;
     a.scalar_gate = desc->scalar_gate != 0;
+    a.wait_limit = desc->wait_limit ? desc->wait_limit : kda::kDefaultWaitLimit;
+    a.init_slots = a.final_slots = a.ckpt_slots = nullptr;
+    a.pool_slots = 0;
+    if (pool) {   // every state lives in the pool; a NULL table means none of that kind
+        a.init_state = pool->init_slots ? pool->pool : nullptr;
+        a.final_state = pool->final_slots ? pool->pool : nullptr;
+        a.ckpts = desc->ckpt_stride > 0 && pool->ckpt_slots ? pool->pool : nullptr;
+        a.init_slots = pool->init_slots;
+        a.final_slots = pool->final_slots;
+        a.ckpt_slots = pool->ckpt_slots;
+        a.pool_slots = pool->slots;
+    }
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e;
@@ -214,8 +244,22 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
                        const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
                        kda_stream_t stream)
 {
+    NvtxRange r("kda_prefill");
     return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc, workspace,
                              workspace_bytes, stream, true);
+}
+
+kda_status kda_prefill_pooled(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const int32_t *cu_seqlens, void *out,
+                              float *state_pool, int64_t pool_slots, const int32_t *init_slots,
+                              const int32_t *final_slots, const int32_t *ckpt_slots,
+                              const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                              kda_stream_t stream)
+{
+    NvtxRange r("kda_prefill_pooled");
+    const kda::PoolArgs pool{state_pool, pool_slots, init_slots, final_slots, ckpt_slots};
+    return kda::prefill_call(q, k, v, g, beta, nullptr, cu_seqlens, out, nullptr, nullptr, desc, workspace,
+                             workspace_bytes, stream, true, &pool);
 }
 
 kda_status kda_prefill_status(void *workspace, kda_stream_t stream)
@@ -243,7 +287,7 @@ namespace {
 kda_status decode_common(const void *q, const void *k, const void *v, const float *g, const float *beta,
                          float *state, const int32_t *slots, int64_t pool, int32_t m,
                          const int32_t *commit, void *out, int32_t N, int32_t H, int32_t Dk, int32_t Dv,
-                         kda_dtype dtype, kda_stream_t stream)
+                         kda_dtype dtype, int32_t *status, kda_stream_t stream)
 {
     if (N < 0 || H < 0 || m < 0) return fail(KDA_ERR_INVALID_ARG, "N, m and H must be >= 0");
     if ((int64_t)N * m * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N*m*H too large");
@@ -258,7 +302,7 @@ kda_status decode_common(const void *q, const void *k, const void *v, const floa
     if (out == q || out == k || out == v || out == (void *)state)
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
     cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype, slots, pool, m,
-                                       commit, (cudaStream_t)stream);
+                                       commit, status, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     return KDA_OK;
 }
@@ -268,28 +312,32 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
                       const float *beta, float *state, void *out, int32_t N, int32_t H,
                       int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
 {
-    return decode_common(q, k, v, g, beta, state, nullptr, 0, 1, nullptr, out, N, H, Dk, Dv, dtype, stream);
+    NvtxRange r("kda_decode");
+    return decode_common(q, k, v, g, beta, state, nullptr, 0, 1, nullptr, out, N, H, Dk, Dv, dtype, nullptr,
+                         stream);
 }
 
 kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float *state_pool, int64_t pool_slots,
                             const int32_t *slot_ids, void *out, int32_t N, int32_t H, int32_t Dk,
-                            int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+                            int32_t Dv, kda_dtype dtype, int32_t *status, kda_stream_t stream)
 {
+    NvtxRange r("kda_decode_paged");
     if (pool_slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
     if (N > 0 && H > 0 && !slot_ids) return fail(KDA_ERR_INVALID_ARG, "slot_ids is NULL");
     return decode_common(q, k, v, g, beta, state_pool, slot_ids, pool_slots, 1, nullptr, out, N, H, Dk, Dv,
-                         dtype, stream);
+                         dtype, status, stream);
 }
 
 kda_status kda_decode_multi(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float *state, int64_t pool_slots, const int32_t *slot_ids,
                             const int32_t *commit_len, void *out, int32_t N, int32_t m, int32_t H,
-                            int32_t Dk, int32_t Dv, kda_dtype dtype, kda_stream_t stream)
+                            int32_t Dk, int32_t Dv, kda_dtype dtype, int32_t *status, kda_stream_t stream)
 {
+    NvtxRange r("kda_decode_multi");
     if (slot_ids && pool_slots < 0) return fail(KDA_ERR_INVALID_ARG, "pool_slots must be >= 0");
     return decode_common(q, k, v, g, beta, state, slot_ids, slot_ids ? pool_slots : 0, m, commit_len, out,
-                         N, H, Dk, Dv, dtype, stream);
+                         N, H, Dk, Dv, dtype, slot_ids ? status : nullptr, stream);
 }
 
 }  // extern "C"

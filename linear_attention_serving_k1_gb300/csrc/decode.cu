@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(THREADS)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
-              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit)
+              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status)
 {
     const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
@@ -63,6 +63,16 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float4 s[RPT];
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = __ldcs(S + (size_t)(r0 + j * RPI) * C4 + c4);
+
+    // Slots must be distinct: the head-0 CTA of sequence n compares its slot
+    // with those of sequences 0 .. n-1 (while its state loads are in flight)
+    // and reports a repeat in the caller's status word.
+    if (slots && status && hh == 0) {
+        const int32_t mine = slots[n];
+        bool dup = false;
+        for (size_t i = tid; i < n; i += THREADS) dup |= slots[i] == mine;
+        if (dup) atomicCAS(status, 0, (int32_t)KDA_ERR_INVALID_ARG);
+    }
 
     __shared__ float sh_qh[D], sh_kh[D], sh_a[D], sh_u[D];
     __shared__ float sh_part[3][NW];
@@ -151,16 +161,19 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 template <int D, typename T>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, float *state, void *out, int N, int H,
-                     const int32_t *slots, int64_t pool, int m, const int32_t *commit, cudaStream_t st)
+                     const int32_t *slots, int64_t pool, int m, const int32_t *commit, int32_t *status,
+                     cudaStream_t st)
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
     if (m == 1 && !commit)
         decode_kernel<D, T, THREADS, false><<<blocks, THREADS, 0, st>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr);
+            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr,
+            status);
     else
         decode_kernel<D, T, THREADS, true><<<blocks, THREADS, 0, st>>>(
-            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit);
+            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit,
+            status);
     return cudaGetLastError();
 }
 
@@ -169,16 +182,19 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
-                          const int32_t *commit, cudaStream_t stream)
+                          const int32_t *commit, int32_t *status, cudaStream_t stream)
 {
     if ((size_t)N * H == 0 || m == 0) return cudaSuccess;
     if (D == 128)
         return dtype == KDA_DTYPE_BF16
-                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream)
-                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream);
+                   ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit,
+                                                  status, stream)
+                   : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status,
+                                          stream);
     return dtype == KDA_DTYPE_BF16
-               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream)
-               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, stream);
+               ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status,
+                                             stream)
+               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status, stream);
 }
 
 }  // namespace kda

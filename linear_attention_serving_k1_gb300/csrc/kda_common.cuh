@@ -34,6 +34,21 @@ struct DevStatus {
     int32_t pad[63];
 };
 
+// Records `code` in the status word unless an earlier condition is already
+// recorded there (the first one reported wins).
+__device__ __forceinline__ void record_status(DevStatus *st, int32_t code)
+{
+    atomicCAS(&st->code, 0, code);
+}
+
+// Largest magnitude of the exponent of one factor of the chunked form's
+// decayed Gram product.  Per key channel the in-chunk log-decays b_r are
+// referred to the midpoint B of their range (b_r - B and B - b_r), so the
+// factors stay within e^{+-kMaxDecayExp} while the chunk's total decay stays
+// below 2 * kMaxDecayExp; beyond that the factors are clamped (finite, no
+// longer exact) and the chunk is reported as KDA_ERR_UNSUPPORTED.
+constexpr float kMaxDecayExp = 80.f;
+
 // Per-call table produced on the device from cu_seqlens (no host sync):
 //   cu[n]        token offset of sequence n (a validated copy)
 //   chunk_off[n] first global chunk index of sequence n (prefix sum of ceil(len/C))
@@ -83,8 +98,42 @@ struct PrefillArgs {
     SegPlan plan;
     int seq_cap_chunks;          // chunks any sequence may have (0 = unbounded)
     bool scalar_gate;            // g is [T, H] (one decay per head), else [T, H, Dk]
+    uint32_t wait_limit;         // polls before a bounded device-side wait gives up
+    // State pool (kda_prefill_pooled): init_state, final_state and ckpts then
+    // all point to a pool of pool_slots [H, D, D] slots and these tables map
+    // sequence n (or checkpoint j) to its slot; NULL tables: dense arrays.
+    const int32_t *init_slots, *final_slots, *ckpt_slots;
+    int64_t pool_slots;
     cudaStream_t stream;
 };
+
+// Where a prefill's recurrence reads initial states and writes final states
+// and checkpoints: dense [N, H, D, D] / [capacity, H, D, D] arrays (NULL slot
+// tables) or slots of one pool (kda_prefill_pooled).
+struct StateIO {
+    const float *init;           // NULL: zero initial states
+    float *fin;                  // NULL: final states not written
+    float *ckpts;                // NULL: no checkpoints
+    const int32_t *init_slots, *final_slots, *ckpt_slots;
+    int64_t pool;                // slots of the pool (with slot tables)
+    int64_t capacity;            // checkpoint slots
+    int stride;                  // checkpoint stride in tokens (0: none)
+};
+
+inline StateIO state_io(const PrefillArgs &a)
+{
+    return StateIO{a.init_state, a.final_state, a.ckpts, a.init_slots, a.final_slots, a.ckpt_slots,
+                   a.pool_slots, a.ckpt_capacity, a.ckpts ? a.ckpt_stride : 0};
+}
+
+// Slot of entry i under an optional slot table: the table's entry when it is in
+// [0, pool), -1 otherwise (no state there); without a table, i itself.
+__device__ __forceinline__ int64_t pool_slot(const int32_t *slots, int64_t i, int64_t pool)
+{
+    if (!slots) return i;
+    const int64_t s = slots[i];
+    return (s >= 0 && s < pool) ? s : -1;
+}
 
 // Bytes of the K1 -> K2 handoff buffer for one (chunk, head).
 size_t simt_handoff_bytes_per_chunk(int D, int C);
@@ -105,12 +154,23 @@ SegPlan tc_segment_plan(const kda_prefill_desc *desc);
 // Validates `desc` and returns the workspace bytes kda_prefill needs for it
 // (on error: the status, with the thread-local message set).
 kda_status prefill_workspace_bytes(const kda_prefill_desc *desc, size_t *bytes);
+// A state pool and its slot tables (kda_prefill_pooled).
+struct PoolArgs {
+    float *pool;
+    int64_t slots;
+    const int32_t *init_slots, *final_slots, *ckpt_slots;
+};
 // kda_prefill's body; use_graph = false launches every kernel directly (no
-// CUDA graph is captured or instantiated: the no-allocation entry point)
+// CUDA graph is captured or instantiated: the no-allocation entry point).
+// With `pool`, states and checkpoints live in pool slots (init_state,
+// final_state and ckpts are ignored).
 kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
                         const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
                         float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
-                        kda_stream_t stream, bool use_graph);
+                        kda_stream_t stream, bool use_graph, const PoolArgs *pool = nullptr);
+
+// Default number of polls of a bounded device-side wait.
+constexpr uint32_t kDefaultWaitLimit = 1u << 22;
 // Sets the thread-local message that kda_last_error() returns; returns `s`.
 kda_status fail_with_message(kda_status s, const char *fmt, ...);
 
@@ -126,6 +186,6 @@ const char *launch_failure_detail();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
-                          const int32_t *commit, cudaStream_t stream);
+                          const int32_t *commit, int32_t *status, cudaStream_t stream);
 
 }  // namespace kda

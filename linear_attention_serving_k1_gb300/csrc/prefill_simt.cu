@@ -97,7 +97,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, int N, int H,
-               SeqTable tab, float *__restrict__ handoff, int scalar_gate)
+               SeqTable tab, float *__restrict__ handoff, int scalar_gate, DevStatus *st)
 {
     constexpr int P = D + 1;   // padded row pitch (bank-conflict free columns)
     extern __shared__ float smem[];
@@ -108,6 +108,7 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
     float *Lm = Vs + kC * P;          // [C][C+1]
     float *Tm = Lm + kC * (kC + 1);   // [C][C+1]
     float *bs = Tm + kC * (kC + 1);   // [C] beta
+    float *mu = bs + kC;              // [D] e^B, B = half the chunk's log-decay per channel
 
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     if (gc >= tab.chunk_off[N]) return;
@@ -143,24 +144,39 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
     __syncthreads();
 
     // 2. cumulative log-decay per channel and the decayed q/k (thread = channel).
+    //    The Gram factors are referred to the midpoint B = b_last / 2 of the
+    //    channel's decay range: Qg, Kg hold e^(b - B), Kd e^(B - b) (each within
+    //    e^(|b_last| / 2)); the true Qg, Kg are these times mu = e^B, and
+    //    Ke = Kd mu (b_last - B = B).
     if (tid < D) {
         const int d = tid;
+        auto gate = [&](int r) {
+            return scalar_gate ? g[(size_t)(t0 + r) * H + h] : g[((size_t)(t0 + r) * H + h) * D + d];
+        };
+        float tot = 0.f;
+        for (int r = 0; r < L; ++r) tot += gate(r);
+        const float B = 0.5f * tot;
+        bool strong = false;
         float b = 0.f;
         for (int r = 0; r < kC; ++r) {
-            if (r < L) b += scalar_gate ? g[(size_t)(t0 + r) * H + h] : g[((size_t)(t0 + r) * H + h) * D + d];
-            const float e = expf(b), ei = expf(-b);
+            if (r < L) b += gate(r);
+            const float x = b - B;
+            strong |= fabsf(x) > kMaxDecayExp;
+            const float e = expf(fminf(x, kMaxDecayExp)), ei = expf(fminf(-x, kMaxDecayExp));
             const float kh = Kg[r * P + d];
             Qg[r * P + d] *= e;
             Kg[r * P + d] = kh * e;
             Kd[r * P + d] = kh * ei;
         }
-        const float gl = expf(b);
-        ho.gl[d] = gl;
-        for (int r = 0; r < kC; ++r) ho.Ke[r * D + d] = Kd[r * P + d] * gl;
+        if (strong) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
+        const float m = expf(B);
+        mu[d] = m;
+        ho.gl[d] = m * m;
+        for (int r = 0; r < kC; ++r) ho.Ke[r * D + d] = Kd[r * P + d] * m;
     }
     __syncthreads();
 
-    for (int i = tid; i < kC * D; i += kThreads) ho.Qg[i] = Qg[(i / D) * P + (i % D)];
+    for (int i = tid; i < kC * D; i += kThreads) ho.Qg[i] = Qg[(i / D) * P + (i % D)] * mu[i % D];
 
     // 3. Gram products: thread owns rows tr + 16a and columns ti + 16b (a, b < 4).
     {
@@ -215,7 +231,7 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
             wk += t * Kg[i * P + d];
             uv += t * Vs[i * P + d];
         }
-        ho.Wk[o] = wk;
+        ho.Wk[o] = wk * mu[d];
         ho.Uv[o] = uv;
     }
 }
@@ -226,10 +242,8 @@ constexpr int kBV = 32;
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
-k2_simt_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
-               const float *__restrict__ handoff, T *__restrict__ out,
-               float *__restrict__ final_state, float *__restrict__ ckpts, int stride,
-               int64_t capacity)
+k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__ handoff,
+               T *__restrict__ out)
 {
     constexpr int P = D + 1;
     constexpr int NB = D / kBV;
@@ -247,11 +261,18 @@ k2_simt_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const int jb = blockIdx.x % NB;
     const int h = (blockIdx.x / NB) % H;
     const int n = blockIdx.x / (NB * H);
-    const size_t sbase = ((size_t)n * H + h) * D * D + jb * kBV;   // state [D][D] block origin
+    // this CTA's column block of the chain's initial and final states (dense
+    // arrays or pool slots)
+    const size_t DD = (size_t)D * D;
+    const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
+    const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
+    const float *init_blk = is >= 0 ? io.init + ((size_t)is * H + h) * DD + jb * kBV : nullptr;
+    float *fin_blk = fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD + jb * kBV : nullptr;
+    const int stride = io.stride;
 
     for (int i = tid; i < D * kBV; i += kThreads) {
         const int d = i / kBV, j = i % kBV;
-        Ss[i] = init_state ? init_state[sbase + (size_t)d * D + j] : 0.f;
+        Ss[i] = init_blk ? init_blk[(size_t)d * D + j] : 0.f;
     }
     const int c_begin = tab.chunk_off[n], c_end = tab.chunk_off[n + 1];
     const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
@@ -300,27 +321,27 @@ k2_simt_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         }
         // checkpoint after every `stride` tokens of the sequence
         const int done = lc * kC + L;
-        if (stride > 0 && ckpts && L == kC && done % stride == 0) {
-            const int64_t slot = (int64_t)tab.ckpt_off[n] + done / stride - 1;
-            if (slot < capacity) {
+        if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
+            const int64_t jc = (int64_t)tab.ckpt_off[n] + done / stride - 1;
+            const int64_t ps = jc < io.capacity ? pool_slot(io.ckpt_slots, jc, io.pool) : -1;
+            if (ps >= 0) {
                 __syncthreads();
-                float *dst = ckpts + ((size_t)slot * H + h) * D * D + jb * kBV;
+                float *dst = io.ckpts + ((size_t)ps * H + h) * DD + jb * kBV;
                 for (int i = tid; i < D * kBV; i += kThreads)
                     dst[(size_t)(i / kBV) * D + i % kBV] = Ss[i];
             }
         }
     }
     __syncthreads();
-    if (final_state)
-        for (int i = tid; i < D * kBV; i += kThreads)
-            final_state[sbase + (size_t)(i / kBV) * D + i % kBV] = Ss[i];
+    if (fin_blk)
+        for (int i = tid; i < D * kBV; i += kThreads) fin_blk[(size_t)(i / kBV) * D + i % kBV] = Ss[i];
 }
 
 template <int D, typename T>
 cudaError_t launch_simt_t(const PrefillArgs &a)
 {
     constexpr int P = D + 1;
-    const size_t sm1 = sizeof(float) * ((size_t)4 * kC * P + 2 * kC * (kC + 1) + kC);
+    const size_t sm1 = sizeof(float) * ((size_t)4 * kC * P + 2 * kC * (kC + 1) + kC + D);
     const size_t sm2 = sizeof(float) * ((size_t)D * kBV + kC * kBV + 3 * kC * P +
                                         kC * (kC + 1) + kC * kBV + D);
     cudaError_t e;
@@ -334,13 +355,12 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
         dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
         k1_simt_kernel<D, T><<<g1, kThreads, sm1, a.stream>>>(
             (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.N, a.H, a.tab,
-            (float *)a.handoff, a.scalar_gate ? 1 : 0);
+            (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned g2 = (unsigned)((size_t)a.N * a.H * (D / kBV));
-    k2_simt_kernel<D, T><<<g2, kThreads, sm2, a.stream>>>(
-        a.init_state, a.N, a.H, a.tab, (const float *)a.handoff, (T *)a.out, a.final_state,
-        a.ckpts, a.ckpt_stride, a.ckpt_capacity);
+    k2_simt_kernel<D, T><<<g2, kThreads, sm2, a.stream>>>(state_io(a), a.N, a.H, a.tab,
+                                                           (const float *)a.handoff, (T *)a.out);
     return cudaGetLastError();
 }
 

@@ -85,21 +85,25 @@ __device__ __forceinline__ int find_seq_tc(const int32_t *chunk_off, int N, int 
 
 __device__ __forceinline__ void record_timeout(DevStatus *st)
 {
-    atomicExch(&st->code, (int32_t)KDA_ERR_TIMEOUT);
+    record_status(st, (int32_t)KDA_ERR_TIMEOUT);
 }
 
-// Polls `bar` for phase `parity`; gives up after a bounded number of polls, or
-// early when another role of the CTA has flagged an abort.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+// Polls `bar` for phase `parity`; gives up after `limit` polls, or early when
+// another role of the CTA has flagged an abort.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t limit)
 {
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 1023u) == 1023u && *abort_flag) return false;
     }
     return false;
 }
 
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Polls allowed to the waits that drain a CTA's own tensor-core work and
+// copies before it frees its TMEM and exits (independent of the call's wait
+// limit: that work always completes, and must have before the exit).
+constexpr uint32_t kDrainLimit = 1u << 22;
 
 // ============================================================ K1
 // One CTA (256 threads, two CTAs per SM) per (chunk, head).  The Gram product
@@ -168,10 +172,10 @@ __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
-             DevStatus *st)
+             DevStatus *st, uint32_t wait_limit)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t mbar, qbar;
+    __shared__ uint64_t mbar, qbar, dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
     // (16-byte aligned: read as float2 / float4)
@@ -261,6 +265,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     if (tid == 0) {
         mbar_init(&mbar, 1);
         mbar_init(&qbar, 1);
+        mbar_init(&dbar, 1);
         fence_mbar_init();
     }
     fence_before_sync();
@@ -268,6 +273,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
     const uint32_t tm = tmem_sh;
     bool ok = true;
+    bool strong = false;   // a decay factor of this thread's rows left the exact range
     float nsq = 0.f;   // squared row norm of value lane >> 1 (q rows rb .. rb + 7, then k rows)
 
     // 1-3. per channel half p: cumulative gates, decayed operands, partial row
@@ -284,7 +290,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             tot[warp][2 * lane + 1] = c1;
         }
         // the MMA of the previous half has read the operand tiles
-        if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+        if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (p == 0 && tid < kC) bs[tid] = beta_r;
         __syncthreads();
         if (p == 1) ok = ok && wflag[0];
@@ -296,8 +302,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             last0 += a0;
             last1 += a1;
         }
-        const float gam0 = __expf(last0), gam1 = __expf(last1);
-        if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = make_float2(gam0, gam1);
+        // Per channel the decays are referred to the midpoint B = b_last / 2 of
+        // their range [b_last, 0]: the Gram factors e^(b - B) and e^(B - b) then
+        // stay within e^(|b_last| / 2), and mu = e^B carries the rest
+        // (Kg' = k e^(b - B) mu, Ke' = k e^(B - b) mu since b_last - B = B).
+        const float2 ref = make_float2(0.5f * last0, 0.5f * last1);
+        const float2 mu2 = make_float2(__expf(ref.x), __expf(ref.y));
+        if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = __fmul2_rn(mu2, mu2);
         uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4], qp0[4], qp1[4];
         // this half's squared row norms, summed over the warp's 32 lanes by
         // halving exchanges: the exchange across lane bit 4 leaves q of row
@@ -308,7 +319,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const bool up16 = lane & 16;
         // the two channels of a thread as packed fp32 pairs
         float2 bb = make_float2(pre0, pre1);
-        const float2 gam2 = make_float2(gam0, gam1);
 #pragma unroll
         for (int j2 = 0; j2 < 8; j2 += 2) {
             float kgx[2][2], vx[2][2], kex[2][2], qgx[2][2];
@@ -316,19 +326,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int u = 0; u < 2; ++u) {
                 const int j = j2 + u, r = rb + j;
                 bb = __fadd2_rn(bb, gv[j]);
-                const float2 e = make_float2(__expf(bb.x), __expf(bb.y));
-                const float2 ei = make_float2(__expf(-bb.x), __expf(-bb.y));
+                const float2 x = __fadd2_rn(bb, make_float2(-ref.x, -ref.y));
+                strong |= fabsf(x.x) > kMaxDecayExp || fabsf(x.y) > kMaxDecayExp;
+                const float2 e = make_float2(__expf(fminf(x.x, kMaxDecayExp)), __expf(fminf(x.y, kMaxDecayExp)));
+                const float2 ei = make_float2(__expf(fminf(-x.x, kMaxDecayExp)), __expf(fminf(-x.y, kMaxDecayExp)));
                 const float2 qq = make_float2(bf_lo(qv[j]), bf_hi(qv[j])), kk = make_float2(bf_lo(kv[j]), bf_hi(kv[j]));
                 const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
                 const float2 s2 = __ffma2_rn(qk1, qk1, __fmul2_rn(qk0, qk0));
                 sq[j] = (up16 ? s2.y : s2.x) + __shfl_xor_sync(0xffffffffu, up16 ? s2.x : s2.y, 16);
-                const float2 kg = __fmul2_rn(kk, e), qg = __fmul2_rn(qq, e), kd = __fmul2_rn(kk, ei);
-                const float2 ke = __fmul2_rn(kd, gam2);   // k' e^(b_last - b)
+                // Gram factors (referred to B), then the true decayed rows
+                const float2 kgr = __fmul2_rn(kk, e), qgr = __fmul2_rn(qq, e), kd = __fmul2_rn(kk, ei);
+                const float2 kg = __fmul2_rn(kgr, mu2), qg = __fmul2_rn(qgr, mu2);
+                const float2 ke = __fmul2_rn(kd, mu2);   // k' e^(b_last - b)
                 const uint32_t lo = 2 * lane;
                 *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(kg.x), round_tf32(kg.y));
+                    make_float2(round_tf32(kgr.x), round_tf32(kgr.y));
                 *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(64 + r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(qg.x), round_tf32(qg.y));
+                    make_float2(round_tf32(qgr.x), round_tf32(qgr.y));
                 *reinterpret_cast<float2 *>(sm + K1_KD + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
                     make_float2(round_tf32(kd.x), round_tf32(kd.y));
                 qgx[0][u] = qg.x; qgx[1][u] = qg.y;
@@ -397,7 +411,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             mma_commit(&mbar);
         }
     }
-    if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    if (strong) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
+    if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
     __syncthreads();   // G' complete and seen by all: the Gram region may be reused
     fence_after_sync();
     ok = ok && wflag[1];
@@ -605,15 +620,17 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, kWaitLimit);
+    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
     __syncthreads();
     fence_after_sync();
     ok = ok && wflag[2];
 
     // the Kg'^T tile is dead: the parked Qg'^T tile comes back into its place
+    bool q_issued = false;   // (thread 0) the copy is in flight until qbar completes
     if (tid == 0 && ok) {
         mbar_arrive_expect_tx(&qbar, 16384);
         bulk_g2s(sm + K1_KGT, qg_park, 16384, &qbar);
+        q_issued = true;
     }
     // diag(rq) as an f16 operand tile (rows i, K = r; 64 x 64) for Q' = diag(rq) Qg' - Mc Wk
 #pragma unroll
@@ -661,7 +678,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); -Mc Wk = -Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
-    if (tid == 0 && ok && mbar_wait_bounded(&qbar, 0, kWaitLimit)) {
+    bool q_landed = false;
+    if (tid == 0 && ok && (q_landed = mbar_wait_bounded(&qbar, 0, wait_limit))) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
         const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_KGT);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
@@ -677,7 +695,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     make_desc(bq + ks * 256, LBO_KIN, SBO_K64), id64, 1);
         mma_commit(&mbar);
     }
-    if (tid == 0) wflag[3] = ok && mbar_wait_bounded(&mbar, 1, kWaitLimit);
+    if (tid == 0) wflag[3] = ok && q_landed && mbar_wait_bounded(&mbar, 1, wait_limit);
     __syncthreads();
     fence_after_sync();
     ok = ok && wflag[3];
@@ -715,7 +733,15 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             }
         }
     }
-    if (!ok && tid == 0) record_timeout(st);
+    if (!ok && tid == 0) {
+        // A wait gave up: before the TMEM is freed and the shared memory
+        // handed back, every MMA this thread issued and the parked tile's copy
+        // must have completed (a commit arrives once all earlier MMAs are done).
+        record_timeout(st);
+        mma_commit(&dbar);
+        mbar_wait_bounded(&dbar, 0, kDrainLimit);
+        if (q_issued) mbar_wait_bounded(&qbar, 0, kDrainLimit);
+    }
     if (tid == 0) bulk_wait_all();
     fence_before_sync();
     __syncthreads();
@@ -758,14 +784,12 @@ __device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, c
 
 
 __global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
-k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
+k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
-             float *__restrict__ carry, bf16 *__restrict__ out,
-             float *__restrict__ final_state, float *__restrict__ ckpts, int stride,
-             int64_t capacity, DevStatus *st)
+             float *__restrict__ carry, bf16 *__restrict__ out, DevStatus *st, uint32_t wait_limit)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], gfull[kGamSlots], sdone, pread[2], sready[2];
+    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], gfull[kGamSlots], sdone, pread[2], sready[2], dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -780,12 +804,19 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     const int nch = G == 0 ? nch_seq : max(0, min(seg_lo + G, nch_seq) - seg_lo);
     const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
     const bool first_seg = c_lo == 0, last_seg = G == 0 || seg_lo + G >= nch_seq;
-    const size_t sbase = ((size_t)n * H + h) * kD * kD;
+    constexpr size_t DD = (size_t)kD * kD;
+    const size_t sbase = ((size_t)n * H + h) * DD;   // this chain's block of the carry buffer
+    // initial and final state blocks of this chain (dense arrays or pool slots)
+    const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
+    const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
+    const float *init_blk = is >= 0 ? io.init + ((size_t)is * H + h) * DD : nullptr;
+    float *fin_blk = fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD : nullptr;
+    const int stride = io.stride;
     const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * slot_chunks;
     if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
-        if (first_seg && nch_seq == 0 && final_state)
+        if (first_seg && nch_seq == 0 && fin_blk)
             for (int i = tid; i < kD * kD; i += blockDim.x)
-                final_state[sbase + i] = init_state ? init_state[sbase + i] : 0.f;
+                fin_blk[i] = init_blk ? init_blk[i] : 0.f;
         return;
     }
     // record of the sequence's chunk c_lo + i
@@ -798,6 +829,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         }
         for (int j = 0; j < kGamSlots; ++j) mbar_init(&gfull[j], 1);
         mbar_init(&sdone, 1);
+        mbar_init(&dbar, 1);
         for (int j = 0; j < 2; ++j) mbar_init(&pread[j], K2_STATE_THREADS);   // per accumulator buffer
         for (int j = 0; j < 2; ++j) mbar_init(&sready[j], K2_STATE_THREADS / 2);
         abort_flag = 0;
@@ -840,8 +872,8 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         const int s = c % K2_STAGES;
         const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
         const uint32_t idesc = idesc_f16(128, 192);
-        bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v);
-        okw = okw && (c < 2 || wait_or_abort(&pread[c & 1], ((c >> 1) - 1) & 1, abort_v));
+        bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v, wait_limit);
+        okw = okw && (c < 2 || wait_or_abort(&pread[c & 1], ((c >> 1) - 1) & 1, abort_v, wait_limit));
         if (!okw) return false;
         fence_after_sync();
 #pragma unroll
@@ -855,13 +887,13 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
         const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
         const uint32_t sop = smem_u32(sm + K2_SOP);
         const uint32_t idesc = idesc_f16(128, 192);
-        if (!wait_or_abort(&sready[0], c & 1, abort_v)) return false;
+        if (!wait_or_abort(&sready[0], c & 1, abort_v, wait_limit)) return false;
         fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
                     make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
-        if (!wait_or_abort(&sready[1], c & 1, abort_v)) return false;
+        if (!wait_or_abort(&sready[1], c & 1, abort_v, wait_limit)) return false;
         fence_after_sync();
 #pragma unroll
         for (int ks = 4; ks < 8; ++ks)
@@ -884,7 +916,7 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
                 // state-independent steps of chunk c + 1
                 if (!issue_dpart(c)) { alive = false; break; }
                 if (c + K2_STAGES < nch) {
-                    if (!wait_or_abort(&empty[c % K2_STAGES], (c / K2_STAGES) & 1, abort_v)) { alive = false; break; }
+                    if (!wait_or_abort(&empty[c % K2_STAGES], (c / K2_STAGES) & 1, abort_v, wait_limit)) { alive = false; break; }
                     issue_copy(c + K2_STAGES);
                 }
                 if (c + 1 < nch && !issue_rpart(c + 1)) { alive = false; break; }
@@ -893,10 +925,10 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
     } else {
         // ---------------------------------------------------------- state
         float S[32];
-        const float *src_state = first_seg ? init_state : carry;
+        const float *src_state = first_seg ? init_blk : carry + sbase;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            S[j] = src_state ? src_state[sbase + (size_t)(32 * qd + j) * kD + e] : 0.f;
+            S[j] = src_state ? src_state[(size_t)(32 * qd + j) * kD + e] : 0.f;
         write_sop_quarter(sm + K2_SOP, e, qd, S);
         fence_async_smem();
         mbar_arrive(&sready[qd >> 1]);
@@ -904,8 +936,8 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
             // gamma has landed (its slot's barrier cannot run ahead: slot c % 4 is
             // refilled only after the product of chunk c + 2, which needs this
             // thread's S^T of chunk c + 1) and the chunk's product is in TMEM
-            if (!wait_or_abort(&gfull[c % kGamSlots], (c / kGamSlots) & 1, abort_v) ||
-                !wait_or_abort(&sdone, c & 1, abort_v)) {
+            if (!wait_or_abort(&gfull[c % kGamSlots], (c / kGamSlots) & 1, abort_v, wait_limit) ||
+                !wait_or_abort(&sdone, c & 1, abort_v, wait_limit)) {
                 alive = false;
                 break;
             }
@@ -966,28 +998,35 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
             // (output of this chunk done)
             // checkpoint after every `stride` tokens of the sequence
             const int done = (c_lo + c) * kC + L;
-            if (stride > 0 && ckpts && L == kC && done % stride == 0) {
-                const int64_t slot = (int64_t)tab.ckpt_off[n] + done / stride - 1;
-                if (slot < capacity) {
-                    float *dst = ckpts + ((size_t)slot * H + h) * kD * kD + e;
+            if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
+                const int64_t j = (int64_t)tab.ckpt_off[n] + done / stride - 1;
+                const int64_t ps = j < io.capacity ? pool_slot(io.ckpt_slots, j, io.pool) : -1;
+                if (ps >= 0) {
+                    float *dst = io.ckpts + ((size_t)ps * H + h) * DD + e;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[(size_t)(32 * qd + j) * kD] = S[j];
                 }
             }
         }
         if (alive)
-            if (float *dst_state = last_seg ? final_state : carry) {
+            if (float *dst_state = last_seg ? fin_blk : carry + sbase) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dst_state[sbase + (size_t)(32 * qd + j) * kD + e] = S[j];
+                for (int j = 0; j < 32; ++j) dst_state[(size_t)(32 * qd + j) * kD + e] = S[j];
             }
     }
     if (!alive) {
         *abort_v = 1;
         if (lane == 0) record_timeout(st);
-        // never leave a copy in flight
-        if (issuer)
+        // never leave a copy or an MMA in flight: the last stages' copies land,
+        // and a commit arrives once every MMA the issuer started is complete
+        if (issuer) {
             for (int c = max(0, copied - K2_STAGES); c < copied; ++c)
-                mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kWaitLimit);
+                mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kDrainLimit);
+            for (int c = max(0, copied - kGamSlots); c < copied; ++c)
+                mbar_wait_bounded(&gfull[c % kGamSlots], (c / kGamSlots) & 1, kDrainLimit);
+            mma_commit(&dbar);
+            mbar_wait_bounded(&dbar, 0, kDrainLimit);
+        }
     }
 
     fence_before_sync();
@@ -999,6 +1038,31 @@ k2_tc_kernel(const float *__restrict__ init_state, int N, int H, SeqTable tab,
 }  // namespace
 
 size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
+
+namespace {
+// Streaming multiprocessors of the current device (read once per device); 152,
+// a GB300's count, when no device can be queried (a host-only call without a
+// GPU).
+int64_t device_sm_count()
+{
+    constexpr int kDevs = 64;
+    static std::atomic<int> cached[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            return 152;
+        }
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+}  // namespace
 
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
@@ -1012,7 +1076,8 @@ SegPlan tc_segment_plan(const kda_prefill_desc *d)
     // covers two waves only.  The segment just after the first takes the
     // remainder.  At most kMaxSegments segments (else uniform, as for an
     // explicit segment_chunks, which is raised to that bound where needed).
-    constexpr int64_t kSMs = 152, kMaxChains = 96, kMinG = 4;
+    constexpr int64_t kMaxChains = 96, kMinG = 4;
+    const int64_t kSMs = device_sm_count();
     const int64_t T = d->total_tokens;
     const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
     const int64_t maxc = (len + d->chunk - 1) / d->chunk;
@@ -1235,15 +1300,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if (p.nseg <= 1) {   // one K1 over every chunk, then one K2 over every sequence
         if (a.max_chunks > 0) {
             k1_tc_kernel<<<(unsigned)((size_t)a.max_chunks * a.H), K1_THREADS, K1_SMEM, a.stream>>>(
-                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.scalar_gate ? 1 : 0, a.status);
+                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.scalar_gate ? 1 : 0, a.status,
+                a.wait_limit);
             if ((e = cudaGetLastError()) != cudaSuccess) {
                 note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
                 return e;
             }
         }
         k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
-            a.init_state, a.N, a.H, a.tab, ring, 0, 0, 0, 0, nullptr, (bf16 *)a.out, a.final_state,
-            a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
+            state_io(a), a.N, a.H, a.tab, ring, 0, 0, 0, 0, nullptr, (bf16 *)a.out, a.status, a.wait_limit);
         if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
         return e;
     }
@@ -1259,7 +1324,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         const unsigned k1_grid = (unsigned)((size_t)a.N * cnt * a.H);
         if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
         k1_tc_kernel<<<k1_grid, K1_THREADS, K1_SMEM, a.stream>>>(
-            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.scalar_gate ? 1 : 0, a.status);
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.scalar_gate ? 1 : 0, a.status,
+            a.wait_limit);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
             break;
@@ -1267,8 +1333,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(c->side, c->k1[slot], 0)) != cudaSuccess) break;
         k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, c->side>>>(
-            a.init_state, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out,
-            a.final_state, a.ckpts, a.ckpt_stride, a.ckpt_capacity, a.status);
+            state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
+            a.wait_limit);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
             break;

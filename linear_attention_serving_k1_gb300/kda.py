@@ -22,8 +22,8 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
-           "kda_decode", "kda_decode_paged", "kda_decode_multi", "kda_prefill_noalloc", "kda_last_error",
-           "kda_version")
+           "kda_prefill_pooled", "kda_decode", "kda_decode_paged", "kda_decode_multi", "kda_prefill_noalloc",
+           "kda_last_error", "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -41,7 +41,8 @@ class PrefillDesc(ctypes.Structure):
                 ("head_dim_v", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
                 ("ckpt_capacity", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
-                ("segment_chunks", ctypes.c_int32), ("scalar_gate", ctypes.c_int32)]
+                ("segment_chunks", ctypes.c_int32), ("scalar_gate", ctypes.c_int32),
+                ("wait_limit", ctypes.c_uint32)]
 
 
 _lib = None
@@ -67,10 +68,14 @@ def load_library(path: Optional[str] = None):
     lib.kda_prefill_status.argtypes = [_vp, _vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_prefill_pooled.restype = ctypes.c_int
+    lib.kda_prefill_pooled.argtypes = [_vp] * 8 + [ctypes.c_int64, _vp, _vp, _vp, ctypes.POINTER(PrefillDesc),
+                                                   _vp, ctypes.c_size_t, _vp]
     lib.kda_decode_paged.restype = ctypes.c_int
-    lib.kda_decode_paged.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_decode_paged.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp] + [ctypes.c_int32] * 5 + [_vp, _vp]
     lib.kda_decode_multi.restype = ctypes.c_int
-    lib.kda_decode_multi.argtypes = [_vp] * 6 + [ctypes.c_int64, _vp, _vp, _vp] + [ctypes.c_int32] * 6 + [_vp]
+    lib.kda_decode_multi.argtypes = ([_vp] * 6 + [ctypes.c_int64, _vp, _vp, _vp] + [ctypes.c_int32] * 6 +
+                                     [_vp, _vp])
     lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_noalloc.argtypes = [_vp] * 10 + [ctypes.POINTER(PrefillDesc), _vp]
     lib.kda_last_error.restype = ctypes.c_char_p
@@ -112,9 +117,9 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
               ckpt_stride: int = 0, ckpt_capacity: int = 0, max_seq_len: int = 0,
-              segment_chunks: int = 0, scalar_gate: bool = False) -> PrefillDesc:
+              segment_chunks: int = 0, scalar_gate: bool = False, wait_limit: int = 0) -> PrefillDesc:
     return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity,
-                       max_seq_len, segment_chunks, int(bool(scalar_gate)))
+                       max_seq_len, segment_chunks, int(bool(scalar_gate)), wait_limit)
 
 
 def workspace_size(desc: PrefillDesc) -> int:
@@ -143,7 +148,7 @@ def num_checkpoints(lens, ckpt_stride: int) -> int:
 def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
             chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
             out=None, final_state=None, workspace=None, stream=None, want_final: bool = True,
-            max_seq_len: int = 0, segment_chunks: int = 0):
+            max_seq_len: int = 0, segment_chunks: int = 0, wait_limit: int = 0):
     """Chunked KDA prefill through ``kda_prefill``.
 
     q, k: [T, H, D]; v: [T, H, D]; g: [T, H, D] (a decay per key channel) or
@@ -165,7 +170,7 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
     desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
-                     scalar_gate=g.dim() == 2)
+                     scalar_gate=g.dim() == 2, wait_limit=wait_limit)
     if workspace is None:
         workspace = alloc_workspace(desc, dev)
     code = load_library().kda_prefill(
@@ -204,6 +209,33 @@ def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_s
     return out, final_state, ckpts
 
 
+def prefill_pooled(q, k, v, g, beta, state_pool, init_slots=None, final_slots=None, cu_seqlens=None, *,
+                   num_seqs: Optional[int] = None, chunk: int = 64, ckpt_stride: int = 0, ckpt_slots=None,
+                   out=None, workspace=None, stream=None, max_seq_len: int = 0, segment_chunks: int = 0):
+    """Chunked prefill through ``kda_prefill_pooled``: sequence n starts from
+    slot ``init_slots[n]`` of ``state_pool`` [P, H, D, D] and its final state
+    goes to slot ``final_slots[n]``; snapshot j goes to slot ``ckpt_slots[j]``
+    (int32 tables on the device; None = none of that kind; an id outside
+    [0, P) is skipped).  Returns out."""
+    T, H, D = q.shape
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (num_seqs or 1)
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, v.shape[2], dtype=q.dtype, device=dev)
+    cap = ckpt_slots.numel() if (ckpt_stride > 0 and ckpt_slots is not None) else 0
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
+                     scalar_gate=g.dim() == 2)
+    if workspace is None:
+        workspace = alloc_workspace(desc, dev)
+    code = load_library().kda_prefill_pooled(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(out), _ptr(state_pool),
+        ctypes.c_int64(state_pool.shape[0]), _ptr(init_slots), _ptr(final_slots),
+        _ptr(ckpt_slots) if cap else None, ctypes.byref(desc), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(code)
+    return out
+
+
 def prefill_status(workspace: torch.Tensor, stream=None) -> int:
     """Device-side status of the last prefill on ``workspace`` (synchronises)."""
     return int(load_library().kda_prefill_status(_ptr(workspace), _stream(stream)))
@@ -220,22 +252,25 @@ def decode(q, k, v, g, beta, state, out=None, stream=None):
     return out
 
 
-def decode_paged(q, k, v, g, beta, state_pool, slot_ids, out=None, stream=None):
+def decode_paged(q, k, v, g, beta, state_pool, slot_ids, out=None, stream=None, status=None):
     """One decode step through ``kda_decode_paged``: sequence n reads and
     updates slot ``slot_ids[n]`` of ``state_pool`` [P, H, D, D] (int32 ids on
-    the device; an id outside [0, P) marks a padding row with a zero output)."""
+    the device; an id outside [0, P) marks a padding row with a zero output).
+    ``status`` (an int32 device tensor holding 0, or None) is set to
+    KDA_ERR_INVALID_ARG when two sequences name the same slot."""
     N, H, D = q.shape
     if out is None:
         out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
     code = load_library().kda_decode_paged(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool),
         ctypes.c_int64(state_pool.shape[0]), _ptr(slot_ids), _ptr(out), N, H, D, v.shape[2],
-        _dtype_code(q), _stream(stream))
+        _dtype_code(q), _ptr(status), _stream(stream))
     _check(code)
     return out
 
 
-def decode_multi(q, k, v, g, beta, state, commit_len=None, slot_ids=None, out=None, stream=None):
+def decode_multi(q, k, v, g, beta, state, commit_len=None, slot_ids=None, out=None, stream=None,
+                 status=None):
     """m tokens per sequence through ``kda_decode_multi``: q, k, g [N, m, H, D],
     v [N, m, H, D], beta [N, m, H]; ``state`` dense [N, H, D, D] or, with
     ``slot_ids``, a pool [P, H, D, D]; ``commit_len`` int32 [N] on the device
@@ -246,6 +281,7 @@ def decode_multi(q, k, v, g, beta, state, commit_len=None, slot_ids=None, out=No
     pool = state.shape[0] if slot_ids is not None else 0
     code = load_library().kda_decode_multi(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.c_int64(pool),
-        _ptr(slot_ids), _ptr(commit_len), _ptr(out), N, m, H, D, v.shape[3], _dtype_code(q), _stream(stream))
+        _ptr(slot_ids), _ptr(commit_len), _ptr(out), N, m, H, D, v.shape[3], _dtype_code(q), _ptr(status),
+        _stream(stream))
     _check(code)
     return out

@@ -134,6 +134,33 @@ def make_prefill(w: PrefillWorkload, device="cpu") -> dict:
                 cu_seqlens=cu.to(device) if w.varlen else None, cu_host=cu, workload=w)
 
 
+def scale_qk_rows(inp: dict, lo: float = 0.05, hi: float = 40.0, seed: int = 0) -> dict:
+    """The same inputs with every (token, head) row of q and k multiplied by its
+    own factor, log-uniform in [lo, hi] (drawn in fp32, the product cast back
+    to the inputs' dtype once), so that q and k reach the library un-normalised.
+    Returns a new dict; the other entries are shared."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    q, k = inp["q"], inp["k"]
+    T, H = q.shape[0], q.shape[1]
+    out = dict(inp)
+    for name, x in (("q", q), ("k", k)):
+        u = torch.rand(T, H, 1, generator=gen, dtype=torch.float32)
+        f = torch.exp(torch.log(torch.tensor(lo)) + u * (torch.log(torch.tensor(hi)) - torch.log(torch.tensor(lo))))
+        out[name] = (x.float().cpu() * f).to(x.dtype).to(x.device)
+    return out
+
+
+def strong_decay_gates(inp: dict, lo: float = 1.0, hi: float = 3.0, seed: int = 0) -> dict:
+    """The same inputs with g replaced by -U(lo, hi) per element (fp32): a decay
+    of 1 to 3 nepers per token and channel, so that one chunk of 64 tokens
+    decays by about e^-128.  Returns a new dict; the other entries are shared."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    g = inp["g"]
+    out = dict(inp)
+    out["g"] = (-(lo + (hi - lo) * torch.rand(g.shape, generator=gen, dtype=torch.float32))).to(g.device)
+    return out
+
+
 def make_decode_state(w: DecodeWorkload, device="cpu") -> torch.Tensor:
     gen = torch.Generator(device=device).manual_seed(w.seed)
     return torch.randn(w.N, w.H, w.D, w.D, generator=gen, device=device,

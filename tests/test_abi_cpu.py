@@ -154,13 +154,13 @@ def test_decode_paged_rejects_before_launch(lib):
     args = [p] * 6
     # NULL slot ids with rows to decode
     assert lib.kda_decode_paged(*args, ctypes.c_int64(8), None, ctypes.c_void_p(8192), 2, 2, 128, 128,
-                                kda.DTYPE_BF16, None) == -1
+                                kda.DTYPE_BF16, None, None) == -1
     # negative pool size
     assert lib.kda_decode_paged(*args, ctypes.c_int64(-1), p, ctypes.c_void_p(8192), 2, 2, 128, 128,
-                                kda.DTYPE_BF16, None) == -1
+                                kda.DTYPE_BF16, None, None) == -1
     # unsupported head dim
     assert lib.kda_decode_paged(*args, ctypes.c_int64(8), p, ctypes.c_void_p(8192), 2, 2, 96, 96,
-                                kda.DTYPE_BF16, None) == -2
+                                kda.DTYPE_BF16, None, None) == -2
     # nothing to do
     assert lib.kda_decode_paged(*args, ctypes.c_int64(8), None, ctypes.c_void_p(8192), 0, 2, 128, 128,
-                                kda.DTYPE_BF16, None) == 0
+                                kda.DTYPE_BF16, None, None) == 0
