@@ -217,8 +217,9 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True, graph=True)
     s0, cu = inp["init_state"], inp["cu_seqlens"]
     T, H, D, N = w.total_tokens, w.H, w.D, w.num_seqs
     n_ck = kda.num_checkpoints(w.lens, w.ckpt_stride)
+    L = max(w.lens)   # the longest sequence: bounds the segment plan and the workspace
     desc = kda.make_desc(T, H, D, N, kda.DTYPE_BF16 if w.dtype == "bf16" else kda.DTYPE_FP32, 64,
-                         w.ckpt_stride, n_ck)
+                         w.ckpt_stride, n_ck, max_seq_len=L)
     ws = kda.alloc_workspace(desc, dev)
     launches = kda.launch_count(desc)
     out = torch.empty_like(v)
@@ -228,7 +229,7 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True, graph=True)
 
     def step():
         kda.prefill(q, k, v, g, beta, s0, cu, num_seqs=N, ckpt_stride=w.ckpt_stride, ckpts=ck,
-                    ckpt_capacity=n_ck, out=out, final_state=fin, workspace=ws, stream=stream)
+                    ckpt_capacity=n_ck, out=out, final_state=fin, workspace=ws, stream=stream, max_seq_len=L)
 
     barrier(world)
     torch.cuda.synchronize()
@@ -249,7 +250,7 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True, graph=True)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
             kda.prefill(q, k, v, g, beta, s0, cu, num_seqs=N, ckpt_stride=w.ckpt_stride, ckpts=ck,
-                        ckpt_capacity=n_ck, out=out, final_state=fin, workspace=ws, stream=cap)
+                        ckpt_capacity=n_ck, out=out, final_state=fin, workspace=ws, stream=cap, max_seq_len=L)
         torch.cuda.synchronize()
         graph_ms = time_steps(graph.replay, steps, warmup, flush_buf, stream)
         assert kda.prefill_status(ws) == 0
@@ -304,7 +305,7 @@ def bench_prefill(w, steps, warmup, dev, flush_buf, world, e2e=True, graph=True)
             d = sl["in"]
             kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], sl["s0"], cu, num_seqs=N,
                         ckpt_stride=w.ckpt_stride, ckpts=ck, ckpt_capacity=n_ck, out=sl["out"],
-                        final_state=sl["fin"], workspace=ws, stream=stream)
+                        final_state=sl["fin"], workspace=ws, stream=stream, max_seq_len=L)
             sl["comp_done"].record(stream)
             d2h_stream.wait_event(sl["comp_done"])
             with torch.cuda.stream(d2h_stream):

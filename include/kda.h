@@ -103,6 +103,12 @@ typedef enum {
  *                  "一、Kimi Delta Attention（KDA）", contrasts KDA with);
  *                  the results equal those of the per-channel form with
  *                  the gate repeated over the channels.
+ *   recurrence_ctas 0 = chosen by the library.  Otherwise, when the
+ *                  tensor-core path splits the call into segments, the number
+ *                  of CTAs of each recurrence launch (each runs its share of
+ *                  the sequence x head chains one after another); the rest of
+ *                  the GPU prepares the next segment meanwhile.  A tuning knob
+ *                  only: results are bit-identical for every value.
  *   wait_limit     0 = default.  Otherwise the number of polls after which a
  *                  wait of the tensor-core kernels on an asynchronous step
  *                  (a copy, a tensor-core product, another role of the same
@@ -125,6 +131,7 @@ typedef struct {
     int64_t max_seq_len;
     int32_t segment_chunks;
     int32_t scalar_gate;
+    int32_t recurrence_ctas;
     uint32_t wait_limit;
 } kda_prefill_desc;
 

@@ -67,6 +67,7 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     if (d->ckpt_capacity < 0) return fail(KDA_ERR_INVALID_ARG, "ckpt_capacity must be >= 0");
     if (d->max_seq_len < 0) return fail(KDA_ERR_INVALID_ARG, "max_seq_len must be >= 0");
     if (d->segment_chunks < 0) return fail(KDA_ERR_INVALID_ARG, "segment_chunks must be >= 0");
+    if (d->recurrence_ctas < 0) return fail(KDA_ERR_INVALID_ARG, "recurrence_ctas must be >= 0");
     if (d->scalar_gate != 0 && d->scalar_gate != 1)
         return fail(KDA_ERR_INVALID_ARG, "scalar_gate must be 0 or 1 (got %d)", d->scalar_gate);
     const int64_t maxc = d->total_tokens / d->chunk + d->num_seqs;
@@ -79,7 +80,7 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     L.chunk_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.ckpt_off = off; off = align256(off + sizeof(int32_t) * (size_t)(d->num_seqs + 1));
     L.handoff = off;
-    L.plan = kda::SegPlan{0, 1, 1};
+    L.plan = kda::SegPlan{0, 1, 1, 0, {}};
     if (kda::use_tc_path(d->dtype, d->head_dim_k, d->chunk)) {
         L.plan = kda::tc_segment_plan(d);
         if ((int64_t)d->num_seqs * L.plan.G * d->num_heads > INT32_MAX)

@@ -72,6 +72,7 @@ struct SegPlan {
     int G;      // ring slot capacity: chunks per sequence of the longest segment
     int nseg;   // number of segments
     int R;      // ring slots
+    int k2_ctas;   // CTAs of each recurrence launch (each runs chains one after another); 0: one per chain
     int lo[kMaxSegments + 1];   // segment s: local chunks [lo[s], lo[s + 1]) of every sequence
     int begin(int s) const { return lo[s]; }
     int count(int s) const { return lo[s + 1] - lo[s]; }

@@ -783,6 +783,7 @@ __device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, c
 }
 
 
+template <bool kMulti>   // false: one chain per CTA (grid = chains); true: chains in turn
 __global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
 k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
@@ -794,34 +795,11 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
-    // This launch covers the sequence's local chunks [c_lo, c_lo + nch) of segment
-    // [seg_lo, seg_lo + G); the state enters from init_state (first segment) or
-    // the carry buffer and leaves to final_state (last segment) or the carry.
-    // G == 0: the whole sequence, records indexed by global chunk.
-    const int nch_seq = tab.chunk_off[n + 1] - tab.chunk_off[n];
-    const int c_lo = G == 0 ? 0 : seg_lo;
-    const int nch = G == 0 ? nch_seq : max(0, min(seg_lo + G, nch_seq) - seg_lo);
-    const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
-    const bool first_seg = c_lo == 0, last_seg = G == 0 || seg_lo + G >= nch_seq;
-    constexpr size_t DD = (size_t)kD * kD;
-    const size_t sbase = ((size_t)n * H + h) * DD;   // this chain's block of the carry buffer
-    // initial and final state blocks of this chain (dense arrays or pool slots)
-    const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
-    const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
-    const float *init_blk = is >= 0 ? io.init + ((size_t)is * H + h) * DD : nullptr;
-    float *fin_blk = fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD : nullptr;
-    const int stride = io.stride;
-    const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * slot_chunks;
-    if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
-        if (first_seg && nch_seq == 0 && fin_blk)
-            for (int i = tid; i < kD * kD; i += blockDim.x)
-                fin_blk[i] = init_blk ? init_blk[i] : 0.f;
-        return;
-    }
-    // record of the sequence's chunk c_lo + i
-    auto rec_at = [&](int i) { return ring + ((rec_base + i) * H + h) * REC_BYTES; };
-
+    // A CTA runs the chains (sequence n, head h) = blockIdx.x, blockIdx.x +
+    // gridDim.x, ... one after another (one chain per CTA when the grid covers
+    // them all; fewer, longer-lived CTAs leave the other SMs to K1).  Barrier
+    // phases and ring positions follow one chunk count that runs on across the
+    // CTA's chains: the chain's local chunk c is chunk base + c of the CTA.
     if (tid == 0) {
         for (int s = 0; s < K2_STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -848,171 +826,221 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
     const int q4 = warp & 3, qd = warp >> 2;
     const int e = 32 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    // Lane 0 of the last warp drives the record copies and the MMAs.
+    // Lane 0 of the last warp drives the record copies and the MMAs; the other
+    // lanes of that warp have no part.
     const bool issuer = tid == K2_STATE_THREADS;
-    int copied = 0;
-    auto issue_copy = [&](int c) {   // record c -> stage c % K2_STAGES, once that stage is free
-        const int s = c % K2_STAGES;
-        // the operand tiles into the stage (free again as soon as the MMA has
-        // read it), gamma into its own slot with its own barrier (the state
-        // threads read it later)
-        mbar_arrive_expect_tx(&full[s], REC_G);
-        bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_G, &full[s]);
-        mbar_arrive_expect_tx(&gfull[c % kGamSlots], 512);
-        bulk_g2s(sm + K2_GAM + (c % kGamSlots) * 512, rec_at(c) + REC_G, 512, &gfull[c % kGamSlots]);
-        copied = c + 1;
-    };
-    // chunk c: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T, in
-    // TMEM buffer c & 1 (N = 192 rows of B: d, then r).  The K = r steps
-    // (A = Uv^T) do not involve the state: they are issued as soon as the
-    // record has landed and the buffer's previous contents (chunk c - 2) were
-    // read, so they run while the state threads still work on chunk c - 1; the
-    // K = d' steps (A = S^T) follow half by half as the state threads write S^T.
-    auto issue_rpart = [&](int c) -> bool {
-        const int s = c % K2_STAGES;
-        const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
-        const uint32_t idesc = idesc_f16(128, 192);
-        bool okw = wait_or_abort(&full[s], (c / K2_STAGES) & 1, abort_v, wait_limit);
-        okw = okw && (c < 2 || wait_or_abort(&pread[c & 1], ((c >> 1) - 1) & 1, abort_v, wait_limit));
-        if (!okw) return false;
-        fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_f16(acc, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
-                    make_desc(stg + REC_KM + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
-        return true;
-    };
-    auto issue_dpart = [&](int c) -> bool {
-        const int s = c % K2_STAGES;
-        const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (c & 1);
-        const uint32_t sop = smem_u32(sm + K2_SOP);
-        const uint32_t idesc = idesc_f16(128, 192);
-        if (!wait_or_abort(&sready[0], c & 1, abort_v, wait_limit)) return false;
-        fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                    make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
-        if (!wait_or_abort(&sready[1], c & 1, abort_v, wait_limit)) return false;
-        fence_after_sync();
-#pragma unroll
-        for (int ks = 4; ks < 8; ++ks)
-            mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                    make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
-        mma_commit(&sdone);
-        mma_commit(&empty[s]);
-        return true;
-    };
-
+    const bool state_thread = tid < K2_STATE_THREADS;
+    constexpr size_t DD = (size_t)kD * kD;
+    const int stride = io.stride;
+    int copied = 0;          // (issuer) chunks whose record copies were issued, CTA count
+    int base_run = 0;        // chunks of this CTA's earlier chains
     bool alive = true;
-    if (warp == K2_STATE_WARPS) {
-        // ---------------------------------------------------------- issuer
+
+    for (int chain = blockIdx.x; chain < N * H && alive && (issuer || state_thread); chain += gridDim.x) {
+        const int base = kMulti ? base_run : 0;
+        const int n = chain / H, h = chain % H;
+        // This launch covers the sequence's local chunks [c_lo, c_lo + nch) of
+        // segment [seg_lo, seg_lo + G); the state enters from the initial state
+        // (first segment) or the carry buffer and leaves to the final state
+        // (last segment) or the carry.  G == 0: the whole sequence, records
+        // indexed by global chunk.
+        const int nch_seq = tab.chunk_off[n + 1] - tab.chunk_off[n];
+        const int c_lo = G == 0 ? 0 : seg_lo;
+        const int nch = G == 0 ? nch_seq : max(0, min(seg_lo + G, nch_seq) - seg_lo);
+        const int seq_t0 = tab.cu[n], seq_t1 = tab.cu[n + 1];
+        const bool first_seg = c_lo == 0, last_seg = G == 0 || seg_lo + G >= nch_seq;
+        const size_t sbase = ((size_t)n * H + h) * DD;   // this chain's block of the carry buffer
+        // initial and final state blocks of this chain (dense arrays or pool
+        // slots), looked up where they are used so that nothing of them stays
+        // live across the chunk loop
+        auto init_block = [&]() -> const float * {
+            const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
+            return is >= 0 ? io.init + ((size_t)is * H + h) * DD : nullptr;
+        };
+        auto final_block = [&]() -> float * {
+            const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
+            return fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD : nullptr;
+        };
+        const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * slot_chunks;
+        if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
+            if (state_thread && first_seg && nch_seq == 0)
+                if (float *fin_blk = final_block()) {
+                    const float *init_blk = init_block();
+                    for (int i = tid; i < kD * kD; i += K2_STATE_THREADS) fin_blk[i] = init_blk ? init_blk[i] : 0.f;
+                }
+            continue;
+        }
+        // record of the sequence's chunk c_lo + i
+        auto rec_at = [&](int i) { return ring + ((rec_base + i) * H + h) * REC_BYTES; };
+
         if (issuer) {
-            for (int c = 0; c < min(nch, K2_STAGES); ++c) issue_copy(c);
-            alive = issue_rpart(0);
+            // record of local chunk c -> stage cc % K2_STAGES (cc = base + c),
+            // once the product of chunk cc - K2_STAGES has read that stage
+            auto issue_copy = [&](int c) -> bool {
+                const int cc = base + c, s = cc % K2_STAGES;
+                if (cc >= K2_STAGES && !wait_or_abort(&empty[s], ((cc - K2_STAGES) / K2_STAGES) & 1, abort_v, wait_limit))
+                    return false;
+                // the operand tiles into the stage (free again as soon as the MMA
+                // has read it), gamma into its own slot with its own barrier (the
+                // state threads read it later); the record two chunks further on
+                // is brought towards L2 meanwhile
+                mbar_arrive_expect_tx(&full[s], REC_G);
+                bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_G, &full[s]);
+                mbar_arrive_expect_tx(&gfull[cc % kGamSlots], 512);
+                bulk_g2s(sm + K2_GAM + (cc % kGamSlots) * 512, rec_at(c) + REC_G, 512, &gfull[cc % kGamSlots]);
+                if (kMulti && c + K2_STAGES < nch) prefetch_l2(rec_at(c + K2_STAGES), REC_BYTES);
+                copied = cc + 1;
+                return true;
+            };
+            // chunk cc: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T,
+            // in TMEM buffer cc & 1 (N = 192 rows of B: d, then r).  The K = r
+            // steps (A = Uv^T) do not involve the state: they are issued as soon
+            // as the record has landed and the buffer's previous contents (chunk
+            // cc - 2) were read, so they run while the state threads still work
+            // on chunk cc - 1; the K = d' steps (A = S^T) follow half by half as
+            // the state threads write S^T.
+            auto issue_rpart = [&](int cc) -> bool {
+                const int s = cc % K2_STAGES;
+                const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
+                const uint32_t idesc = idesc_f16(128, 192);
+                bool okw = wait_or_abort(&full[s], (cc / K2_STAGES) & 1, abort_v, wait_limit);
+                okw = okw && (cc < 2 || wait_or_abort(&pread[cc & 1], ((cc >> 1) - 1) & 1, abort_v, wait_limit));
+                if (!okw) return false;
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
+                            make_desc(stg + REC_KM + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
+                return true;
+            };
+            auto issue_dpart = [&](int cc) -> bool {
+                const int s = cc % K2_STAGES;
+                const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
+                const uint32_t sop = smem_u32(sm + K2_SOP);
+                const uint32_t idesc = idesc_f16(128, 192);
+                if (!wait_or_abort(&sready[0], cc & 1, abort_v, wait_limit)) return false;
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+                if (!wait_or_abort(&sready[1], cc & 1, abort_v, wait_limit)) return false;
+                fence_after_sync();
+#pragma unroll
+                for (int ks = 4; ks < 8; ++ks)
+                    mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
+                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+                mma_commit(&sdone);
+                mma_commit(&empty[s]);
+                return true;
+            };
+            // ---------------------------------------------------------- issuer
+            for (int c = 0; c < min(nch, K2_STAGES) && alive; ++c) alive = issue_copy(c);
+            alive = alive && issue_rpart(base);
             for (int c = 0; c < nch && alive; ++c) {
                 // chunk c's state-dependent steps; then record c + 2 into the
                 // stage chunk c used, once its product is complete; then the
                 // state-independent steps of chunk c + 1
-                if (!issue_dpart(c)) { alive = false; break; }
-                if (c + K2_STAGES < nch) {
-                    if (!wait_or_abort(&empty[c % K2_STAGES], (c / K2_STAGES) & 1, abort_v, wait_limit)) { alive = false; break; }
-                    issue_copy(c + K2_STAGES);
-                }
-                if (c + 1 < nch && !issue_rpart(c + 1)) { alive = false; break; }
+                if (!issue_dpart(base + c)) { alive = false; break; }
+                if (c + K2_STAGES < nch && !issue_copy(c + K2_STAGES)) { alive = false; break; }
+                if (c + 1 < nch && !issue_rpart(base + c + 1)) { alive = false; break; }
             }
-        }
-    } else {
-        // ---------------------------------------------------------- state
-        float S[32];
-        const float *src_state = first_seg ? init_blk : carry + sbase;
+        } else {
+            // ---------------------------------------------------------- state
+            float S[32];
+            const float *src_state = first_seg ? init_block() : carry + sbase;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            S[j] = src_state ? src_state[(size_t)(32 * qd + j) * kD + e] : 0.f;
-        write_sop_quarter(sm + K2_SOP, e, qd, S);
-        fence_async_smem();
-        mbar_arrive(&sready[qd >> 1]);
-        for (int c = 0; c < nch && alive; ++c) {
-            // gamma has landed (its slot's barrier cannot run ahead: slot c % 4 is
-            // refilled only after the product of chunk c + 2, which needs this
-            // thread's S^T of chunk c + 1) and the chunk's product is in TMEM
-            if (!wait_or_abort(&gfull[c % kGamSlots], (c / kGamSlots) & 1, abort_v, wait_limit) ||
-                !wait_or_abort(&sdone, c & 1, abort_v, wait_limit)) {
-                alive = false;
-                break;
-            }
-            fence_after_sync();
-            // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16 now and
-            // stored after the state is handed on; then S = gamma * S + P over this
-            // thread's 32 rows d
-            uint32_t ob16[8];
-            {
-                float o[16];
-                tmem_ld16(tm + lane_base + T2_O + 256 * (c & 1) + 16 * qd, o);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-                    ob16[j] = *reinterpret_cast<const uint32_t *>(&v2);
-                }
-            }
-            {
-                const float *gam = reinterpret_cast<const float *>(sm + K2_GAM + (c % kGamSlots) * 512) + 32 * qd;
-#pragma unroll
-                for (int h16 = 0; h16 < 32; h16 += 16) {
-                    float p[16];
-                    tmem_ld16(tm + lane_base + T2_P + 256 * (c & 1) + 32 * qd + h16, p);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j4 = 0; j4 < 16; j4 += 4) {
-                        const int j = h16 + j4;
-                        const float4 g4 = *reinterpret_cast<const float4 *>(gam + j);
-                        const float2 s01 = __ffma2_rn(make_float2(g4.x, g4.y), make_float2(S[j], S[j + 1]),
-                                                      make_float2(p[j4], p[j4 + 1]));
-                        const float2 s23 = __ffma2_rn(make_float2(g4.z, g4.w), make_float2(S[j + 2], S[j + 3]),
-                                                      make_float2(p[j4 + 2], p[j4 + 3]));
-                        S[j] = s01.x; S[j + 1] = s01.y; S[j + 2] = s23.x; S[j + 3] = s23.y;
-                    }
-                }
-            }
-            fence_before_sync();
-            mbar_arrive(&pread[c & 1]);
+            for (int j = 0; j < 32; ++j)
+                S[j] = src_state ? src_state[(size_t)(32 * qd + j) * kD + e] : 0.f;
             write_sop_quarter(sm + K2_SOP, e, qd, S);
             fence_async_smem();
             mbar_arrive(&sready[qd >> 1]);
+            for (int c = 0; c < nch && alive; ++c) {
+                const int cc = base + c;
+                // gamma has landed (its slot's barrier cannot run ahead: slot cc % 4
+                // is refilled only after the product of chunk cc + 2, which needs
+                // this thread's S^T of chunk cc + 1) and the chunk's product is in TMEM
+                if (!wait_or_abort(&gfull[cc % kGamSlots], (cc / kGamSlots) & 1, abort_v, wait_limit) ||
+                    !wait_or_abort(&sdone, cc & 1, abort_v, wait_limit)) {
+                    alive = false;
+                    break;
+                }
+                fence_after_sync();
+                // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16 now and
+                // stored after the state is handed on; then S = gamma * S + P over this
+                // thread's 32 rows d
+                uint32_t ob16[8];
+                {
+                    float o[16];
+                    tmem_ld16(tm + lane_base + T2_O + 256 * (cc & 1) + 16 * qd, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+                        ob16[j] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                }
+                {
+                    const float *gam = reinterpret_cast<const float *>(sm + K2_GAM + (cc % kGamSlots) * 512) + 32 * qd;
+#pragma unroll
+                    for (int h16 = 0; h16 < 32; h16 += 16) {
+                        float p[16];
+                        tmem_ld16(tm + lane_base + T2_P + 256 * (cc & 1) + 32 * qd + h16, p);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j4 = 0; j4 < 16; j4 += 4) {
+                            const int j = h16 + j4;
+                            const float4 g4 = *reinterpret_cast<const float4 *>(gam + j);
+                            const float2 s01 = __ffma2_rn(make_float2(g4.x, g4.y), make_float2(S[j], S[j + 1]),
+                                                          make_float2(p[j4], p[j4 + 1]));
+                            const float2 s23 = __ffma2_rn(make_float2(g4.z, g4.w), make_float2(S[j + 2], S[j + 3]),
+                                                          make_float2(p[j4 + 2], p[j4 + 3]));
+                            S[j] = s01.x; S[j + 1] = s01.y; S[j + 2] = s23.x; S[j + 3] = s23.y;
+                        }
+                    }
+                }
+                fence_before_sync();
+                mbar_arrive(&pread[cc & 1]);
+                if (c + 1 < nch) {   // the next chunk's S^T (none after the chain's last chunk)
+                    write_sop_quarter(sm + K2_SOP, e, qd, S);
+                    fence_async_smem();
+                    mbar_arrive(&sready[qd >> 1]);
+                }
 
-            // this chunk's output, while the next state product runs: straight from
-            // registers (shared memory is busy feeding that product), each warp
-            // store covering 64 contiguous bytes of one row
-            const int t0 = seq_t0 + (c_lo + c) * kC;
-            const int L = min(kC, seq_t1 - t0);
-            {
-                unsigned short *orow = reinterpret_cast<unsigned short *>(out) + ((size_t)(t0 + 16 * qd) * H + h) * kD + e;
-                const size_t rs = (size_t)H * kD;
+                // this chunk's output, while the next state product runs: straight from
+                // registers (shared memory is busy feeding that product), each warp
+                // store covering 64 contiguous bytes of one row
+                const int t0 = seq_t0 + (c_lo + c) * kC;
+                const int L = min(kC, seq_t1 - t0);
+                {
+                    unsigned short *orow = reinterpret_cast<unsigned short *>(out) + ((size_t)(t0 + 16 * qd) * H + h) * kD + e;
+                    const size_t rs = (size_t)H * kD;
 #pragma unroll
-                for (int rl2 = 0; rl2 < 8; ++rl2) {
-                    if (16 * qd + 2 * rl2 < L) orow[(size_t)(2 * rl2) * rs] = (unsigned short)(ob16[rl2] & 0xFFFFu);
-                    if (16 * qd + 2 * rl2 + 1 < L) orow[(size_t)(2 * rl2 + 1) * rs] = (unsigned short)(ob16[rl2] >> 16);
+                    for (int rl2 = 0; rl2 < 8; ++rl2) {
+                        if (16 * qd + 2 * rl2 < L) orow[(size_t)(2 * rl2) * rs] = (unsigned short)(ob16[rl2] & 0xFFFFu);
+                        if (16 * qd + 2 * rl2 + 1 < L) orow[(size_t)(2 * rl2 + 1) * rs] = (unsigned short)(ob16[rl2] >> 16);
+                    }
+                }
+                // checkpoint after every `stride` tokens of the sequence
+                const int done = (c_lo + c) * kC + L;
+                if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
+                    const int64_t jc = (int64_t)tab.ckpt_off[n] + done / stride - 1;
+                    const int64_t ps = jc < io.capacity ? pool_slot(io.ckpt_slots, jc, io.pool) : -1;
+                    if (ps >= 0) {
+                        float *dst = io.ckpts + ((size_t)ps * H + h) * DD + e;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) dst[(size_t)(32 * qd + j) * kD] = S[j];
+                    }
                 }
             }
-            // (output of this chunk done)
-            // checkpoint after every `stride` tokens of the sequence
-            const int done = (c_lo + c) * kC + L;
-            if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
-                const int64_t j = (int64_t)tab.ckpt_off[n] + done / stride - 1;
-                const int64_t ps = j < io.capacity ? pool_slot(io.ckpt_slots, j, io.pool) : -1;
-                if (ps >= 0) {
-                    float *dst = io.ckpts + ((size_t)ps * H + h) * DD + e;
+            if (alive)
+                if (float *dst_state = last_seg ? final_block() : carry + sbase) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) dst[(size_t)(32 * qd + j) * kD] = S[j];
+                    for (int j = 0; j < 32; ++j) dst_state[(size_t)(32 * qd + j) * kD + e] = S[j];
                 }
-            }
         }
-        if (alive)
-            if (float *dst_state = last_seg ? fin_blk : carry + sbase) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dst_state[(size_t)(32 * qd + j) * kD + e] = S[j];
-            }
+        base_run += nch;
+        if (!kMulti) break;
     }
     if (!alive) {
         *abort_v = 1;
@@ -1066,6 +1094,14 @@ int64_t device_sm_count()
 
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
+    // Many chains (sequences x heads): the recurrence alone would fill the GPU,
+    // so it runs on a small persistent grid (kK2Share of the SMs, each CTA
+    // taking chains one after another) while the preparation of the next
+    // segment takes the other SMs.  Segments are uniform, kManyG chunks per
+    // sequence (more where needed to stay within 64 segments), which bounds the
+    // workspace to two ring slots of that many chunks of every chain.
+    constexpr int64_t kManyG = 32, kManySegments = 64;
+    constexpr double kK2Share = 0.26;
     // Automatic choice: overlap only when the recurrence (one CTA per chain and
     // SM) leaves most of the 152 SMs idle.  Segment lengths are whole K1 waves
     // (two K1 CTAs per SM; a wave covers 2 x SMs / chains chunks of every
@@ -1082,15 +1118,26 @@ SegPlan tc_segment_plan(const kda_prefill_desc *d)
     const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
     const int64_t maxc = (len + d->chunk - 1) / d->chunk;
     const int64_t chains = (int64_t)d->num_seqs * d->num_heads;
-    SegPlan p{0, 1, 1, {}};
+    SegPlan p{0, 1, 1, 0, {}};
+    const int64_t k2_many = std::max<int64_t>(1, std::llround(kK2Share * (double)kSMs));
     auto finish = [&]() {
         p.G = 0;
         for (int s = 0; s < p.nseg; ++s) p.G = std::max(p.G, p.count(s));
         p.R = std::min(2, p.nseg);
+        p.k2_ctas = 0;
+        if (p.nseg > 1 && d->recurrence_ctas > 0) p.k2_ctas = (int)std::min<int64_t>(chains, d->recurrence_ctas);
+        else if (p.nseg > 1 && chains > kMaxChains) p.k2_ctas = (int)std::min(chains, k2_many);
         return p;
     };
+    if (d->segment_chunks == 0 && chains > kMaxChains) {
+        const int64_t G = std::max(kManyG, (maxc + kManySegments - 1) / kManySegments);
+        if (G >= maxc) return p;
+        p.nseg = (int)((maxc + G - 1) / G);
+        for (int s = 0; s <= p.nseg; ++s) p.lo[s] = (int)(s * G);
+        return finish();
+    }
     if (d->segment_chunks == 0) {
-        if (chains > kMaxChains || chains <= 0) return p;
+        if (chains <= 0) return p;
         const double wave_all = 2.0 * kSMs / chains, wave = 2.0 * (kSMs - chains) / chains;
         const int64_t first = std::max<int64_t>(kMinG, std::llround(4 * wave_all));
         if (first >= maxc) return p;
@@ -1184,7 +1231,9 @@ cudaError_t tc_kernel_attributes()
     if (!bit || !(attr_done.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
+        e = cudaFuncSetAttribute(k2_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k2_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit, std::memory_order_release);
     }
@@ -1307,9 +1356,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
                 return e;
             }
         }
-        k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
+        k2_tc_kernel<false><<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
             state_io(a), a.N, a.H, a.tab, ring, 0, 0, 0, 0, nullptr, (bf16 *)a.out, a.status, a.wait_limit);
-        if ((e = cudaGetLastError()) != cudaSuccess) note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            note_launch_failure(k2_tc_kernel<false>, "K2", K2_THREADS, K2_SMEM);
         return e;
     }
 
@@ -1332,11 +1382,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         }
         if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(c->side, c->k1[slot], 0)) != cudaSuccess) break;
-        k2_tc_kernel<<<chains, K2_THREADS, K2_SMEM, c->side>>>(
-            state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
-            a.wait_limit);
+        if (p.k2_ctas > 0)
+            k2_tc_kernel<true><<<(unsigned)p.k2_ctas, K2_THREADS, K2_SMEM, c->side>>>(
+                state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
+                a.wait_limit);
+        else
+            k2_tc_kernel<false><<<chains, K2_THREADS, K2_SMEM, c->side>>>(
+                state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
+                a.wait_limit);
         if ((e = cudaGetLastError()) != cudaSuccess) {
-            note_launch_failure(k2_tc_kernel, "K2", K2_THREADS, K2_SMEM);
+            note_launch_failure(k2_tc_kernel<false>, "K2", K2_THREADS, K2_SMEM);
             break;
         }
         e = cudaEventRecord(c->k2[slot], c->side);

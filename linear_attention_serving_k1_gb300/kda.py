@@ -42,7 +42,7 @@ class PrefillDesc(ctypes.Structure):
                 ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
                 ("ckpt_capacity", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
                 ("segment_chunks", ctypes.c_int32), ("scalar_gate", ctypes.c_int32),
-                ("wait_limit", ctypes.c_uint32)]
+                ("recurrence_ctas", ctypes.c_int32), ("wait_limit", ctypes.c_uint32)]
 
 
 _lib = None
@@ -117,9 +117,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
               ckpt_stride: int = 0, ckpt_capacity: int = 0, max_seq_len: int = 0,
-              segment_chunks: int = 0, scalar_gate: bool = False, wait_limit: int = 0) -> PrefillDesc:
+              segment_chunks: int = 0, scalar_gate: bool = False, wait_limit: int = 0,
+              recurrence_ctas: int = 0) -> PrefillDesc:
     return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity,
-                       max_seq_len, segment_chunks, int(bool(scalar_gate)), wait_limit)
+                       max_seq_len, segment_chunks, int(bool(scalar_gate)), recurrence_ctas, wait_limit)
 
 
 def workspace_size(desc: PrefillDesc) -> int:
@@ -148,7 +149,7 @@ def num_checkpoints(lens, ckpt_stride: int) -> int:
 def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Optional[int] = None,
             chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None,
             out=None, final_state=None, workspace=None, stream=None, want_final: bool = True,
-            max_seq_len: int = 0, segment_chunks: int = 0, wait_limit: int = 0):
+            max_seq_len: int = 0, segment_chunks: int = 0, wait_limit: int = 0, recurrence_ctas: int = 0):
     """Chunked KDA prefill through ``kda_prefill``.
 
     q, k: [T, H, D]; v: [T, H, D]; g: [T, H, D] (a decay per key channel) or
@@ -170,7 +171,7 @@ def prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs: Opt
         ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
     cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
     desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
-                     scalar_gate=g.dim() == 2, wait_limit=wait_limit)
+                     scalar_gate=g.dim() == 2, wait_limit=wait_limit, recurrence_ctas=recurrence_ctas)
     if workspace is None:
         workspace = alloc_workspace(desc, dev)
     code = load_library().kda_prefill(

@@ -101,3 +101,27 @@ def test_segmented_prefill_in_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(out, o_ref)
     assert torch.equal(fin, f_ref)
+
+
+def test_many_chains_persistent_recurrence():
+    """More chains (sequences x heads) than the one-CTA-per-chain plan takes:
+    with segments, the recurrence runs on a small grid whose CTAs take chains
+    one after another (barrier phases and ring positions carried across
+    chains).  Every segment length gives the same bytes as one segment, and
+    the oracle agrees."""
+    lens = [1, 700, 0, 64, 65, 300, 130, 1000]
+    w = workloads.custom_prefill(H=16, D=128, lens=lens, dtype="bf16", init="randn", ckpt_stride=64,
+                                 seed=35, varlen=True)
+    inp = workloads.make_prefill(w)
+    d = gpu_inputs(inp)
+    assert w.num_seqs * w.H > 96
+    o0, f0, c0 = _run(d, w, ckpt_stride=64, segment_chunks=1 << 20)
+    for G in (1, 2, 3, 5):
+        o, f, c = _run(d, w, ckpt_stride=64, segment_chunks=G, max_seq_len=max(lens))
+        assert torch.equal(o, o0), f"outputs differ at segment_chunks={G}"
+        assert torch.equal(f, f0), f"final states differ at segment_chunks={G}"
+        assert torch.equal(c, c0), f"checkpoints differ at segment_chunks={G}"
+    o_r, f_r, c_r = run_oracle_prefill(inp, ckpt_stride=64)
+    assert out_err(to_np(o0), o_r) <= TOL_OUT_BF16
+    assert state_err(to_np(f0), f_r) <= TOL_STATE
+    assert state_err(to_np(c0), c_r) <= TOL_STATE
