@@ -32,6 +32,7 @@
 // tensor-core shared-memory layout (no-swizzle K-major core matrices), moved
 // into K2's shared memory by one bulk TMA copy, and gamma.
 #include <atomic>
+#include <type_traits>
 #include "kda_common.cuh"
 #include <algorithm>
 
@@ -229,6 +230,17 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     auto load_half = [&](int p) {
         int d = 64 * p + 2 * lane;
         asm volatile("" : "+r"(d));   // keeps the second half's loads after its barrier (registers)
+        if (L == kC && !scalar_gate) {   // a full chunk with a per-channel gate: no row predicates
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const size_t o = (size_t)(rb + j) * rstride + d;
+                gv[j] = __ldg(reinterpret_cast<const float2 *>(grow + o));
+                qv[j] = __ldg(reinterpret_cast<const unsigned int *>(qrow + o));
+                kv[j] = __ldg(reinterpret_cast<const unsigned int *>(krow + o));
+                vv[j] = __ldg(reinterpret_cast<const unsigned int *>(vrow + o));
+            }
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int r = rb + j;
@@ -318,6 +330,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         float sq[8];
         const bool up16 = lane & 16;
         // the two channels of a thread as packed fp32 pairs
+        // With g <= 0 each channel's b runs from 0 down to b_last, so |b - B| <=
+        // |B|: while |B| <= kMaxDecayExp for every channel of the half (the
+        // same channels in every warp), no factor can leave the range and the
+        // clamps are skipped (a warp-uniform choice).
+        const bool clamp = __any_sync(0xffffffffu, fabsf(ref.x) > kMaxDecayExp || fabsf(ref.y) > kMaxDecayExp);
+        auto build_rows = [&](auto kClamp) {
         float2 bb = make_float2(pre0, pre1);
 #pragma unroll
         for (int j2 = 0; j2 < 8; j2 += 2) {
@@ -327,9 +345,15 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 const int j = j2 + u, r = rb + j;
                 bb = __fadd2_rn(bb, gv[j]);
                 const float2 x = __fadd2_rn(bb, make_float2(-ref.x, -ref.y));
-                strong |= fabsf(x.x) > kMaxDecayExp || fabsf(x.y) > kMaxDecayExp;
-                const float2 e = make_float2(__expf(fminf(x.x, kMaxDecayExp)), __expf(fminf(x.y, kMaxDecayExp)));
-                const float2 ei = make_float2(__expf(fminf(-x.x, kMaxDecayExp)), __expf(fminf(-x.y, kMaxDecayExp)));
+                float2 e, ei;
+                if constexpr (decltype(kClamp)::value) {
+                    strong |= fabsf(x.x) > kMaxDecayExp || fabsf(x.y) > kMaxDecayExp;
+                    e = make_float2(__expf(fminf(x.x, kMaxDecayExp)), __expf(fminf(x.y, kMaxDecayExp)));
+                    ei = make_float2(__expf(fminf(-x.x, kMaxDecayExp)), __expf(fminf(-x.y, kMaxDecayExp)));
+                } else {
+                    e = make_float2(__expf(x.x), __expf(x.y));
+                    ei = make_float2(__expf(-x.x), __expf(-x.y));
+                }
                 const float2 qq = make_float2(bf_lo(qv[j]), bf_hi(qv[j])), kk = make_float2(bf_lo(kv[j]), bf_hi(kv[j]));
                 const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
                 const float2 s2 = __ffma2_rn(qk1, qk1, __fmul2_rn(qk0, qk0));
@@ -359,6 +383,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             ke0[j2 / 2] = pack_f16x2(kex[0][0], kex[0][1]);
             ke1[j2 / 2] = pack_f16x2(kex[1][0], kex[1][1]);
         }
+        };
+        if (clamp) build_rows(std::true_type{});
+        else build_rows(std::false_type{});
         // f16 operand rows d and d + 1, K = rows rb .. rb + 7.  Lanes 4-7 of each
         // quarter-warp store row d + 1 first, so that every store instruction
         // covers eight distinct rows modulo 8 (conflict-free).

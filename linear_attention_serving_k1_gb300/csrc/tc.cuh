@@ -210,12 +210,13 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// Rounds an fp32 value to the nearest tf32 (10-bit mantissa), as a float.
+// Rounds a finite fp32 value to the nearest tf32 (10 explicit mantissa bits,
+// ties away from zero) on its bit pattern: half a tf32 unit is added to the
+// magnitude bits and the 13 bits below the tf32 mantissa are cleared (a carry
+// into the exponent gives the next binade, as rounding should).
 __device__ __forceinline__ float round_tf32(float x)
 {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 // Arrives once on `bar` when every MMA this thread issued before has completed.
