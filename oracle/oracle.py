@@ -187,6 +187,66 @@ def gdn_prefill(q, k, v, a, beta, init_state=None, cu_seqlens=None, lib=None):
     return out, fin
 
 
+def short_conv(x, w, cu_seqlens=None, silu=False):
+    """Causal depthwise short convolution along time, inside each sequence.
+
+    x: [T, H, D]; w: [W, H, D] taps; cu_seqlens: [N + 1] token offsets (None:
+    one sequence).  For token t of a sequence starting at s:
+        y[t] = sum_{i < W} w[i] * x[t - (W - 1) + i],   x[tau] = 0 for tau < s
+    (tap W - 1 multiplies the current token; nothing crosses a sequence start),
+    then y * sigmoid(y) when ``silu``.  float64 throughout.
+
+    Source: "Kimi K3 reconstructs long-context inference efficiency through
+    KDA, cross-depth attention, and latent expert routing", section
+    "Methodology notes", item "Memory control: Kimi Delta Attention" (KDA
+    combines a short convolution with the L2-normalised q/k and an output
+    forget gate); width, causality and activation are readings, the pages
+    give none.
+    """
+    x = _f64(x)
+    w = _f64(w)
+    T = x.shape[0]
+    W = w.shape[0]
+    cu = _cu(cu_seqlens, T)
+    y = np.zeros_like(x)
+    for n in range(cu.shape[0] - 1):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for t in range(s, e):
+            for i in range(W):
+                tau = t - (W - 1) + i
+                if tau >= s:
+                    y[t] += w[i] * x[tau]
+    if silu:
+        y = y / (1.0 + np.exp(-y))
+    return y
+
+
+def output_gate(o, z):
+    """The output forget gate read as an elementwise sigmoid gate:
+    out = o * sigmoid(z) (same shapes; float64).  Source: the page named in
+    ``short_conv``, same item; the gate's form is a reading."""
+    o = _f64(o)
+    z = _f64(z)
+    return o / (1.0 + np.exp(-z))
+
+
+def prefill_fused(q, k, v, g, beta, init_state=None, cu_seqlens=None, ckpt_stride=0, conv_w=None,
+                  silu=False, gate=None, lib=None):
+    """The prefill with the steps around the recurrence: q, k, v pass through
+    ``short_conv`` (taps conv_w [3, W, H, D] for q, k, v; None: none) before
+    the recurrence, and its output through ``output_gate`` (gate [T, H, Dv];
+    None: none).  Returns (out, final_state, ckpts) like ``prefill``."""
+    if conv_w is not None:
+        conv_w = _f64(conv_w)
+        q = short_conv(q, conv_w[0], cu_seqlens, silu)
+        k = short_conv(k, conv_w[1], cu_seqlens, silu)
+        v = short_conv(v, conv_w[2], cu_seqlens, silu)
+    o, f, ck = prefill(q, k, v, g, beta, init_state, cu_seqlens, ckpt_stride, lib=lib)
+    if gate is not None:
+        o = output_gate(o, gate)
+    return o, f, ck
+
+
 def num_threads(lib=None) -> int:
     lib = lib or load()
     return int(lib.oracle_num_threads())

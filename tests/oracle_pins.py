@@ -341,6 +341,84 @@ def pin_decode_heads_match_prefill_T1(lib=None, seed=17):
     return worst
 
 
+# ---------------------------------------------------------------- prologue / epilogue
+# The short convolution and the output gate (page "Kimi K3 reconstructs ...",
+# section "Methodology notes", item "Memory control: Kimi Delta Attention").
+def pin_conv_identity_tap(lib=None, seed=18):
+    """Taps (0, .., 0, 1) without activation pass the inputs through unchanged,
+    and the fused prefill then equals the plain one exactly."""
+    rng = _rng(seed)
+    T, H, D = 23, 2, 6
+    q, k, v, g, b = _inputs(rng, T, H, D, D)
+    cu = np.array([0, 9, 9, 23])
+    w = np.zeros((3, 4, H, D))
+    w[:, 3] = 1.0
+    worst = np.abs(oracle.short_conv(q, w[0], cu) - q).max()
+    o1, f1, _ = oracle.prefill_fused(q, k, v, g, b, None, cu, conv_w=w, lib=lib)
+    o2, f2, _ = oracle.prefill(q, k, v, g, b, None, cu, lib=lib)
+    return max(worst, np.abs(o1 - o2).max(), np.abs(f1 - f2).max())
+
+
+def pin_conv_matches_library(lib=None, seed=19):
+    """Per sequence and channel, the causal convolution is numpy's full
+    convolution with the reversed taps, cut to the sequence length."""
+    rng = _rng(seed)
+    T, H, D, W = 30, 2, 3, 4
+    x = rng.standard_normal((T, H, D))
+    w = rng.standard_normal((W, H, D))
+    cu = np.array([0, 2, 17, 30])
+    y = oracle.short_conv(x, w, cu)
+    worst = 0.0
+    for n in range(3):
+        s, e = cu[n], cu[n + 1]
+        for h in range(H):
+            for d in range(D):
+                ref = np.convolve(x[s:e, h, d], w[::-1, h, d], mode="full")[: e - s]
+                worst = max(worst, np.abs(y[s:e, h, d] - ref).max())
+    return worst
+
+
+def pin_conv_stays_in_sequence(lib=None, seed=20):
+    """An impulse at the last token of one sequence leaves the next sequence
+    at zero, and one at a sequence's first token touches nothing before it."""
+    rng = _rng(seed)
+    T, H, D, W = 12, 1, 2, 4
+    w = rng.standard_normal((W, H, D))
+    cu = np.array([0, 5, 12])
+    worst = 0.0
+    for pos, zero in ((4, slice(5, 12)), (5, slice(0, 5))):
+        x = np.zeros((T, H, D))
+        x[pos] = 1.0
+        y = oracle.short_conv(x, w, cu)
+        worst = max(worst, np.abs(y[zero]).max())
+        # and inside its own sequence the impulse response is the taps, newest first
+        s_end = 5 if pos < 5 else 12
+        for j in range(min(W, s_end - pos)):
+            worst = max(worst, np.abs(y[pos + j] - w[W - 1 - j]).max())
+    return worst
+
+
+def pin_silu_closed_form(lib=None, seed=21):
+    """With pass-through taps, the activation is x sigmoid(x): 0 at 0,
+    (3/4) ln 3 at ln 3 and -(1/4) ln 3 at -ln 3 (sigmoid(ln 3) = 3/4)."""
+    l3 = np.log(3.0)
+    x = np.array([0.0, l3, -l3]).reshape(3, 1, 1)
+    w = np.ones((1, 1, 1))
+    y = oracle.short_conv(x, w, None, silu=True).ravel()
+    return np.abs(y - np.array([0.0, 0.75 * l3, -0.25 * l3])).max()
+
+
+def pin_output_gate_values(lib=None, seed=22):
+    """sigmoid(0) = 1/2, sigmoid(+-ln 3) = 3/4, 1/4 and sigmoid(60) = 1 to
+    double precision: the gate halves, scales by 3/4 and 1/4, or passes o."""
+    rng = _rng(seed)
+    o = rng.standard_normal((4, 2, 3))
+    l3 = np.log(3.0)
+    z = np.broadcast_to(np.array([0.0, l3, -l3, 60.0]).reshape(4, 1, 1), o.shape)
+    want = o * np.array([0.5, 0.75, 0.25, 1.0]).reshape(4, 1, 1)
+    return np.abs(oracle.output_gate(o, z) - want).max()
+
+
 # name -> (pin, bar).  Bars: 1e-12 where the identity is exact in float64
 # arithmetic up to rounding; looser where a finite difference or eps enters.
 PINS = {
@@ -361,6 +439,11 @@ PINS = {
     "non_expansive": (pin_non_expansive, 1e-12),
     "qk_scale_invariance": (pin_qk_scale_invariance, 1e-4),
     "decode_heads_match_prefill_T1": (pin_decode_heads_match_prefill_T1, 1e-12),
+    "conv_identity_tap": (pin_conv_identity_tap, 0.0),
+    "conv_matches_library": (pin_conv_matches_library, 1e-12),
+    "conv_stays_in_sequence": (pin_conv_stays_in_sequence, 0.0),
+    "silu_closed_form": (pin_silu_closed_form, 1e-15),
+    "output_gate_values": (pin_output_gate_values, 1e-15),
 }
 
 

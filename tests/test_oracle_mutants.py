@@ -4,6 +4,8 @@ modified: each mutant is compiled from a patched temporary copy."""
 import os
 import subprocess
 
+import numpy as np
+
 import pytest
 
 import oracle_pins
@@ -57,5 +59,48 @@ def test_mutant_is_caught(tmp_path, label, old, new):
                    check=True)
     lib = oracle.load(str(so))
     res = oracle_pins.run_all(lib=lib)
+    failed = [n for n, (_, _, ok) in res.items() if not ok]
+    assert failed, f"mutant '{label}' passed every pin"
+
+
+# Mistakes planted in the float64 prologue / epilogue functions (Python),
+# each caught by at least one pin.
+def _conv_reversed_taps(x, w, cu_seqlens=None, silu=False):
+    return _orig_conv(x, np.asarray(w)[::-1].copy(), cu_seqlens, silu)
+
+
+def _conv_crosses_sequences(x, w, cu_seqlens=None, silu=False):
+    return _orig_conv(x, w, None, silu)
+
+
+def _conv_skips_current_token(x, w, cu_seqlens=None, silu=False):
+    w = np.asarray(w, np.float64)
+    shifted = np.concatenate([np.zeros_like(w[:1]), w[:-1]], 0)
+    return _orig_conv(x, shifted, cu_seqlens, silu)
+
+
+def _conv_wrong_activation(x, w, cu_seqlens=None, silu=False):
+    y = _orig_conv(x, w, cu_seqlens, False)
+    return y / (1.0 + np.exp(y)) if silu else y
+
+
+def _gate_wrong_sign(o, z):
+    return _orig_gate(o, -np.asarray(z, np.float64))
+
+
+_orig_conv = oracle.short_conv
+_orig_gate = oracle.output_gate
+
+PY_MUTANTS = [("conv taps reversed", "short_conv", _conv_reversed_taps),
+              ("conv crosses sequence starts", "short_conv", _conv_crosses_sequences),
+              ("conv skips the current token", "short_conv", _conv_skips_current_token),
+              ("activation sigmoid(-x)", "short_conv", _conv_wrong_activation),
+              ("gate sigmoid(-z)", "output_gate", _gate_wrong_sign)]
+
+
+@pytest.mark.parametrize("label,name,fn", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_python_mutant_is_caught(monkeypatch, label, name, fn):
+    monkeypatch.setattr(oracle, name, fn)
+    res = oracle_pins.run_all()
     failed = [n for n, (_, _, ok) in res.items() if not ok]
     assert failed, f"mutant '{label}' passed every pin"
