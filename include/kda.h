@@ -109,6 +109,10 @@ typedef enum {
  *                  the sequence x head chains one after another); the rest of
  *                  the GPU prepares the next segment meanwhile.  A tuning knob
  *                  only: results are bit-identical for every value.
+ *   conv_width     taps of the short convolution of kda_prefill_fused (1 to
+ *                  4; 0 when there is none).  Ignored by the other entry points.
+ *   conv_silu      1: the convolution's output passes through x*sigmoid(x)
+ *                  (kda_prefill_fused only); 0: no activation.
  *   wait_limit     0 = default.  Otherwise the number of polls after which a
  *                  wait of the tensor-core kernels on an asynchronous step
  *                  (a copy, a tensor-core product, another role of the same
@@ -132,6 +136,8 @@ typedef struct {
     int32_t segment_chunks;
     int32_t scalar_gate;
     int32_t recurrence_ctas;
+    int32_t conv_width;
+    int32_t conv_silu;
     uint32_t wait_limit;
 } kda_prefill_desc;
 
@@ -238,6 +244,35 @@ kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, cons
                                const float *beta, const float *init_state,
                                const int32_t *cu_seqlens, void *out, float *final_state,
                                float *ckpts, const kda_prefill_desc *desc, kda_stream_t stream);
+
+/*
+ * kda_prefill with the steps on either side of the recurrence fused into its
+ * kernels (page "Kimi K3 reconstructs long-context inference efficiency
+ * ...", section "Methodology notes", item "Memory control: Kimi Delta
+ * Attention": KDA combines a short convolution, the L2 normalisation of q and
+ * k, and an output forget gate with the recurrence):
+ *   conv_w  [3, desc->conv_width, H, D] fp32, or NULL for no convolution: the
+ *           taps for q, k and v of a causal depthwise convolution along the
+ *           tokens of each sequence,
+ *               x'[t] = sum_{i < W} conv_w[., i] * x[t - (W - 1) + i],
+ *           with tokens before the sequence's first counted as zero (tap
+ *           W - 1 multiplies the current token), then x' * sigmoid(x') when
+ *           desc->conv_silu.  The preparation kernel convolves q, k and v as
+ *           it loads them (the tensor-core path rounds the results to f16,
+ *           11 significant bits, within the f16 range it requires of q, k
+ *           and v; the fp32 path keeps fp32); the L2
+ *           normalisation of q and k follows as in kda_prefill.
+ *   gate    [T, H, Dv] dtype of out, or NULL for no gate: the output is
+ *           o * sigmoid(gate), applied as the recurrence kernel stores it.
+ * Every other argument, and the results without conv_w and gate, as
+ * kda_prefill.  A sequence's convolution starts from zeros: a prefill resumed
+ * from a checkpoint mid-sequence does not see the tokens before it.
+ */
+kda_status kda_prefill_fused(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                             void *out, float *final_state, float *ckpts, const float *conv_w,
+                             const void *gate, const kda_prefill_desc *desc, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream);
 
 /*
  * Chunked prefill whose states live in a pool of slots (the prefill side of

@@ -68,6 +68,10 @@ kda_status check_desc(const kda_prefill_desc *d, Layout *lay)
     if (d->max_seq_len < 0) return fail(KDA_ERR_INVALID_ARG, "max_seq_len must be >= 0");
     if (d->segment_chunks < 0) return fail(KDA_ERR_INVALID_ARG, "segment_chunks must be >= 0");
     if (d->recurrence_ctas < 0) return fail(KDA_ERR_INVALID_ARG, "recurrence_ctas must be >= 0");
+    if (d->conv_width < 0 || d->conv_width > kda::kConvTaps)
+        return fail(KDA_ERR_UNSUPPORTED, "conv_width %d not in [0, %d]", d->conv_width, kda::kConvTaps);
+    if (d->conv_silu != 0 && d->conv_silu != 1)
+        return fail(KDA_ERR_INVALID_ARG, "conv_silu must be 0 or 1 (got %d)", d->conv_silu);
     if (d->scalar_gate != 0 && d->scalar_gate != 1)
         return fail(KDA_ERR_INVALID_ARG, "scalar_gate must be 0 or 1 (got %d)", d->scalar_gate);
     const int64_t maxc = d->total_tokens / d->chunk + d->num_seqs;
@@ -156,7 +160,7 @@ namespace kda {
 kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
                         const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
                         float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
-                        kda_stream_t stream, bool use_graph, const PoolArgs *pool)
+                        kda_stream_t stream, bool use_graph, const PoolArgs *pool, const FusedArgs *fused)
 {
     Layout L;
     kda_status s = check_desc(desc, &L);
@@ -178,6 +182,11 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     } else if (desc->ckpt_stride > 0 && !ckpts && desc->ckpt_capacity > 0) {
         return fail(KDA_ERR_INVALID_ARG, "ckpts is NULL but ckpt_capacity > 0");
     }
+    if (fused && fused->conv_w && desc->conv_width < 1)
+        return fail(KDA_ERR_INVALID_ARG, "conv_w given but conv_width is %d (must be 1 to %d)", desc->conv_width,
+                    kda::kConvTaps);
+    if (fused && fused->gate && (fused->gate == q || fused->gate == k || fused->gate == v || fused->gate == out))
+        return fail(KDA_ERR_INVALID_ARG, "gate aliases q, k, v or out");
     if (!workspace) return fail(KDA_ERR_WORKSPACE, "workspace is NULL");
     if (workspace_bytes < L.total)
         return fail(KDA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
@@ -220,6 +229,10 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
         a.ckpt_slots = pool->ckpt_slots;
         a.pool_slots = pool->slots;
     }
+    a.conv_w = fused ? fused->conv_w : nullptr;
+    a.conv_width = a.conv_w ? desc->conv_width : 0;
+    a.conv_silu = a.conv_w ? desc->conv_silu : 0;
+    a.gate = fused ? fused->gate : nullptr;
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e;
@@ -248,6 +261,18 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
     NvtxRange r("kda_prefill");
     return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc, workspace,
                              workspace_bytes, stream, true);
+}
+
+kda_status kda_prefill_fused(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                             void *out, float *final_state, float *ckpts, const float *conv_w,
+                             const void *gate, const kda_prefill_desc *desc, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream)
+{
+    NvtxRange r("kda_prefill_fused");
+    const kda::FusedArgs fused{conv_w, gate};
+    return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc, workspace,
+                             workspace_bytes, stream, true, nullptr, &fused);
 }
 
 kda_status kda_prefill_pooled(const void *q, const void *k, const void *v, const float *g,

@@ -105,6 +105,11 @@ struct PrefillArgs {
     // sequence n (or checkpoint j) to its slot; NULL tables: dense arrays.
     const int32_t *init_slots, *final_slots, *ckpt_slots;
     int64_t pool_slots;
+    // Fused prologue / epilogue (kda_prefill_fused): short-convolution taps
+    // [3, conv_width, H, D] (NULL: none) with optional SiLU, output gate [T, H, Dv]
+    const float *conv_w;
+    int conv_width, conv_silu;
+    const void *gate;
     cudaStream_t stream;
 };
 
@@ -161,6 +166,14 @@ struct PoolArgs {
     int64_t slots;
     const int32_t *init_slots, *final_slots, *ckpt_slots;
 };
+// The fused prologue / epilogue of kda_prefill_fused.
+struct FusedArgs {
+    const float *conv_w;
+    const void *gate;
+};
+// Taps of the short convolution as the kernels apply it (narrower
+// convolutions are padded with zero taps on the older side).
+constexpr int kConvTaps = 4;
 // kda_prefill's body; use_graph = false launches every kernel directly (no
 // CUDA graph is captured or instantiated: the no-allocation entry point).
 // With `pool`, states and checkpoints live in pool slots (init_state,
@@ -168,7 +181,8 @@ struct PoolArgs {
 kda_status prefill_call(const void *q, const void *k, const void *v, const float *g, const float *beta,
                         const float *init_state, const int32_t *cu_seqlens, void *out, float *final_state,
                         float *ckpts, const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
-                        kda_stream_t stream, bool use_graph, const PoolArgs *pool = nullptr);
+                        kda_stream_t stream, bool use_graph, const PoolArgs *pool = nullptr,
+                        const FusedArgs *fused = nullptr);
 
 // Default number of polls of a bounded device-side wait.
 constexpr uint32_t kDefaultWaitLimit = 1u << 22;

@@ -97,7 +97,8 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, int N, int H,
-               SeqTable tab, float *__restrict__ handoff, int scalar_gate, DevStatus *st)
+               SeqTable tab, float *__restrict__ handoff, int scalar_gate, DevStatus *st,
+               const float *__restrict__ conv_w, int conv_width, int conv_silu)
 {
     constexpr int P = D + 1;   // padded row pitch (bank-conflict free columns)
     extern __shared__ float smem[];
@@ -113,22 +114,35 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     if (gc >= tab.chunk_off[N]) return;
     const int n = find_seq(tab.chunk_off, N, gc);
+    const int seq_t0 = tab.cu[n];
     const int t0 = tab.cu[n] + (gc - tab.chunk_off[n]) * kC;
     const int L = min(kC, tab.cu[n + 1] - t0);
     Handoff ho = handoff_at(handoff, (size_t)gc * H + h, D);
 
     // 1. rows: qh, kh (normalised, one warp per row), v, beta.  Rows >= L are zero.
+    //    With conv_w (the fused prologue) q, k, v are first convolved along the
+    //    sequence's tokens: x'[t] = sum_i w[i] x[t - (W - 1) + i] (tokens before the
+    //    sequence's first count as zero), optionally x' sigmoid(x'), in fp32.
     const int warp = tid >> 5, lane = tid & 31;
+    auto input = [&](const T *x, int t, int r, int d) -> float {   // x'[t0 + r] at channel d (or x itself)
+        if (!conv_w) return to_f32(x[((size_t)(t0 + r) * H + h) * D + d]);
+        float acc = 0.f;
+        for (int i = 0; i < conv_width; ++i) {
+            const int tau = t0 + r - (conv_width - 1) + i;
+            if (tau >= seq_t0)
+                acc += conv_w[(((size_t)t * conv_width + i) * H + h) * D + d] * to_f32(x[((size_t)tau * H + h) * D + d]);
+        }
+        return conv_silu ? acc / (1.f + expf(-acc)) : acc;
+    };
     for (int r = warp; r < kC; r += kThreads / 32) {
         float qa[D / 32], ka[D / 32];
         float sq = 0.f, sk = 0.f;
-        const size_t row = ((size_t)(t0 + r) * H + h) * D;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) {
             const int d = lane + 32 * j;
-            qa[j] = r < L ? to_f32(q[row + d]) : 0.f;
-            ka[j] = r < L ? to_f32(k[row + d]) : 0.f;
-            Vs[r * P + d] = r < L ? to_f32(v[row + d]) : 0.f;
+            qa[j] = r < L ? input(q, 0, r, d) : 0.f;
+            ka[j] = r < L ? input(k, 1, r, d) : 0.f;
+            Vs[r * P + d] = r < L ? input(v, 2, r, d) : 0.f;
             sq += qa[j] * qa[j];
             sk += ka[j] * ka[j];
         }
@@ -243,7 +257,7 @@ constexpr int kBV = 32;
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__ handoff,
-               T *__restrict__ out)
+               T *__restrict__ out, const T *__restrict__ gate)
 {
     constexpr int P = D + 1;
     constexpr int NB = D / kBV;
@@ -310,7 +324,9 @@ k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__
             float acc = 0.f;
             for (int d = 0; d < D; ++d) acc += Qg[r * P + d] * Ss[d * kBV + j];
             for (int i = 0; i <= r; ++i) acc += Ms[r * (kC + 1) + i] * Ws[i * kBV + j];
-            out[((size_t)(t0 + r) * H + h) * D + jb * kBV + j] = from_f32<T>(acc);
+            const size_t oi = ((size_t)(t0 + r) * H + h) * D + jb * kBV + j;
+            if (gate) acc /= 1.f + expf(-to_f32(gate[oi]));   // the fused output gate o sigmoid(z)
+            out[oi] = from_f32<T>(acc);
         }
         __syncthreads();
         // S1 = Diag(gamma_last) S0 + Ke^T W
@@ -355,12 +371,12 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
         dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
         k1_simt_kernel<D, T><<<g1, kThreads, sm1, a.stream>>>(
             (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.N, a.H, a.tab,
-            (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status);
+            (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status, a.conv_w, a.conv_width, a.conv_silu);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned g2 = (unsigned)((size_t)a.N * a.H * (D / kBV));
     k2_simt_kernel<D, T><<<g2, kThreads, sm2, a.stream>>>(state_io(a), a.N, a.H, a.tab,
-                                                           (const float *)a.handoff, (T *)a.out);
+                                                           (const float *)a.handoff, (T *)a.out, (const T *)a.gate);
     return cudaGetLastError();
 }
 

@@ -169,11 +169,20 @@ __device__ __forceinline__ uint4 pack_f16x8(const float *x)
                       pack_f16x2(x[6], x[7]));
 }
 
+// The fused prologue's taps (kConv): fp32 [3 (q, k, v)][kConvTaps][128
+// channels] after the kernel's other shared memory, the oldest taps zero for a
+// narrower convolution.
+constexpr uint32_t K1_TAPS_BYTES = 3 * kConvTaps * kD * 4;
+// two CTAs per SM with the taps: dynamic + static (3 KB) + the 1 KB the SM reserves per CTA
+static_assert(2 * (K1_SMEM + K1_TAPS_BYTES + 3072 + 1024) <= 228 * 1024, "two CTAs per SM with the taps");
+
+template <bool kConv>   // true: q, k, v pass through the short convolution as they are loaded
 __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
-             DevStatus *st, uint32_t wait_limit)
+             DevStatus *st, uint32_t wait_limit, const float *__restrict__ conv_w, int conv_width,
+             int conv_silu)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar, qbar, dbar;
@@ -221,6 +230,22 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int rb = 8 * warp;
     const bf16 *qrow = q + ((size_t)t0 * H + h) * kD, *krow = k + ((size_t)t0 * H + h) * kD;
     const bf16 *vrow = v + ((size_t)t0 * H + h) * kD;
+    size_t xstride = (size_t)H * kD;   // row stride of q, k, v (kConv: of their convolved copies)
+    // q, k, v element pairs: read-only inputs, or (kConv) the convolved rows this
+    // CTA wrote, which must not go through the read-only path
+    // an element pair of q, k, v as fp32: bf16 inputs, or (kConv) f16 convolved rows
+    auto up2 = [&](uint32_t u) -> float2 {
+        if constexpr (kConv) {
+            const __half2 h2 = *reinterpret_cast<const __half2 *>(&u);
+            return __half22float2(h2);
+        } else {
+            return make_float2(bf_lo(u), bf_hi(u));
+        }
+    };
+    auto ldx = [&](const bf16 *p) -> uint32_t {
+        if constexpr (kConv) return *reinterpret_cast<const volatile uint32_t *>(p);
+        else return __ldg(reinterpret_cast<const unsigned int *>(p));
+    };
     // the gate: a decay per key channel ([T, H, Dk]) or one per row shared by
     // every channel ([T, H], then the same value fills both lanes of gv)
     const float *grow = g + ((size_t)t0 * H + h) * (scalar_gate ? 1 : kD);
@@ -233,11 +258,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         if (L == kC && !scalar_gate) {   // a full chunk with a per-channel gate: no row predicates
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const size_t o = (size_t)(rb + j) * rstride + d;
+                const size_t o = (size_t)(rb + j) * rstride + d, ox = (size_t)(rb + j) * xstride + d;
                 gv[j] = __ldg(reinterpret_cast<const float2 *>(grow + o));
-                qv[j] = __ldg(reinterpret_cast<const unsigned int *>(qrow + o));
-                kv[j] = __ldg(reinterpret_cast<const unsigned int *>(krow + o));
-                vv[j] = __ldg(reinterpret_cast<const unsigned int *>(vrow + o));
+                qv[j] = ldx(qrow + ox);
+                kv[j] = ldx(krow + ox);
+                vv[j] = ldx(vrow + ox);
             }
             return;
         }
@@ -245,18 +270,75 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         for (int j = 0; j < 8; ++j) {
             const int r = rb + j;
             const bool valid = r < L;
-            const size_t o = (size_t)r * rstride + d;
+            const size_t o = (size_t)r * rstride + d, ox = (size_t)r * xstride + d;
             if (scalar_gate) {
                 const float gs = valid ? __ldg(grow + (size_t)r * H) : 0.f;
                 gv[j] = make_float2(gs, gs);
             } else {
                 gv[j] = valid ? __ldg(reinterpret_cast<const float2 *>(grow + o)) : make_float2(0.f, 0.f);
             }
-            qv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(qrow + o)) : 0u;
-            kv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(krow + o)) : 0u;
-            vv[j] = valid ? __ldg(reinterpret_cast<const unsigned int *>(vrow + o)) : 0u;
+            qv[j] = valid ? ldx(qrow + ox) : 0u;
+            kv[j] = valid ? ldx(krow + ox) : 0u;
+            vv[j] = valid ? ldx(vrow + ox) : 0u;
         }
     };
+    if constexpr (kConv) {
+        // The fused short convolution, as a first pass over the chunk: the taps
+        // of this head into shared memory (zero on the older side of a narrower
+        // convolution), then x'[r] = sum_i tap[i] x[r - 3 + i] in fp32 (x = 0
+        // before the sequence's first token; x' = 0 from row L on), optionally
+        // x' sigmoid(x'), rounded to f16 (11 significant bits; within the f16
+        // range the operand tiles require of q, k, v anyway) into this chunk's
+        // record, in areas the
+        // record's own tiles fill only after the operand build (q' at the Q'
+        // tile, k' at the Ke^T tile, v' at the Uv^T tile; rows of 128 channels).
+        // The build below then reads q', k', v' from there.
+        float *taps = reinterpret_cast<float *>(sm + K1_SMEM);
+        for (int i = tid; i < 3 * kConvTaps * kD; i += K1_THREADS) {
+            const int t = i / (kConvTaps * kD), j = (i / kD) % kConvTaps, c = i % kD;
+            const int jw = j - (kConvTaps - conv_width);
+            taps[i] = jw >= 0 ? __ldg(conv_w + (((size_t)t * conv_width + jw) * H + h) * kD + c) : 0.f;
+        }
+        __syncthreads();
+        const int cp = 2 * (tid & 63), r0 = 16 * (tid >> 6);   // channel pair, 16 output rows
+#pragma unroll 1
+        for (int t = 0; t < 3; ++t) {
+            const bf16 *src = t == 0 ? qrow : t == 1 ? krow : vrow;
+            uint32_t *dst = reinterpret_cast<uint32_t *>(rec + (t == 0 ? REC_QP : t == 1 ? REC_KM : REC_UV));
+            float2 w[kConvTaps], win[kConvTaps];
+#pragma unroll
+            for (int i = 0; i < kConvTaps; ++i) {
+                w[i] = *reinterpret_cast<const float2 *>(taps + (t * kConvTaps + i) * kD + cp);
+                // window slots 1 .. 3 start with rows r0 - 3 .. r0 - 1 (slot 0 is
+                // shifted out before first use); each step shifts and appends a row
+                const int rr = r0 - kConvTaps + i;
+                const bool valid = i > 0 && rr < L && lc * kC + rr >= 0;
+                const uint32_t u = valid ? __ldg(reinterpret_cast<const unsigned int *>(
+                                               src + (ptrdiff_t)rr * (ptrdiff_t)rstride + cp)) : 0u;
+                win[i] = make_float2(bf_lo(u), bf_hi(u));
+            }
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                const int r = r0 + j;
+                const uint32_t u = r < L ? __ldg(reinterpret_cast<const unsigned int *>(src + (size_t)r * rstride + cp))
+                                         : 0u;
+#pragma unroll
+                for (int i = 0; i < kConvTaps - 1; ++i) win[i] = win[i + 1];
+                win[kConvTaps - 1] = make_float2(bf_lo(u), bf_hi(u));
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < kConvTaps; ++i) acc = __ffma2_rn(w[i], win[i], acc);
+                if (conv_silu)
+                    acc = make_float2(__fdividef(acc.x, 1.f + __expf(-acc.x)), __fdividef(acc.y, 1.f + __expf(-acc.y)));
+                dst[(r * kD + cp) >> 1] = r < L ? pack_f16x2(acc.x, acc.y) : 0u;
+            }
+        }
+        __syncthreads();   // the convolved rows are visible to the whole CTA (global memory)
+        qrow = reinterpret_cast<const bf16 *>(rec + REC_QP);
+        krow = reinterpret_cast<const bf16 *>(rec + REC_KM);
+        vrow = reinterpret_cast<const bf16 *>(rec + REC_UV);
+        xstride = kD;
+    }
     const float beta_r = (tid < kC && tid < L) ? __ldg(beta + (size_t)(t0 + tid) * H + h) : 0.f;
     load_half(0);
     // L2 prefetch of the second channel half of this chunk's rows (bulk, one
@@ -266,7 +348,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const char *base = which == 0 ? (const char *)q : which == 1 ? (const char *)k
                          : which == 2 ? (const char *)v : (const char *)g;
         const uint32_t esz = which == 3 ? 4u : 2u;
-        if (r < L && (which < 3 || !scalar_gate))
+        if (!kConv && r < L && (which < 3 || !scalar_gate))
             prefetch_l2(base + (((size_t)(t0 + r) * H + h) * kD + 64) * esz, 64 * esz);
     }
 
@@ -354,7 +436,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     e = make_float2(__expf(x.x), __expf(x.y));
                     ei = make_float2(__expf(-x.x), __expf(-x.y));
                 }
-                const float2 qq = make_float2(bf_lo(qv[j]), bf_hi(qv[j])), kk = make_float2(bf_lo(kv[j]), bf_hi(kv[j]));
+                const float2 qq = up2(qv[j]), kk = up2(kv[j]);
                 const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
                 const float2 s2 = __ffma2_rn(qk1, qk1, __fmul2_rn(qk0, qk0));
                 sq[j] = (up16 ? s2.y : s2.x) + __shfl_xor_sync(0xffffffffu, up16 ? s2.x : s2.y, 16);
@@ -371,7 +453,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     make_float2(round_tf32(kd.x), round_tf32(kd.y));
                 qgx[0][u] = qg.x; qgx[1][u] = qg.y;
                 kgx[0][u] = kg.x; kgx[1][u] = kg.y;
-                vx[0][u] = bf_lo(vv[j]); vx[1][u] = bf_hi(vv[j]);
+                const float2 vf = up2(vv[j]);
+                vx[0][u] = vf.x; vx[1][u] = vf.y;
                 kex[0][u] = ke.x; kex[1][u] = ke.y;
             }
             qp0[j2 / 2] = pack_f16x2(qgx[0][0], qgx[0][1]);
@@ -810,11 +893,14 @@ __device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, c
 }
 
 
-template <bool kMulti>   // false: one chain per CTA (grid = chains); true: chains in turn
+// kMulti false: one chain per CTA (grid = chains); true: chains in turn.
+// kGate: the output is o * sigmoid(gate) (the fused epilogue), gate [T, H, Dv] bf16.
+template <bool kMulti, bool kGate>
 __global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
 k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
-             float *__restrict__ carry, bf16 *__restrict__ out, DevStatus *st, uint32_t wait_limit)
+             float *__restrict__ carry, bf16 *__restrict__ out, DevStatus *st, uint32_t wait_limit,
+             const bf16 *__restrict__ gate)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], gfull[kGamSlots], sdone, pread[2], sready[2], dbar;
@@ -984,6 +1070,18 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
             mbar_arrive(&sready[qd >> 1]);
             for (int c = 0; c < nch && alive; ++c) {
                 const int cc = base + c;
+                // kGate: this chunk's gate values for the thread's output rows
+                // [16 qd, 16 qd + 16) of column e, loaded before the waits so that
+                // they arrive with the product; the gate then applies to the fp32
+                // output before its one rounding to bf16
+                uint32_t zg[kGate ? 16 : 1];
+                if constexpr (kGate) {
+                    const int tz = seq_t0 + (c_lo + c) * kC, Lz = min(kC, seq_t1 - tz);
+                    const unsigned short *zrow = reinterpret_cast<const unsigned short *>(gate) +
+                                                 ((size_t)(tz + 16 * qd) * H + h) * kD + e;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zg[i] = 16 * qd + i < Lz ? zrow[(size_t)i * H * kD] : 0u;
+                }
                 // gamma has landed (its slot's barrier cannot run ahead: slot cc % 4
                 // is refilled only after the product of chunk cc + 2, which needs
                 // this thread's S^T of chunk cc + 1) and the chunk's product is in TMEM
@@ -1001,6 +1099,10 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     float o[16];
                     tmem_ld16(tm + lane_base + T2_O + 256 * (cc & 1) + 16 * qd, o);
                     tmem_ld_wait();
+                    if constexpr (kGate) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __fdividef(o[i], 1.f + __expf(-__uint_as_float(zg[i] << 16)));
+                    }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
@@ -1256,12 +1358,16 @@ cudaError_t tc_kernel_attributes()
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(k1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
+        e = cudaFuncSetAttribute(k1_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k2_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
+        e = cudaFuncSetAttribute(k1_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(K1_SMEM + K1_TAPS_BYTES));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k2_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
-        if (e != cudaSuccess) return e;
+        const void *k2s[] = {(const void *)k2_tc_kernel<false, false>, (const void *)k2_tc_kernel<true, false>,
+                             (const void *)k2_tc_kernel<false, true>, (const void *)k2_tc_kernel<true, true>};
+        for (const void *f : k2s)
+            if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM)) != cudaSuccess)
+                return e;
         attr_done.fetch_or(bit, std::memory_order_release);
     }
     return cudaSuccess;
@@ -1363,30 +1469,63 @@ cudaError_t launch_prefill_tc_graph(const PrefillArgs &a)
     return cudaGraphLaunch(g.exec[slot], a.stream);
 }
 
+namespace {
+// One K1 launch (the plain or the convolving kernel).
+void launch_k1(const PrefillArgs &a, unsigned grid, cudaStream_t stream, uint8_t *ring, int lo, int cnt, int G,
+               int slot)
+{
+    const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
+    if (a.conv_w)
+        k1_tc_kernel<true><<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
+            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu);
+    else
+        k1_tc_kernel<false><<<grid, K1_THREADS, K1_SMEM, stream>>>(
+            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
+            a.wait_limit, nullptr, 0, 0);
+}
+// One K2 launch (one chain per CTA or chains in turn; with or without the gate).
+void launch_k2(const PrefillArgs &a, bool multi, unsigned grid, cudaStream_t stream, const uint8_t *ring, int lo,
+               int cnt, int G, int slot, float *carry)
+{
+    const bf16 *gate = (const bf16 *)a.gate;
+    bf16 *out = (bf16 *)a.out;
+    const StateIO io = state_io(a);
+    if (multi && gate)
+        k2_tc_kernel<true, true><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
+                                                                         carry, out, a.status, a.wait_limit, gate);
+    else if (multi)
+        k2_tc_kernel<true, false><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
+                                                                          carry, out, a.status, a.wait_limit, nullptr);
+    else if (gate)
+        k2_tc_kernel<false, true><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
+                                                                          carry, out, a.status, a.wait_limit, gate);
+    else
+        k2_tc_kernel<false, false><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
+                                                                           carry, out, a.status, a.wait_limit, nullptr);
+}
+}  // namespace
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a)
 {
     cudaError_t e;
     g_detail[0] = 0;
     if ((e = tc_kernel_attributes()) != cudaSuccess) return e;
-    const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
     uint8_t *ring = (uint8_t *)a.handoff;
     const unsigned chains = (unsigned)((size_t)a.N * a.H);
     const SegPlan &p = a.plan;
 
     if (p.nseg <= 1) {   // one K1 over every chunk, then one K2 over every sequence
         if (a.max_chunks > 0) {
-            k1_tc_kernel<<<(unsigned)((size_t)a.max_chunks * a.H), K1_THREADS, K1_SMEM, a.stream>>>(
-                q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, 0, 0, 0, 0, a.scalar_gate ? 1 : 0, a.status,
-                a.wait_limit);
+            launch_k1(a, (unsigned)((size_t)a.max_chunks * a.H), a.stream, ring, 0, 0, 0, 0);
             if ((e = cudaGetLastError()) != cudaSuccess) {
-                note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
+                note_launch_failure(k1_tc_kernel<false>, "K1", K1_THREADS, K1_SMEM);
                 return e;
             }
         }
-        k2_tc_kernel<false><<<chains, K2_THREADS, K2_SMEM, a.stream>>>(
-            state_io(a), a.N, a.H, a.tab, ring, 0, 0, 0, 0, nullptr, (bf16 *)a.out, a.status, a.wait_limit);
+        launch_k2(a, false, chains, a.stream, ring, 0, 0, 0, 0, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess)
-            note_launch_failure(k2_tc_kernel<false>, "K2", K2_THREADS, K2_SMEM);
+            note_launch_failure(k2_tc_kernel<false, false>, "K2", K2_THREADS, K2_SMEM);
         return e;
     }
 
@@ -1400,25 +1539,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         const int slot = s % p.R, lo = p.begin(s), cnt = p.count(s);
         const unsigned k1_grid = (unsigned)((size_t)a.N * cnt * a.H);
         if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
-        k1_tc_kernel<<<k1_grid, K1_THREADS, K1_SMEM, a.stream>>>(
-            q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit);
+        launch_k1(a, k1_grid, a.stream, ring, lo, cnt, p.G, slot);
         if ((e = cudaGetLastError()) != cudaSuccess) {
-            note_launch_failure(k1_tc_kernel, "K1", K1_THREADS, K1_SMEM);
+            note_launch_failure(k1_tc_kernel<false>, "K1", K1_THREADS, K1_SMEM);
             break;
         }
         if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(c->side, c->k1[slot], 0)) != cudaSuccess) break;
-        if (p.k2_ctas > 0)
-            k2_tc_kernel<true><<<(unsigned)p.k2_ctas, K2_THREADS, K2_SMEM, c->side>>>(
-                state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
-                a.wait_limit);
-        else
-            k2_tc_kernel<false><<<chains, K2_THREADS, K2_SMEM, c->side>>>(
-                state_io(a), a.N, a.H, a.tab, ring, lo, cnt, p.G, slot, a.carry, (bf16 *)a.out, a.status,
-                a.wait_limit);
+        launch_k2(a, p.k2_ctas > 0, p.k2_ctas > 0 ? (unsigned)p.k2_ctas : chains, c->side, ring, lo, cnt, p.G, slot,
+                  a.carry);
         if ((e = cudaGetLastError()) != cudaSuccess) {
-            note_launch_failure(k2_tc_kernel<false>, "K2", K2_THREADS, K2_SMEM);
+            note_launch_failure(k2_tc_kernel<false, false>, "K2", K2_THREADS, K2_SMEM);
             break;
         }
         e = cudaEventRecord(c->k2[slot], c->side);

@@ -22,8 +22,8 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
-           "kda_prefill_pooled", "kda_decode", "kda_decode_paged", "kda_decode_multi", "kda_prefill_noalloc",
-           "kda_last_error", "kda_version")
+           "kda_prefill_pooled", "kda_prefill_fused", "kda_decode", "kda_decode_paged", "kda_decode_multi",
+           "kda_prefill_noalloc", "kda_last_error", "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -42,7 +42,8 @@ class PrefillDesc(ctypes.Structure):
                 ("chunk", ctypes.c_int32), ("ckpt_stride", ctypes.c_int32),
                 ("ckpt_capacity", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
                 ("segment_chunks", ctypes.c_int32), ("scalar_gate", ctypes.c_int32),
-                ("recurrence_ctas", ctypes.c_int32), ("wait_limit", ctypes.c_uint32)]
+                ("recurrence_ctas", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+                ("conv_silu", ctypes.c_int32), ("wait_limit", ctypes.c_uint32)]
 
 
 _lib = None
@@ -68,6 +69,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_prefill_status.argtypes = [_vp, _vp]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
+    lib.kda_prefill_fused.restype = ctypes.c_int
+    lib.kda_prefill_fused.argtypes = [_vp] * 12 + [ctypes.POINTER(PrefillDesc), _vp, ctypes.c_size_t, _vp]
     lib.kda_prefill_pooled.restype = ctypes.c_int
     lib.kda_prefill_pooled.argtypes = [_vp] * 8 + [ctypes.c_int64, _vp, _vp, _vp, ctypes.POINTER(PrefillDesc),
                                                    _vp, ctypes.c_size_t, _vp]
@@ -118,9 +121,10 @@ def _dtype_code(t: torch.Tensor) -> int:
 def make_desc(T: int, H: int, D: int, num_seqs: int, dtype_code: int, chunk: int = 64,
               ckpt_stride: int = 0, ckpt_capacity: int = 0, max_seq_len: int = 0,
               segment_chunks: int = 0, scalar_gate: bool = False, wait_limit: int = 0,
-              recurrence_ctas: int = 0) -> PrefillDesc:
+              recurrence_ctas: int = 0, conv_width: int = 0, conv_silu: bool = False) -> PrefillDesc:
     return PrefillDesc(num_seqs, T, H, D, D, dtype_code, chunk, ckpt_stride, ckpt_capacity,
-                       max_seq_len, segment_chunks, int(bool(scalar_gate)), recurrence_ctas, wait_limit)
+                       max_seq_len, segment_chunks, int(bool(scalar_gate)), recurrence_ctas, conv_width,
+                       int(bool(conv_silu)), wait_limit)
 
 
 def workspace_size(desc: PrefillDesc) -> int:
@@ -206,6 +210,38 @@ def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_s
     code = load_library().kda_prefill_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
         _ptr(out), _ptr(final_state), _ptr(ckpts), ctypes.byref(desc), _stream(stream))
+    _check(code)
+    return out, final_state, ckpts
+
+
+def prefill_fused(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, conv_w=None, conv_silu: bool = False,
+                  gate=None, num_seqs: Optional[int] = None, chunk: int = 64, ckpt_stride: int = 0, ckpts=None,
+                  ckpt_capacity: Optional[int] = None, out=None, final_state=None, workspace=None, stream=None,
+                  max_seq_len: int = 0, segment_chunks: int = 0):
+    """``kda_prefill_fused``: the prefill with the short convolution of q, k, v
+    (taps ``conv_w`` [3, W, H, D] fp32, W <= 4, optional SiLU) before the
+    recurrence and the output gate ``out = o * sigmoid(gate)`` (``gate``
+    [T, H, Dv], the dtype of q) after it.  Returns (out, final_state, ckpts)."""
+    T, H, D = q.shape
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (num_seqs or 1)
+    dev = q.device
+    if out is None:
+        out = torch.empty(T, H, v.shape[2], dtype=q.dtype, device=dev)
+    if final_state is None:
+        final_state = torch.empty(N, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    if ckpt_stride > 0 and ckpts is None:
+        cap = ckpt_capacity if ckpt_capacity is not None else max(1, (T // ckpt_stride) + N)
+        ckpts = torch.zeros(cap, H, D, v.shape[2], dtype=torch.float32, device=dev)
+    cap = ckpt_capacity if ckpt_capacity is not None else (ckpts.shape[0] if ckpts is not None else 0)
+    W = int(conv_w.shape[1]) if conv_w is not None else 0
+    desc = make_desc(T, H, D, N, _dtype_code(q), chunk, ckpt_stride, cap, max_seq_len, segment_chunks,
+                     scalar_gate=g.dim() == 2, conv_width=W, conv_silu=conv_silu)
+    if workspace is None:
+        workspace = alloc_workspace(desc, dev)
+    code = load_library().kda_prefill_fused(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+        _ptr(final_state), _ptr(ckpts), _ptr(conv_w), _ptr(gate), ctypes.byref(desc), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
     _check(code)
     return out, final_state, ckpts
 

@@ -164,3 +164,26 @@ def test_decode_paged_rejects_before_launch(lib):
     # nothing to do
     assert lib.kda_decode_paged(*args, ctypes.c_int64(8), None, ctypes.c_void_p(8192), 0, 2, 128, 128,
                                 kda.DTYPE_BF16, None, None) == 0
+
+
+def test_fused_and_pooled_reject_before_launch(lib):
+    p = ctypes.c_void_p(4096)
+    d = _desc(T=128, H=2, D=128, dtype_code=kda.DTYPE_BF16)
+    ws = lib.kda_prefill_workspace_size(ctypes.byref(d))
+    o = ctypes.c_void_p(8192)
+    # taps given without a width
+    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, p, None, ctypes.byref(d),
+                                 ctypes.c_void_p(1 << 20), ws, None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
+    # width beyond the supported four taps
+    d5 = _desc(T=128, H=2, D=128, dtype_code=kda.DTYPE_BF16, conv_width=5)
+    assert lib.kda_prefill_workspace_size(ctypes.byref(d5)) == 0
+    # the gate may not alias the output
+    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, None, o, ctypes.byref(d),
+                                 ctypes.c_void_p(1 << 20), ws, None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
+    # pooled: slot tables without a pool; checkpoints without their slot table
+    assert lib.kda_prefill_pooled(p, p, p, p, p, None, o, None, ctypes.c_int64(4), p, None, None,
+                                  ctypes.byref(d), ctypes.c_void_p(1 << 20), ws, None) == -1
+    dc = _desc(T=128, H=2, D=128, dtype_code=kda.DTYPE_BF16, ckpt_stride=64, ckpt_capacity=2)
+    wsc = lib.kda_prefill_workspace_size(ctypes.byref(dc))
+    assert lib.kda_prefill_pooled(p, p, p, p, p, None, o, p, ctypes.c_int64(4), None, None, None,
+                                  ctypes.byref(dc), ctypes.c_void_p(1 << 20), wsc, None) == -1
