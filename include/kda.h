@@ -26,7 +26,13 @@
  *     a caller's own stream capture, and in kda_prefill_noalloc, the kernels
  *     are launched directly).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  No entry point synchronises the stream.
+ *     stream).  No entry point synchronises the stream.  Tensor-core prefill
+ *     calls made from one host thread replay the same cached CUDA graphs, so
+ *     the GPU runs them one after another even when they are enqueued on
+ *     different streams; calls from different threads do not share graphs.
+ *     The per-thread side stream, events and graphs live until the process
+ *     exits.
+ *   - g <= 0 (alpha = exp(g) is a decay); see kda_prefill for the range.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns a negative kda_status and touches no buffer.
  *     kda_last_error() then returns a message (thread-local).
@@ -227,7 +233,13 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
  * fixed device array of KDA_NOALLOC_SCRATCH_BYTES built into the library:
  * every GPU that loads the library keeps it resident until the process exits.
  * A call whose kda_prefill_workspace_size() exceeds it returns
- * KDA_ERR_UNSUPPORTED before any work is queued.  Nothing is allocated: no
+ * KDA_ERR_UNSUPPORTED before any work is queued.  The need is about 90.6 KB
+ * per chunk of 64 tokens and head for the bf16 path with Dk = Dv = 128 in
+ * one segment (so about 360 chunk-heads, e.g. 11 chunks of 32 heads); a
+ * smaller desc->segment_chunks bounds it by two ring slots of that many
+ * chunks of every sequence and head plus 64 KB of fp32 carry per sequence
+ * and head (segment_chunks = 1 with 32 heads: about 6 MB plus 2 MB per
+ * sequence).  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library routine is called.
  *
  * The first call on a device looks up the array's device address (with that

@@ -38,6 +38,33 @@ def test_noalloc_matches_workspace_prefill_twice(dtype, D, lens, stride):
         assert state_err(to_np(ck), to_np(ck_ref)) <= TOL_STATE
 
 
+@pytest.mark.parametrize("segment_chunks", [1, 2])
+def test_noalloc_segmented_is_bit_identical(segment_chunks):
+    """With an explicit segment length the call runs the segmented plan: the
+    two-slot record ring and the fp32 carry between segments then live in the
+    built-in array too.  Two calls in a row, compared bit for bit with
+    kda_prefill at the same segment length."""
+    for seed in (33, 34):
+        w = workloads.custom_prefill(H=3, D=128, lens=[300, 0, 129, 64], dtype="bf16", init="randn",
+                                     ckpt_stride=64, seed=seed, varlen=True)
+        d = gpu_inputs(workloads.make_prefill(w))
+        cap = kda.num_checkpoints(w.lens, 64)
+        desc = kda.make_desc(w.total_tokens, 3, 128, w.num_seqs, kda.DTYPE_BF16, 64, 64, cap,
+                             segment_chunks=segment_chunks)
+        assert kda.workspace_size(desc) <= kda.NOALLOC_SCRATCH_BYTES
+        assert kda.launch_count(desc) > 3   # more than one segment
+        o_ref, f_ref, ck_ref = kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                           d["cu_seqlens"], ckpt_stride=64, ckpt_capacity=cap,
+                                           segment_chunks=segment_chunks)
+        o, f, ck = kda.prefill_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                       d["cu_seqlens"], ckpt_stride=64, ckpt_capacity=cap,
+                                       segment_chunks=segment_chunks)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref)
+        assert torch.equal(f, f_ref)
+        assert torch.equal(ck, ck_ref)
+
+
 def test_noalloc_rejects_calls_beyond_its_scratch():
     lib = kda.load_library()
     T = 1 << 20   # about 1M tokens x 32 heads needs far more than the built-in array
