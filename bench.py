@@ -374,12 +374,23 @@ def cpu_baseline_prefill(w, max_token_heads=4_000_000):
                       f"tokens/s counts all H heads of a token"}
 
 
+def shrink(w, factor: int):
+    """The workload with every sequence length divided by ``factor`` (at least
+    one token), named accordingly; ``factor`` 1 returns it unchanged."""
+    if factor <= 1:
+        return w
+    import dataclasses
+    lens = tuple(max(1, L // factor) for L in w.lens)
+    stride = w.ckpt_stride // factor // 64 * 64 if w.ckpt_stride else 0
+    return dataclasses.replace(w, lens=lens, ckpt_stride=stride, name=f"{w.name}, lengths / {factor}")
+
+
 def run_ours(args):
     world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local if world > 1 else 0)
     kda.load_library()
     peaks = load_peaks()
-    w = workloads.workload(args.workload)
+    w = shrink(workloads.workload(args.workload), args.shrink)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     clk = ClockSampler(dev.index if dev.index is not None else 0)
@@ -528,6 +539,9 @@ def main():
     ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 4, 5])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide every sequence length of the workload by this factor (a smaller case of the "
+                         "same shape for profiler captures; the JSON line then names the shrunk workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     args = ap.parse_args()
