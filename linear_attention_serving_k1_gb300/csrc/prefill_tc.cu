@@ -84,6 +84,17 @@ __device__ __forceinline__ int find_seq_tc(const int32_t *chunk_off, int N, int 
     return lo;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+
+// 2^x by the hardware's approximate base-2 exponential, results below the
+// normal range flushed to zero (PTX ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void record_timeout(DevStatus *st)
 {
     record_status(st, (int32_t)KDA_ERR_TIMEOUT);
@@ -417,6 +428,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         // same channels in every warp), no factor can leave the range and the
         // clamps are skipped (a warp-uniform choice).
         const bool clamp = __any_sync(0xffffffffu, fabsf(ref.x) > kMaxDecayExp || fabsf(ref.y) > kMaxDecayExp);
+        const float2 l2e2 = make_float2(kLog2e, kLog2e);
+        const float2 refl2 = make_float2(-ref.x * kLog2e, -ref.y * kLog2e);
         auto build_rows = [&](auto kClamp) {
         float2 bb = make_float2(pre0, pre1);
 #pragma unroll
@@ -426,15 +439,18 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int u = 0; u < 2; ++u) {
                 const int j = j2 + u, r = rb + j;
                 bb = __fadd2_rn(bb, gv[j]);
-                const float2 x = __fadd2_rn(bb, make_float2(-ref.x, -ref.y));
+                // e^(b - B) and e^(B - b) as 2^(+-(b - B) log2 e): one packed FMA for
+                // the exponent, then the hardware base-2 exponential (flush to zero:
+                // the factors stay at or above e^-80, far from the subnormal range)
+                const float2 x = __ffma2_rn(bb, l2e2, refl2);
                 float2 e, ei;
                 if constexpr (decltype(kClamp)::value) {
-                    strong |= fabsf(x.x) > kMaxDecayExp || fabsf(x.y) > kMaxDecayExp;
-                    e = make_float2(__expf(fminf(x.x, kMaxDecayExp)), __expf(fminf(x.y, kMaxDecayExp)));
-                    ei = make_float2(__expf(fminf(-x.x, kMaxDecayExp)), __expf(fminf(-x.y, kMaxDecayExp)));
+                    strong |= fabsf(x.x) > kMaxDecayExp * kLog2e || fabsf(x.y) > kMaxDecayExp * kLog2e;
+                    e = make_float2(ex2_ftz(fminf(x.x, kMaxDecayExp * kLog2e)), ex2_ftz(fminf(x.y, kMaxDecayExp * kLog2e)));
+                    ei = make_float2(ex2_ftz(fminf(-x.x, kMaxDecayExp * kLog2e)), ex2_ftz(fminf(-x.y, kMaxDecayExp * kLog2e)));
                 } else {
-                    e = make_float2(__expf(x.x), __expf(x.y));
-                    ei = make_float2(__expf(-x.x), __expf(-x.y));
+                    e = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
+                    ei = make_float2(ex2_ftz(-x.x), ex2_ftz(-x.y));
                 }
                 const float2 qq = up2(qv[j]), kk = up2(kv[j]);
                 const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
