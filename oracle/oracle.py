@@ -187,14 +187,16 @@ def gdn_prefill(q, k, v, a, beta, init_state=None, cu_seqlens=None, lib=None):
     return out, fin
 
 
-def short_conv(x, w, cu_seqlens=None, silu=False):
+def short_conv(x, w, cu_seqlens=None, silu=False, history=None):
     """Causal depthwise short convolution along time, inside each sequence.
 
     x: [T, H, D]; w: [W, H, D] taps; cu_seqlens: [N + 1] token offsets (None:
     one sequence).  For token t of a sequence starting at s:
-        y[t] = sum_{i < W} w[i] * x[t - (W - 1) + i],   x[tau] = 0 for tau < s
-    (tap W - 1 multiplies the current token; nothing crosses a sequence start),
-    then y * sigmoid(y) when ``silu``.  float64 throughout.
+        y[t] = sum_{i < W} w[i] * x[t - (W - 1) + i]
+    with x[tau] for tau < s taken from ``history`` [N, W - 1, H, D] (the W - 1
+    rows before the sequence, oldest first; None: zeros), so nothing crosses
+    into another sequence (tap W - 1 multiplies the current token), then
+    y * sigmoid(y) when ``silu``.  float64 throughout.
 
     Source: "Kimi K3 reconstructs long-context inference efficiency through
     KDA, cross-depth attention, and latent expert routing", section
@@ -209,6 +211,7 @@ def short_conv(x, w, cu_seqlens=None, silu=False):
     W = w.shape[0]
     cu = _cu(cu_seqlens, T)
     y = np.zeros_like(x)
+    hist = None if history is None else _f64(history)
     for n in range(cu.shape[0] - 1):
         s, e = int(cu[n]), int(cu[n + 1])
         for t in range(s, e):
@@ -216,9 +219,28 @@ def short_conv(x, w, cu_seqlens=None, silu=False):
                 tau = t - (W - 1) + i
                 if tau >= s:
                     y[t] += w[i] * x[tau]
+                elif hist is not None:
+                    y[t] += w[i] * hist[n, (W - 1) + (tau - s)]
     if silu:
         y = y / (1.0 + np.exp(-y))
     return y
+
+
+def conv_tail(x, W, cu_seqlens=None, history=None):
+    """The convolution state after each sequence: its last W - 1 input rows
+    (oldest first) [N, W - 1, H, D], reaching into ``history`` (or zeros) when
+    the sequence is shorter."""
+    x = _f64(x)
+    T, H, D = x.shape
+    cu = _cu(cu_seqlens, T)
+    N = cu.shape[0] - 1
+    hist = np.zeros((N, W - 1, H, D)) if history is None else _f64(history)
+    out = np.zeros((N, W - 1, H, D))
+    for n in range(N):
+        s, e = int(cu[n]), int(cu[n + 1])
+        seq = np.concatenate([hist[n], x[s:e]], 0)
+        out[n] = seq[seq.shape[0] - (W - 1):]
+    return out
 
 
 def output_gate(o, z):
@@ -231,20 +253,55 @@ def output_gate(o, z):
 
 
 def prefill_fused(q, k, v, g, beta, init_state=None, cu_seqlens=None, ckpt_stride=0, conv_w=None,
-                  silu=False, gate=None, lib=None):
+                  silu=False, gate=None, conv_state=None, return_conv_state=False, lib=None):
     """The prefill with the steps around the recurrence: q, k, v pass through
-    ``short_conv`` (taps conv_w [3, W, H, D] for q, k, v; None: none) before
-    the recurrence, and its output through ``output_gate`` (gate [T, H, Dv];
-    None: none).  Returns (out, final_state, ckpts) like ``prefill``."""
+    ``short_conv`` (taps conv_w [3, W, H, D] for q, k, v; None: none; history
+    ``conv_state`` [N, 3, W - 1, H, D] or None for zeros) before the
+    recurrence, and its output through ``output_gate`` (gate [T, H, Dv];
+    None: none).  Returns (out, final_state, ckpts) like ``prefill``, and with
+    ``return_conv_state`` also the convolution state after each sequence
+    ([N, 3, W - 1, H, D], ``conv_tail``) as a fourth element."""
+    tails = None
     if conv_w is not None:
         conv_w = _f64(conv_w)
-        q = short_conv(q, conv_w[0], cu_seqlens, silu)
-        k = short_conv(k, conv_w[1], cu_seqlens, silu)
-        v = short_conv(v, conv_w[2], cu_seqlens, silu)
+        W = conv_w.shape[1]
+        hist = [None] * 3 if conv_state is None else [_f64(conv_state)[:, t] for t in range(3)]
+        tails = np.stack([conv_tail(x, W, cu_seqlens, hist[t]) for t, x in enumerate((q, k, v))], 1)
+        q = short_conv(q, conv_w[0], cu_seqlens, silu, hist[0])
+        k = short_conv(k, conv_w[1], cu_seqlens, silu, hist[1])
+        v = short_conv(v, conv_w[2], cu_seqlens, silu, hist[2])
     o, f, ck = prefill(q, k, v, g, beta, init_state, cu_seqlens, ckpt_stride, lib=lib)
     if gate is not None:
         o = output_gate(o, gate)
+    if return_conv_state:
+        return o, f, ck, tails
     return o, f, ck
+
+
+def decode_fused(q, k, v, g, beta, state, conv_w=None, silu=False, gate=None, conv_state=None, lib=None):
+    """One decode step with the steps around the recurrence: each sequence's
+    new q, k, v ([N, H, D]) are convolved with its history ``conv_state``
+    [N, 3, W - 1, H, D] (None: zeros), the step runs as ``decode`` and the
+    output is gated.  Returns (out, new_state, new_conv_state or None)."""
+    new_cs = None
+    if conv_w is not None:
+        conv_w = _f64(conv_w)
+        W = conv_w.shape[1]
+        N, H, D = q.shape
+        cs = np.zeros((N, 3, W - 1, H, D)) if conv_state is None else _f64(conv_state)
+        xs = []
+        for t, x in enumerate((q, k, v)):
+            x = _f64(x)
+            rows = np.concatenate([cs[:, t], x[:, None]], 1)          # [N, W, H, D], oldest first
+            y = np.einsum("nwhd,whd->nhd", rows, conv_w[t])
+            xs.append(y / (1.0 + np.exp(-y)) if silu else y)
+        new_cs = np.stack([np.concatenate([cs[:, t], _f64(x)[:, None]], 1)[:, 1:]
+                           for t, x in enumerate((q, k, v))], 1)
+        q, k, v = xs
+    o, st = decode(q, k, v, g, beta, state, lib=lib)
+    if gate is not None:
+        o = output_gate(o, gate)
+    return o, st, new_cs
 
 
 def num_threads(lib=None) -> int:

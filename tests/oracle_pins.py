@@ -398,6 +398,49 @@ def pin_conv_stays_in_sequence(lib=None, seed=20):
     return worst
 
 
+def pin_conv_history_continues(lib=None, seed=23):
+    """A sequence convolved in two parts, the second seeded with the first's
+    last W - 1 inputs, gives the whole sequence's convolution; and the fused
+    prefill of the parts (state and convolution state handed on) reproduces
+    the fused prefill of the whole."""
+    rng = _rng(seed)
+    T, H, D, W, cut = 19, 2, 4, 4, 7
+    q, k, v, g, b = _inputs(rng, T, H, D, D)
+    w = rng.standard_normal((3, W, H, D))
+    worst = 0.0
+    whole = oracle.short_conv(q, w[0])
+    tail = oracle.conv_tail(q[:cut], W)
+    second = oracle.short_conv(q[cut:], w[0], history=tail)
+    worst = max(worst, np.abs(whole[cut:] - second).max())
+    o, f, _, cs = oracle.prefill_fused(q, k, v, g, b, conv_w=w, silu=True, return_conv_state=True, lib=lib)
+    o1, f1, _, cs1 = oracle.prefill_fused(q[:cut], k[:cut], v[:cut], g[:cut], b[:cut], conv_w=w, silu=True,
+                                          return_conv_state=True, lib=lib)
+    o2, f2, _, cs2 = oracle.prefill_fused(q[cut:], k[cut:], v[cut:], g[cut:], b[cut:], f1, conv_w=w, silu=True,
+                                          conv_state=cs1, return_conv_state=True, lib=lib)
+    worst = max(worst, np.abs(o[cut:] - o2).max(), np.abs(f - f2).max(), np.abs(cs - cs2).max())
+    # the convolution state is the raw input rows themselves
+    worst = max(worst, np.abs(cs[0, 0] - q[T - (W - 1):]).max(), np.abs(cs[0, 2] - v[T - (W - 1):]).max())
+    return worst
+
+
+def pin_decode_fused_continues_prefill(lib=None, seed=24):
+    """prefill_fused over t tokens, then decode_fused on token t + 1 with the
+    handed-on state and convolution state, equals prefill_fused over t + 1
+    tokens (its last output, final state and convolution state)."""
+    rng = _rng(seed)
+    T, H, D, W = 11, 2, 5, 3
+    q, k, v, g, b = _inputs(rng, T, H, D, D)
+    w = rng.standard_normal((3, W, H, D))
+    z = rng.standard_normal((T, H, D))
+    s0 = rng.standard_normal((1, H, D, D)) * 0.1
+    o, f, _, cs = oracle.prefill_fused(q, k, v, g, b, s0, conv_w=w, gate=z, return_conv_state=True, lib=lib)
+    _, fp, _, csp = oracle.prefill_fused(q[:-1], k[:-1], v[:-1], g[:-1], b[:-1], s0, conv_w=w, gate=z[:-1],
+                                         return_conv_state=True, lib=lib)
+    od, sd, csd = oracle.decode_fused(q[-1:], k[-1:], v[-1:], g[-1:], b[-1:], fp, conv_w=w, gate=z[-1:],
+                                      conv_state=csp, lib=lib)
+    return max(np.abs(od[0] - o[-1]).max(), np.abs(sd - f).max(), np.abs(csd - cs).max())
+
+
 def pin_silu_closed_form(lib=None, seed=21):
     """With pass-through taps, the activation is x sigmoid(x): 0 at 0,
     (3/4) ln 3 at ln 3 and -(1/4) ln 3 at -ln 3 (sigmoid(ln 3) = 3/4)."""
@@ -443,6 +486,8 @@ PINS = {
     "conv_matches_library": (pin_conv_matches_library, 1e-12),
     "conv_stays_in_sequence": (pin_conv_stays_in_sequence, 0.0),
     "silu_closed_form": (pin_silu_closed_form, 1e-15),
+    "conv_history_continues": (pin_conv_history_continues, 1e-12),
+    "decode_fused_continues_prefill": (pin_decode_fused_continues_prefill, 1e-12),
     "output_gate_values": (pin_output_gate_values, 1e-15),
 }
 

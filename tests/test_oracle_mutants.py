@@ -65,23 +65,32 @@ def test_mutant_is_caught(tmp_path, label, old, new):
 
 # Mistakes planted in the float64 prologue / epilogue functions (Python),
 # each caught by at least one pin.
-def _conv_reversed_taps(x, w, cu_seqlens=None, silu=False):
-    return _orig_conv(x, np.asarray(w)[::-1].copy(), cu_seqlens, silu)
+def _conv_reversed_taps(x, w, cu_seqlens=None, silu=False, history=None):
+    return _orig_conv(x, np.asarray(w)[::-1].copy(), cu_seqlens, silu, history)
 
 
-def _conv_crosses_sequences(x, w, cu_seqlens=None, silu=False):
-    return _orig_conv(x, w, None, silu)
+def _conv_crosses_sequences(x, w, cu_seqlens=None, silu=False, history=None):
+    return _orig_conv(x, w, None, silu, None if history is None else history[:1])
 
 
-def _conv_skips_current_token(x, w, cu_seqlens=None, silu=False):
+def _conv_skips_current_token(x, w, cu_seqlens=None, silu=False, history=None):
     w = np.asarray(w, np.float64)
     shifted = np.concatenate([np.zeros_like(w[:1]), w[:-1]], 0)
-    return _orig_conv(x, shifted, cu_seqlens, silu)
+    return _orig_conv(x, shifted, cu_seqlens, silu, history)
 
 
-def _conv_wrong_activation(x, w, cu_seqlens=None, silu=False):
-    y = _orig_conv(x, w, cu_seqlens, False)
+def _conv_wrong_activation(x, w, cu_seqlens=None, silu=False, history=None):
+    y = _orig_conv(x, w, cu_seqlens, False, history)
     return y / (1.0 + np.exp(y)) if silu else y
+
+
+def _conv_ignores_history(x, w, cu_seqlens=None, silu=False, history=None):
+    return _orig_conv(x, w, cu_seqlens, silu, None)
+
+
+def _tail_off_by_one(x, W, cu_seqlens=None, history=None):
+    t = _orig_tail(x, W, cu_seqlens, history)
+    return np.concatenate([t[:, :1], t[:, :-1]], 1)
 
 
 def _gate_wrong_sign(o, z):
@@ -90,12 +99,15 @@ def _gate_wrong_sign(o, z):
 
 _orig_conv = oracle.short_conv
 _orig_gate = oracle.output_gate
+_orig_tail = oracle.conv_tail
 
 PY_MUTANTS = [("conv taps reversed", "short_conv", _conv_reversed_taps),
               ("conv crosses sequence starts", "short_conv", _conv_crosses_sequences),
               ("conv skips the current token", "short_conv", _conv_skips_current_token),
               ("activation sigmoid(-x)", "short_conv", _conv_wrong_activation),
-              ("gate sigmoid(-z)", "output_gate", _gate_wrong_sign)]
+              ("gate sigmoid(-z)", "output_gate", _gate_wrong_sign),
+              ("convolution history ignored", "short_conv", _conv_ignores_history),
+              ("convolution state shifted by a row", "conv_tail", _tail_off_by_one)]
 
 
 @pytest.mark.parametrize("label,name,fn", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
