@@ -274,17 +274,41 @@ kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, cons
  *           11 significant bits, within the f16 range it requires of q, k
  *           and v; the fp32 path keeps fp32); the L2
  *           normalisation of q and k follows as in kda_prefill.
+ *   conv_state_in   [N, 3, conv_width - 1, H, D] dtype of q, or NULL: the
+ *           raw q, k, v rows before each sequence (oldest first), the tokens
+ *           a prefill resumed mid-sequence (or a decode) would otherwise not
+ *           see; NULL counts them as zeros.
+ *   conv_state_out  same shape, or NULL: written, last, with the raw rows
+ *           ending each sequence (reaching into conv_state_in for sequences
+ *           shorter than conv_width - 1), the history kda_decode_fused or a
+ *           later prefill continues from; may be conv_state_in itself.
  *   gate    [T, H, Dv] dtype of out, or NULL for no gate: the output is
  *           o * sigmoid(gate), applied as the recurrence kernel stores it.
  * Every other argument, and the results without conv_w and gate, as
- * kda_prefill.  A sequence's convolution starts from zeros: a prefill resumed
- * from a checkpoint mid-sequence does not see the tokens before it.
+ * kda_prefill (with conv_state_out one launch more than
+ * kda_prefill_launch_count reports).
  */
 kda_status kda_prefill_fused(const void *q, const void *k, const void *v, const float *g,
                              const float *beta, const float *init_state, const int32_t *cu_seqlens,
                              void *out, float *final_state, float *ckpts, const float *conv_w,
-                             const void *gate, const kda_prefill_desc *desc, void *workspace,
-                             size_t workspace_bytes, kda_stream_t stream);
+                             const void *conv_state_in, void *conv_state_out, const void *gate,
+                             const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                             kda_stream_t stream);
+
+/*
+ * kda_decode with the steps around the recurrence (the decode side of
+ * kda_prefill_fused): each sequence's new q, k, v ([N, H, D] dtype) are
+ * convolved with its history conv_state [N, 3, conv_width - 1, H, D] (dtype;
+ * NULL: zeros), which the call then advances by the new raw rows; the step
+ * runs as kda_decode on the dense states [N, H, Dk, Dv]; the output is
+ * o * sigmoid(gate) (gate [N, H, Dv] dtype, or NULL).  conv_w [3, conv_width,
+ * H, D] fp32 as for kda_prefill_fused, or NULL with conv_width 0 for no
+ * convolution; conv_silu 0 or 1.
+ */
+kda_status kda_decode_fused(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state, void *conv_state, const float *conv_w,
+                            const void *gate, void *out, int32_t N, int32_t H, int32_t Dk, int32_t Dv,
+                            kda_dtype dtype, int32_t conv_width, int32_t conv_silu, kda_stream_t stream);
 
 /*
  * Chunked prefill whose states live in a pool of slots (the prefill side of

@@ -233,6 +233,8 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     a.conv_width = a.conv_w ? desc->conv_width : 0;
     a.conv_silu = a.conv_w ? desc->conv_silu : 0;
     a.gate = fused ? fused->gate : nullptr;
+    a.conv_in = a.conv_w && a.conv_width > 1 ? fused->conv_in : nullptr;
+    a.conv_out = a.conv_w && a.conv_width > 1 ? fused->conv_out : nullptr;
     a.stream = (cudaStream_t)stream;
 
     cudaError_t e;
@@ -246,6 +248,7 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
     if ((e = kda::launch_prefill_simt(a)) != cudaSuccess)
         return fail(KDA_ERR_CUDA, "prefill kernels: %s", cudaGetErrorString(e));
+    if (a.conv_out && (e = kda::launch_conv_tail(a)) != cudaSuccess) return cuda_fail(e, "convolution state");
     return KDA_OK;
 }
 }  // namespace kda
@@ -266,11 +269,14 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
 kda_status kda_prefill_fused(const void *q, const void *k, const void *v, const float *g,
                              const float *beta, const float *init_state, const int32_t *cu_seqlens,
                              void *out, float *final_state, float *ckpts, const float *conv_w,
-                             const void *gate, const kda_prefill_desc *desc, void *workspace,
-                             size_t workspace_bytes, kda_stream_t stream)
+                             const void *conv_state_in, void *conv_state_out, const void *gate,
+                             const kda_prefill_desc *desc, void *workspace, size_t workspace_bytes,
+                             kda_stream_t stream)
 {
     NvtxRange r("kda_prefill_fused");
-    const kda::FusedArgs fused{conv_w, gate};
+    if (!conv_w && (conv_state_in || conv_state_out))
+        return fail(KDA_ERR_INVALID_ARG, "a convolution state is given without conv_w");
+    const kda::FusedArgs fused{conv_w, gate, conv_state_in, conv_state_out};
     return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc, workspace,
                              workspace_bytes, stream, true, nullptr, &fused);
 }
@@ -341,6 +347,34 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
     NvtxRange r("kda_decode");
     return decode_common(q, k, v, g, beta, state, nullptr, 0, 1, nullptr, out, N, H, Dk, Dv, dtype, nullptr,
                          stream);
+}
+
+kda_status kda_decode_fused(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float *state, void *conv_state, const float *conv_w,
+                            const void *gate, void *out, int32_t N, int32_t H, int32_t Dk, int32_t Dv,
+                            kda_dtype dtype, int32_t conv_width, int32_t conv_silu, kda_stream_t stream)
+{
+    NvtxRange r("kda_decode_fused");
+    if (conv_w && (conv_width < 1 || conv_width > kda::kConvTaps))
+        return fail(KDA_ERR_UNSUPPORTED, "conv_width %d not in [1, %d]", conv_width, kda::kConvTaps);
+    if (conv_silu != 0 && conv_silu != 1) return fail(KDA_ERR_INVALID_ARG, "conv_silu must be 0 or 1");
+    if (!conv_w && conv_state) return fail(KDA_ERR_INVALID_ARG, "conv_state given without conv_w");
+    if (N < 0 || H < 0) return fail(KDA_ERR_INVALID_ARG, "N and H must be >= 0");
+    if ((int64_t)N * H > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "N*H too large");
+    if (Dk != Dv) return fail(KDA_ERR_UNSUPPORTED, "Dk (%d) != Dv (%d)", Dk, Dv);
+    if (Dk != 64 && Dk != 128) return fail(KDA_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", Dk);
+    if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32)
+        return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if ((size_t)N * H == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !out)
+        return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta, state and out must be non-NULL");
+    if (((uintptr_t)state & 15) != 0) return fail(KDA_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    if (out == q || out == k || out == v || out == (void *)state || (gate && out == gate))
+        return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
+    const kda::DecodeFused f{conv_w, conv_w ? conv_width : 0, conv_silu, conv_w ? conv_state : nullptr, gate};
+    cudaError_t e = kda::launch_decode_fused(q, k, v, g, beta, state, out, N, H, Dk, dtype, f, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    return KDA_OK;
 }
 
 kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,

@@ -21,12 +21,23 @@
 namespace kda {
 namespace {
 
-template <int D, typename T, int THREADS, bool MULTI>
+// FUSED (single token, dense states): q, k, v pass through the short
+// convolution with the sequence's history (conv_state, then advanced by the
+// new raw rows) before the step, and the output through o * sigmoid(gate).
+struct FusedIO {
+    const float *conv_w;   // [3, W, H, D] or NULL
+    int W, silu;
+    void *conv_state;      // [N, 3, W - 1, H, D] of T, or NULL (zero history, nothing kept)
+    const void *gate;      // [N, H, D] of T, or NULL
+};
+
+template <int D, typename T, int THREADS, bool MULTI, bool FUSED = false>
 __global__ void __launch_bounds__(THREADS)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
-              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status)
+              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status,
+              FusedIO fz = FusedIO{})
 {
     const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
@@ -82,11 +93,43 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     for (int t = 0; t < m; ++t) {
         const size_t tok = (n * m + t) * H + hh;   // token-head row of q, k, v, g, beta, out
         // Token vectors and the two L2 norms (fp32).
-        float qv = 0.f, kv = 0.f;
+        float qv = 0.f, kv = 0.f, vconv = 0.f;
         if (tid < D) {
             qv = to_f32(q[tok * D + tid]);
             kv = to_f32(k[tok * D + tid]);
             sh_a[tid] = expf(g[tok * D + tid]);
+            if constexpr (FUSED) {
+                if (fz.conv_w) {
+                    // x' = sum_{i < W-1} w[i] history[i] + w[W-1] x, then the history
+                    // advances by the raw row (each thread owns its column of it)
+                    T *cs = reinterpret_cast<T *>(fz.conv_state);
+                    const float vraw = to_f32(v[tok * D + tid]);
+                    float xs[3] = {qv, kv, vraw};
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        float acc = fz.conv_w[(((size_t)t * fz.W + fz.W - 1) * H + hh) * D + tid] * xs[t];
+                        float hist[3];
+                        for (int i = 0; i < fz.W - 1; ++i) {
+                            hist[i] = cs ? to_f32(cs[((((size_t)n * 3 + t) * (fz.W - 1) + i) * H + hh) * D + tid]) : 0.f;
+                            acc += fz.conv_w[(((size_t)t * fz.W + i) * H + hh) * D + tid] * hist[i];
+                        }
+                        if (cs) {
+                            for (int i = 0; i + 1 < fz.W - 1; ++i)
+                                cs[((((size_t)n * 3 + t) * (fz.W - 1) + i) * H + hh) * D + tid] = from_f32<T>(hist[i + 1]);
+                            if (fz.W > 1)
+                                cs[((((size_t)n * 3 + t) * (fz.W - 1) + fz.W - 2) * H + hh) * D + tid] =
+                                    t == 0 ? q[tok * D + tid] : t == 1 ? k[tok * D + tid] : v[tok * D + tid];
+                        }
+                        if (fz.silu) acc = acc / (1.f + expf(-acc));
+                        xs[t] = acc;
+                    }
+                    qv = xs[0];
+                    kv = xs[1];
+                    vconv = xs[2];
+                } else {
+                    vconv = to_f32(v[tok * D + tid]);
+                }
+            }
         }
         float pq = warp_sum(qv * qv), pk = warp_sum(kv * kv), pqk = warp_sum(qv * kv);
         if ((tid & 31) == 0) {
@@ -133,10 +176,13 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
                 sk += rk_[r * D + tid];
                 sq += rq_[r * D + tid];
             }
-            const float u = to_f32(v[tok * D + tid]) - sk;
+            const float u = (FUSED ? vconv : to_f32(v[tok * D + tid])) - sk;
             sh_u[tid] = u;
             const float kq = nqk * rq * rk;   // kh . qh
-            out[tok * D + tid] = from_f32<T>(sq + b * kq * u);
+            float o = sq + b * kq * u;
+            if constexpr (FUSED)
+                if (fz.gate) o /= 1.f + expf(-to_f32(reinterpret_cast<const T *>(fz.gate)[tok * D + tid]));
+            out[tok * D + tid] = from_f32<T>(o);
         }
         __syncthreads();
 
@@ -178,6 +224,30 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 }
 
 }  // namespace
+
+template <int D, typename T>
+cudaError_t launch_fused_t(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                           float *state, void *out, int N, int H, const DecodeFused &f, cudaStream_t st)
+{
+    constexpr int THREADS = (D == 128) ? 256 : 128;
+    const FusedIO fz{f.conv_w, f.conv_width, f.conv_silu, f.conv_state, f.gate};
+    decode_kernel<D, T, THREADS, false, true><<<(unsigned)((size_t)N * H), THREADS, 0, st>>>(
+        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, nullptr, H, 0, 1, nullptr, nullptr, fz);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fused(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float *state, void *out, int N, int H, int D,
+                                kda_dtype dtype, const DecodeFused &f, cudaStream_t stream)
+{
+    if ((size_t)N * H == 0) return cudaSuccess;
+    if (D == 128)
+        return dtype == KDA_DTYPE_BF16
+                   ? launch_fused_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, stream)
+                   : launch_fused_t<128, float>(q, k, v, g, beta, state, out, N, H, f, stream);
+    return dtype == KDA_DTYPE_BF16 ? launch_fused_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, stream)
+                                   : launch_fused_t<64, float>(q, k, v, g, beta, state, out, N, H, f, stream);
+}
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,

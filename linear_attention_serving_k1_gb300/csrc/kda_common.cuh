@@ -110,6 +110,10 @@ struct PrefillArgs {
     const float *conv_w;
     int conv_width, conv_silu;
     const void *gate;
+    // convolution state [N, 3, conv_width - 1, H, D] (dtype of q): the rows before
+    // each sequence (NULL: zeros) and, written at the end of the call, after it
+    const void *conv_in;
+    void *conv_out;
     cudaStream_t stream;
 };
 
@@ -170,6 +174,8 @@ struct PoolArgs {
 struct FusedArgs {
     const float *conv_w;
     const void *gate;
+    const void *conv_in;
+    void *conv_out;
 };
 // Taps of the short convolution as the kernels apply it (narrower
 // convolutions are padded with zero taps on the older side).
@@ -190,6 +196,8 @@ constexpr uint32_t kDefaultWaitLimit = 1u << 22;
 kda_status fail_with_message(kda_status s, const char *fmt, ...);
 
 cudaError_t launch_seq_table(const PrefillArgs &a);
+// Writes the convolution state after each sequence (a.conv_out), last in a call.
+cudaError_t launch_conv_tail(const PrefillArgs &a);
 cudaError_t launch_prefill_simt(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a);
 // The whole tensor-core call (status reset, sequence table, K1/K2 segments) on
@@ -202,5 +210,16 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
                           const int32_t *commit, int32_t *status, cudaStream_t stream);
+// The fused decode step (kda_decode_fused): convolution with a per-sequence
+// history, the step, the output gate.
+struct DecodeFused {
+    const float *conv_w;   // [3, W, H, D] or NULL
+    int conv_width, conv_silu;
+    void *conv_state;      // [N, 3, W - 1, H, D] dtype, read and advanced (NULL: zeros, not kept)
+    const void *gate;      // [N, H, D] dtype or NULL
+};
+cudaError_t launch_decode_fused(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float *state, void *out, int N, int H, int D,
+                                kda_dtype dtype, const DecodeFused &f, cudaStream_t stream);
 
 }  // namespace kda

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads)
 k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, int N, int H,
                SeqTable tab, float *__restrict__ handoff, int scalar_gate, DevStatus *st,
-               const float *__restrict__ conv_w, int conv_width, int conv_silu)
+               const float *__restrict__ conv_w, int conv_width, int conv_silu, const T *__restrict__ conv_in)
 {
     constexpr int P = D + 1;   // padded row pitch (bank-conflict free columns)
     extern __shared__ float smem[];
@@ -129,8 +129,11 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
         float acc = 0.f;
         for (int i = 0; i < conv_width; ++i) {
             const int tau = t0 + r - (conv_width - 1) + i;
+            const float wi = conv_w[(((size_t)t * conv_width + i) * H + h) * D + d];
             if (tau >= seq_t0)
-                acc += conv_w[(((size_t)t * conv_width + i) * H + h) * D + d] * to_f32(x[((size_t)tau * H + h) * D + d]);
+                acc += wi * to_f32(x[((size_t)tau * H + h) * D + d]);
+            else if (conv_in)   // the history before the sequence (oldest first)
+                acc += wi * to_f32(conv_in[((((size_t)n * 3 + t) * (conv_width - 1) + (conv_width - 1 + tau - seq_t0)) * H + h) * D + d]);
         }
         return conv_silu ? acc / (1.f + expf(-acc)) : acc;
     };
@@ -371,7 +374,8 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
         dim3 g1((unsigned)a.max_chunks, (unsigned)a.H);
         k1_simt_kernel<D, T><<<g1, kThreads, sm1, a.stream>>>(
             (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.N, a.H, a.tab,
-            (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status, a.conv_w, a.conv_width, a.conv_silu);
+            (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status, a.conv_w, a.conv_width, a.conv_silu,
+            (const T *)a.conv_in);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned g2 = (unsigned)((size_t)a.N * a.H * (D / kBV));
@@ -383,6 +387,48 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
 }  // namespace
 
 size_t simt_handoff_bytes_per_chunk(int D, int /*C*/) { return sizeof(float) * handoff_floats(D); }
+
+// The convolution state after each sequence: its last W - 1 raw q, k, v rows
+// (oldest first), reaching into the history before it when the sequence is
+// shorter.  One CTA per (sequence, head); each thread owns whole columns
+// (tensor, channel) and reads them before writing, so the output may be the
+// history buffer itself.
+template <typename T>
+__global__ void conv_tail_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                                 const T *conv_in, T *conv_out, int N, int H, int D, int W, SeqTable tab)
+{
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const int len = tab.cu[n + 1] - tab.cu[n];
+    for (int col = threadIdx.x; col < 3 * D; col += blockDim.x) {
+        const int t = col / D, c = col % D;
+        const T *x = t == 0 ? q : t == 1 ? k : v;
+        T vals[kConvTaps - 1];
+        for (int j = 0; j < W - 1; ++j) {
+            const int p = len - (W - 1) + j;   // position in the sequence
+            if (p >= 0) vals[j] = x[((size_t)(tab.cu[n] + p) * H + h) * D + c];
+            else if (conv_in)
+                vals[j] = conv_in[((((size_t)n * 3 + t) * (W - 1) + (W - 1 + p)) * H + h) * D + c];
+            else vals[j] = from_f32<T>(0.f);
+        }
+        for (int j = 0; j < W - 1; ++j) conv_out[((((size_t)n * 3 + t) * (W - 1) + j) * H + h) * D + c] = vals[j];
+    }
+}
+
+cudaError_t launch_conv_tail(const PrefillArgs &a)
+{
+    if (a.conv_width <= 1) return cudaSuccess;
+    const unsigned grid = (unsigned)((size_t)a.N * a.H);
+    if (a.dtype == KDA_DTYPE_BF16)
+        conv_tail_kernel<__nv_bfloat16><<<grid, 128, 0, a.stream>>>(
+            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v,
+            (const __nv_bfloat16 *)a.conv_in, (__nv_bfloat16 *)a.conv_out, a.N, a.H, a.D, a.conv_width, a.tab);
+    else
+        conv_tail_kernel<float><<<grid, 128, 0, a.stream>>>((const float *)a.q, (const float *)a.k,
+                                                             (const float *)a.v, (const float *)a.conv_in,
+                                                             (float *)a.conv_out, a.N, a.H, a.D, a.conv_width,
+                                                             a.tab);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_seq_table(const PrefillArgs &a)
 {

@@ -193,7 +193,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
              DevStatus *st, uint32_t wait_limit, const float *__restrict__ conv_w, int conv_width,
-             int conv_silu)
+             int conv_silu, const bf16 *__restrict__ conv_in)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar, qbar, dbar;
@@ -322,10 +322,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 w[i] = *reinterpret_cast<const float2 *>(taps + (t * kConvTaps + i) * kD + cp);
                 // window slots 1 .. 3 start with rows r0 - 3 .. r0 - 1 (slot 0 is
                 // shifted out before first use); each step shifts and appends a row
-                const int rr = r0 - kConvTaps + i;
-                const bool valid = i > 0 && rr < L && lc * kC + rr >= 0;
-                const uint32_t u = valid ? __ldg(reinterpret_cast<const unsigned int *>(
-                                               src + (ptrdiff_t)rr * (ptrdiff_t)rstride + cp)) : 0u;
+                const int rr = r0 - kConvTaps + i, pos = lc * kC + rr;   // position in the sequence
+                uint32_t u = 0u;
+                if (i > 0 && pos >= 0)
+                    u = __ldg(reinterpret_cast<const unsigned int *>(src + (ptrdiff_t)rr * (ptrdiff_t)rstride + cp));
+                else if (i > 0 && conv_in && pos >= -(conv_width - 1))   // the history before the sequence
+                    u = __ldg(reinterpret_cast<const unsigned int *>(
+                        conv_in + ((((size_t)n * 3 + t) * (conv_width - 1) + (conv_width - 1 + pos)) * H + h) * kD + cp));
                 win[i] = make_float2(bf_lo(u), bf_hi(u));
             }
 #pragma unroll 4
@@ -1411,7 +1414,8 @@ cudaError_t enqueue_prefill_tc(PrefillArgs a, cudaStream_t stream)
     cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     if ((e = launch_seq_table(a)) != cudaSuccess) return e;
-    return launch_prefill_tc(a);
+    if ((e = launch_prefill_tc(a)) != cudaSuccess) return e;
+    return a.conv_out ? launch_conv_tail(a) : cudaSuccess;
 }
 
 cudaError_t launch_prefill_tc_graph(const PrefillArgs &a)
@@ -1494,11 +1498,11 @@ void launch_k1(const PrefillArgs &a, unsigned grid, cudaStream_t stream, uint8_t
     if (a.conv_w)
         k1_tc_kernel<true><<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu);
+            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in);
     else
         k1_tc_kernel<false><<<grid, K1_THREADS, K1_SMEM, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, nullptr, 0, 0);
+            a.wait_limit, nullptr, 0, 0, nullptr);
 }
 // One K2 launch (one chain per CTA or chains in turn; with or without the gate).
 void launch_k2(const PrefillArgs &a, bool multi, unsigned grid, cudaStream_t stream, const uint8_t *ring, int lo,

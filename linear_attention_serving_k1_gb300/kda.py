@@ -22,8 +22,8 @@ DTYPE_BF16, DTYPE_FP32 = 0, 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_prefill_workspace_size", "kda_prefill_launch_count", "kda_prefill", "kda_prefill_status",
-           "kda_prefill_pooled", "kda_prefill_fused", "kda_decode", "kda_decode_paged", "kda_decode_multi",
-           "kda_prefill_noalloc", "kda_last_error", "kda_version")
+           "kda_prefill_pooled", "kda_prefill_fused", "kda_decode", "kda_decode_fused", "kda_decode_paged",
+           "kda_decode_multi", "kda_prefill_noalloc", "kda_last_error", "kda_version")
 
 # Size of the library's built-in scratch array used by kda_prefill_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -70,7 +70,9 @@ def load_library(path: Optional[str] = None):
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode.argtypes = [_vp] * 7 + [ctypes.c_int32] * 5 + [_vp]
     lib.kda_prefill_fused.restype = ctypes.c_int
-    lib.kda_prefill_fused.argtypes = [_vp] * 12 + [ctypes.POINTER(PrefillDesc), _vp, ctypes.c_size_t, _vp]
+    lib.kda_prefill_fused.argtypes = [_vp] * 14 + [ctypes.POINTER(PrefillDesc), _vp, ctypes.c_size_t, _vp]
+    lib.kda_decode_fused.restype = ctypes.c_int
+    lib.kda_decode_fused.argtypes = [_vp] * 10 + [ctypes.c_int32] * 7 + [_vp]
     lib.kda_prefill_pooled.restype = ctypes.c_int
     lib.kda_prefill_pooled.argtypes = [_vp] * 8 + [ctypes.c_int64, _vp, _vp, _vp, ctypes.POINTER(PrefillDesc),
                                                    _vp, ctypes.c_size_t, _vp]
@@ -215,11 +217,13 @@ def prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_s
 
 
 def prefill_fused(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, conv_w=None, conv_silu: bool = False,
-                  gate=None, num_seqs: Optional[int] = None, chunk: int = 64, ckpt_stride: int = 0, ckpts=None,
-                  ckpt_capacity: Optional[int] = None, out=None, final_state=None, workspace=None, stream=None,
-                  max_seq_len: int = 0, segment_chunks: int = 0):
+                  gate=None, conv_state_in=None, conv_state_out=None, num_seqs: Optional[int] = None,
+                  chunk: int = 64, ckpt_stride: int = 0, ckpts=None, ckpt_capacity: Optional[int] = None, out=None,
+                  final_state=None, workspace=None, stream=None, max_seq_len: int = 0, segment_chunks: int = 0):
     """``kda_prefill_fused``: the prefill with the short convolution of q, k, v
-    (taps ``conv_w`` [3, W, H, D] fp32, W <= 4, optional SiLU) before the
+    (taps ``conv_w`` [3, W, H, D] fp32, W <= 4, optional SiLU; history
+    ``conv_state_in`` [N, 3, W - 1, H, D] or None for zeros; the state after
+    each sequence written to ``conv_state_out`` when given) before the
     recurrence and the output gate ``out = o * sigmoid(gate)`` (``gate``
     [T, H, Dv], the dtype of q) after it.  Returns (out, final_state, ckpts)."""
     T, H, D = q.shape
@@ -240,7 +244,8 @@ def prefill_fused(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, conv_w=
         workspace = alloc_workspace(desc, dev)
     code = load_library().kda_prefill_fused(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
-        _ptr(final_state), _ptr(ckpts), _ptr(conv_w), _ptr(gate), ctypes.byref(desc), _ptr(workspace),
+        _ptr(final_state), _ptr(ckpts), _ptr(conv_w), _ptr(conv_state_in), _ptr(conv_state_out), _ptr(gate),
+        ctypes.byref(desc), _ptr(workspace),
         ctypes.c_size_t(workspace.numel()), _stream(stream))
     _check(code)
     return out, final_state, ckpts
@@ -285,6 +290,23 @@ def decode(q, k, v, g, beta, state, out=None, stream=None):
         out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
     code = load_library().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                                      _ptr(out), N, H, D, v.shape[2], _dtype_code(q), _stream(stream))
+    _check(code)
+    return out
+
+
+def decode_fused(q, k, v, g, beta, state, *, conv_w=None, conv_silu: bool = False, conv_state=None, gate=None,
+                 out=None, stream=None):
+    """One decode step through ``kda_decode_fused``: q, k, v [N, H, D]
+    convolved with the history ``conv_state`` [N, 3, W - 1, H, D] (advanced in
+    place; None: zeros), the step on ``state`` [N, H, D, D] (in place), the
+    output gated by ``gate`` [N, H, D] (None: none)."""
+    N, H, D = q.shape
+    if out is None:
+        out = torch.empty(N, H, v.shape[2], dtype=q.dtype, device=q.device)
+    W = int(conv_w.shape[1]) if conv_w is not None else 0
+    code = load_library().kda_decode_fused(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(conv_state), _ptr(conv_w), _ptr(gate),
+        _ptr(out), N, H, D, v.shape[2], _dtype_code(q), W, int(bool(conv_silu)), _stream(stream))
     _check(code)
     return out
 

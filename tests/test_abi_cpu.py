@@ -172,13 +172,21 @@ def test_fused_and_pooled_reject_before_launch(lib):
     ws = lib.kda_prefill_workspace_size(ctypes.byref(d))
     o = ctypes.c_void_p(8192)
     # taps given without a width
-    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, p, None, ctypes.byref(d),
+    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, p, None, None, None, ctypes.byref(d),
                                  ctypes.c_void_p(1 << 20), ws, None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
+    # a convolution state without taps
+    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, None, p, None, None, ctypes.byref(d),
+                                 ctypes.c_void_p(1 << 20), ws, None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
+    # fused decode: width out of range, state without taps
+    assert lib.kda_decode_fused(p, p, p, p, p, p, None, p, None, o, 2, 2, 128, 128, kda.DTYPE_BF16, 5, 0,
+                                None) == kda.STATUS_CODES["KDA_ERR_UNSUPPORTED"]
+    assert lib.kda_decode_fused(p, p, p, p, p, p, p, None, None, o, 2, 2, 128, 128, kda.DTYPE_BF16, 0, 0,
+                                None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
     # width beyond the supported four taps
     d5 = _desc(T=128, H=2, D=128, dtype_code=kda.DTYPE_BF16, conv_width=5)
     assert lib.kda_prefill_workspace_size(ctypes.byref(d5)) == 0
     # the gate may not alias the output
-    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, None, o, ctypes.byref(d),
+    assert lib.kda_prefill_fused(p, p, p, p, p, None, None, o, None, None, None, None, None, o, ctypes.byref(d),
                                  ctypes.c_void_p(1 << 20), ws, None) == kda.STATUS_CODES["KDA_ERR_INVALID_ARG"]
     # pooled: slot tables without a pool; checkpoints without their slot table
     assert lib.kda_prefill_pooled(p, p, p, p, p, None, o, None, ctypes.c_int64(4), p, None, None,
