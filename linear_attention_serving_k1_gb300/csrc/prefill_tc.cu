@@ -159,11 +159,14 @@ constexpr int K1_XWP = 36;               // its row pitch (conflict-free float4 
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
+constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (16 KB), back from the record over T
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
+static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16384 <= K1_XS, "Qg tile between Wk^T and the merge scratch");
 static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
+constexpr int kH32 = 32;                 // head count with its own K1 instance
 
 // TMEM columns (256 allocated)
 constexpr uint32_t T1_G = 0, T1_W1 = 64, T1_W2 = 128, T1_AP = 0, T1_QP = 128;
@@ -187,7 +190,9 @@ constexpr uint32_t K1_TAPS_BYTES = 3 * kConvTaps * kD * 4;
 // two CTAs per SM with the taps: dynamic + static (3 KB) + the 1 KB the SM reserves per CTA
 static_assert(2 * (K1_SMEM + K1_TAPS_BYTES + 3072 + 1024) <= 228 * 1024, "two CTAs per SM with the taps");
 
-template <bool kConv>   // true: q, k, v pass through the short convolution as they are loaded
+// kConv: q, k, v pass through the short convolution as they are loaded.  kH > 0:
+// the call has kH heads (row strides and head indices fold into constants).
+template <bool kConv, int kH>
 __global__ void __launch_bounds__(K1_THREADS, 2)
 k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
@@ -195,8 +200,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
              DevStatus *st, uint32_t wait_limit, const float *__restrict__ conv_w, int conv_width,
              int conv_silu, const bf16 *__restrict__ conv_in)
 {
+    if constexpr (kH > 0) H = kH;
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t mbar, qbar, dbar;
+    __shared__ uint64_t mbar, qbar, abar, dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
     // (16-byte aligned: read as float2 / float4)
@@ -373,6 +379,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     if (tid == 0) {
         mbar_init(&mbar, 1);
         mbar_init(&qbar, 1);
+        mbar_init(&abar, 1);
         mbar_init(&dbar, 1);
         fence_mbar_init();
     }
@@ -728,12 +735,19 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
 
     // Ke'^T and Mc', already K2's operand tiles, go to the record by bulk copies
-    // (waited for before the CTA exits; neither tile is overwritten)
+    // (waited for before the CTA exits; neither tile is overwritten), and the
+    // parked Qg'^T tile comes back over T, free now that the inverse is done
+    bool q_issued = false;   // (thread 0) the copy is in flight until qbar completes
     if (tid == 0) {
         static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
         bulk_s2g(rec + REC_KM, sm + K1_KET, 16384);
         bulk_s2g(rec + REC_MC, sm + K1_MC, 8192);
         bulk_commit();
+        if (ok) {
+            mbar_arrive_expect_tx(&qbar, 16384);
+            bulk_g2s(sm + K1_QG, qg_park, 16384, &qbar);
+            q_issued = true;
+        }
     }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
@@ -749,19 +763,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
-    __syncthreads();
-    fence_after_sync();
-    ok = ok && wflag[2];
-
-    // the Kg'^T tile is dead: the parked Qg'^T tile comes back into its place
-    bool q_issued = false;   // (thread 0) the copy is in flight until qbar completes
-    if (tid == 0 && ok) {
-        mbar_arrive_expect_tx(&qbar, 16384);
-        bulk_g2s(sm + K1_KGT, qg_park, 16384, &qbar);
-        q_issued = true;
-    }
-    // diag(rq) as an f16 operand tile (rows i, K = r; 64 x 64) for Q' = diag(rq) Qg' - Mc Wk
+    // diag(rq) as an f16 operand tile (rows i, K = r; 64 x 64) for Q' = diag(rq) Qg' - Mc Wk,
+    // while the products run (the merge scratch it overwrites is dead)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int idx = tid + K1_THREADS * h, i = idx >> 3, kg = idx & 7;
@@ -770,6 +773,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         for (int j = 0; j < 8; ++j) dv[j] = (8 * kg + j == i) ? rq[i] : 0.f;
         *reinterpret_cast<uint4 *>(sm + K1_RQD + kmaj_off(i, 8 * kg, LBO_KIN, SBO_K64)) = pack_f16x8(dv);
     }
+    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
+    __syncthreads();
+    fence_after_sync();
+    ok = ok && wflag[2];
+
     // 8. (-diag(rk) Wk)^T -> smem operand and (diag(rk) Uv)^T -> record (rows d / e, K = r).
     //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
     if (ok) {
@@ -806,60 +814,67 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64); -Mc Wk = -Mc' diag(rk) Wk (M = 64, N = 128, K = 64)
+    // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64), committed on its own so
+    //    that its readout overlaps the second product; -Mc Wk = -Mc' diag(rk) Wk
+    //    (M = 64, N = 128, K = 64) plus diag(rq) Qg' (K = 64) into Q'
     bool q_landed = false;
     if (tid == 0 && ok && (q_landed = mbar_wait_bounded(&qbar, 0, wait_limit))) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
-        const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_KGT);
+        const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_QG);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = make_desc(bw + ks * 256, LBO_KIN, SBO_K64);
-            mma_f16(tm + T1_AP, make_desc(ake + ks * 256, LBO_KIN, SBO_K64), bd, id128, ks > 0);
-            mma_f16(tm + T1_QP, make_desc(amc + ks * 256, LBO_KIN, SBO_K64), bd, id64, ks > 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tm + T1_AP, make_desc(ake + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(bw + ks * 256, LBO_KIN, SBO_K64), id128, ks > 0);
+        mma_commit(&abar);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tm + T1_QP, make_desc(amc + ks * 256, LBO_KIN, SBO_K64),
+                    make_desc(bw + ks * 256, LBO_KIN, SBO_K64), id64, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             mma_f16(tm + T1_QP, make_desc(ard + ks * 256, LBO_KIN, SBO_K64),
                     make_desc(bq + ks * 256, LBO_KIN, SBO_K64), id64, 1);
         mma_commit(&mbar);
     }
-    if (tid == 0) wflag[3] = ok && q_landed && mbar_wait_bounded(&mbar, 1, wait_limit);
+    if (tid == 0) wflag[3] = ok && q_landed && mbar_wait_bounded(&abar, 0, wait_limit);
     __syncthreads();
     fence_after_sync();
     ok = ok && wflag[3];
 
+    // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64), all four
+    //     16-column loads in flight before one wait
+    if (ok) {
+        float a[4][16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_AP + 64 * ch + 16 * q, a[q]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int h8 = 0; h8 < 16; h8 += 8)
+                *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
+                    pack_f16x8(a[q] + h8);
+    }
+    if (tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
+    __syncthreads();
+    fence_after_sync();
+    ok = ok && wflag[0];
+    // 11. Q' -> record: the M = 64 accumulator puts row r = 16 q4 + l in lane
+    //     32 q4 + l (l < 16)
     if (ok) {
         const int r = 16 * q4 + lane;
-        // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64), all
-        //     four 16-column loads in flight before one wait
-        {
-            float a[4][16];
+        float a[4][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_AP + 64 * ch + 16 * q, a[q]);
-            tmem_ld_wait();
+        for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_QP + 64 * ch + 16 * q, a[q]);
+        tmem_ld_wait();
+        if (lane < 16) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8)
-                    *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
+                    *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
                         pack_f16x8(a[q] + h8);
-        }
-        // 11. Q' -> record: the M = 64 accumulator puts row r = 16 q4 + l in lane
-        //     32 q4 + l (l < 16)
-        {
-            float a[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_QP + 64 * ch + 16 * q, a[q]);
-            tmem_ld_wait();
-            if (lane < 16) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int h8 = 0; h8 < 16; h8 += 8)
-                        *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
-                            pack_f16x8(a[q] + h8);
-            }
         }
     }
     if (!ok && tid == 0) {
@@ -1377,11 +1392,15 @@ cudaError_t tc_kernel_attributes()
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(k1_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k1_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(K1_SMEM + K1_TAPS_BYTES));
-        if (e != cudaSuccess) return e;
+        const void *k1s[] = {(const void *)k1_tc_kernel<false, 0>, (const void *)k1_tc_kernel<false, kH32>};
+        for (const void *f : k1s)
+            if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K1_SMEM)) != cudaSuccess)
+                return e;
+        const void *k1c[] = {(const void *)k1_tc_kernel<true, 0>, (const void *)k1_tc_kernel<true, kH32>};
+        for (const void *f : k1c)
+            if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)(K1_SMEM + K1_TAPS_BYTES))) != cudaSuccess)
+                return e;
         const void *k2s[] = {(const void *)k2_tc_kernel<false, false>, (const void *)k2_tc_kernel<true, false>,
                              (const void *)k2_tc_kernel<false, true>, (const void *)k2_tc_kernel<true, true>};
         for (const void *f : k2s)
@@ -1495,12 +1514,13 @@ void launch_k1(const PrefillArgs &a, unsigned grid, cudaStream_t stream, uint8_t
                int slot)
 {
     const bf16 *q = (const bf16 *)a.q, *k = (const bf16 *)a.k, *v = (const bf16 *)a.v;
+    const bool h32 = a.H == kH32;   // the common head count: strides fold into constants
     if (a.conv_w)
-        k1_tc_kernel<true><<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
+        (h32 ? k1_tc_kernel<true, kH32> : k1_tc_kernel<true, 0>)<<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
             a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in);
     else
-        k1_tc_kernel<false><<<grid, K1_THREADS, K1_SMEM, stream>>>(
+        (h32 ? k1_tc_kernel<false, kH32> : k1_tc_kernel<false, 0>)<<<grid, K1_THREADS, K1_SMEM, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
             a.wait_limit, nullptr, 0, 0, nullptr);
 }
@@ -1539,7 +1559,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         if (a.max_chunks > 0) {
             launch_k1(a, (unsigned)((size_t)a.max_chunks * a.H), a.stream, ring, 0, 0, 0, 0);
             if ((e = cudaGetLastError()) != cudaSuccess) {
-                note_launch_failure(k1_tc_kernel<false>, "K1", K1_THREADS, K1_SMEM);
+                note_launch_failure(k1_tc_kernel<false, 0>, "K1", K1_THREADS, K1_SMEM);
                 return e;
             }
         }
@@ -1561,7 +1581,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
         if (s >= p.R && (e = cudaStreamWaitEvent(a.stream, c->k2[slot], 0)) != cudaSuccess) break;
         launch_k1(a, k1_grid, a.stream, ring, lo, cnt, p.G, slot);
         if ((e = cudaGetLastError()) != cudaSuccess) {
-            note_launch_failure(k1_tc_kernel<false>, "K1", K1_THREADS, K1_SMEM);
+            note_launch_failure(k1_tc_kernel<false, 0>, "K1", K1_THREADS, K1_SMEM);
             break;
         }
         if ((e = cudaEventRecord(c->k1[slot], a.stream)) != cudaSuccess) break;

@@ -210,13 +210,15 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// Rounds a finite fp32 value to the nearest tf32 (10 explicit mantissa bits,
-// ties away from zero) on its bit pattern: half a tf32 unit is added to the
-// magnitude bits and the 13 bits below the tf32 mantissa are cleared (a carry
-// into the exponent gives the next binade, as rounding should).
+// Prepares a finite fp32 value as a tf32 tensor-core operand rounded to the
+// nearest tf32 (10 explicit mantissa bits, ties away from zero): the tensor
+// core reads the upper 19 bits of a tf32 operand and ignores the 13 below, so
+// adding half a tf32 unit to the magnitude bits turns that truncation into
+// rounding (a carry into the exponent gives the next binade, as rounding
+// should).  One integer add instead of an add and a mask.
 __device__ __forceinline__ float round_tf32(float x)
 {
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
 }
 
 // Arrives once on `bar` when every MMA this thread issued before has completed.
