@@ -142,9 +142,14 @@ constexpr uint32_t K1_F32_SBO = 16 * K1_F32_LBO;       // 8-row group stride (K 
 constexpr uint32_t K1_GA = 0;                          // tf32 [Kg'; Qg']: rows 128 x K = 64 channels
 constexpr uint32_t K1_KD = K1_GA + 16 * K1_F32_SBO;    // tf32 Kd': rows 64 x K = 64 channels
 constexpr uint32_t K1_GRAM_END = K1_KD + 8 * K1_F32_SBO;
-constexpr uint32_t K1_KGT = K1_GRAM_END;               // f16 Kg'^T: rows d (128) x K = i (64)
-constexpr uint32_t K1_VT = K1_KGT + 16384;             // f16 V^T  : rows e x K = i
-constexpr uint32_t K1_KET = K1_VT + 16384;             // f16 Ke'^T: rows d x K = r
+// Kg'^T and V^T stay in shared memory, so their 8-row groups are padded by 16
+// bytes: lanes whose rows d lie 8 apart then hit different banks and a warp
+// stores one channel of its pairs at a time without conflicts.  Ke'^T keeps
+// the record's layout (it is copied there as a whole).
+constexpr uint32_t SBO_K64P = SBO_K64 + 16;
+constexpr uint32_t K1_KGT = K1_GRAM_END;               // f16 Kg'^T: rows d (128) x K = i (64), SBO_K64P
+constexpr uint32_t K1_VT = K1_KGT + 16 * SBO_K64P;     // f16 V^T  : rows e x K = i, SBO_K64P
+constexpr uint32_t K1_KET = K1_VT + 16 * SBO_K64P;     // f16 Ke'^T: rows d x K = r
 constexpr uint32_t K1_SMEM = K1_KET + 16384;
 // later phases, inside [0, K1_GRAM_END)
 constexpr int K1_P = 68;                 // fp32 row pitch of T (16-byte aligned rows)
@@ -204,7 +209,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t mbar, qbar, abar, dbar;
     __shared__ uint32_t tmem_sh;
-    __shared__ float tot[8][64];       // per warp: totals of g over its 8 rows, per channel of the half
+    __shared__ __align__(16) float tot[8][64];   // per warp: totals of g over its 8 rows, per channel of the half
     // (16-byte aligned: read as float2 / float4)
     __shared__ __align__(16) float rq[kC];
     __shared__ __align__(16) float rk[kC];
@@ -398,25 +403,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     for (int p = 0; p < 2; ++p) {
         const int d = 64 * p + 2 * lane;
         {
-            float c0 = 0.f, c1 = 0.f;
+            float2 c = gv[0];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) { c0 += gv[j].x; c1 += gv[j].y; }
-            tot[warp][2 * lane] = c0;
-            tot[warp][2 * lane + 1] = c1;
+            for (int j = 1; j < 8; ++j) c = __fadd2_rn(c, gv[j]);
+            *reinterpret_cast<float2 *>(&tot[warp][2 * lane]) = c;
         }
         // the MMA of the previous half has read the operand tiles
         if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (p == 0 && tid < kC) bs[tid] = beta_r;
         __syncthreads();
         if (p == 1) ok = ok && wflag[0];
-        float pre0 = 0.f, pre1 = 0.f, last0 = 0.f, last1 = 0.f;
+        float2 pre = make_float2(0.f, 0.f), last = pre;   // totals of the warps before this one, of all
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
-            const float a0 = tot[w][2 * lane], a1 = tot[w][2 * lane + 1];
-            if (w < warp) { pre0 += a0; pre1 += a1; }
-            last0 += a0;
-            last1 += a1;
+            if (w == warp) pre = last;
+            last = __fadd2_rn(last, *reinterpret_cast<const float2 *>(&tot[w][2 * lane]));
         }
+        const float last0 = last.x, last1 = last.y;
         // Per channel the decays are referred to the midpoint B = b_last / 2 of
         // their range [b_last, 0]: the Gram factors e^(b - B) and e^(B - b) then
         // stay within e^(|b_last| / 2), and mu = e^B carries the rest
@@ -441,7 +444,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const float2 l2e2 = make_float2(kLog2e, kLog2e);
         const float2 refl2 = make_float2(-ref.x * kLog2e, -ref.y * kLog2e);
         auto build_rows = [&](auto kClamp) {
-        float2 bb = make_float2(pre0, pre1);
+        float2 bb = pre;
 #pragma unroll
         for (int j2 = 0; j2 < 8; j2 += 2) {
             float kgx[2][2], vx[2][2], kex[2][2], qgx[2][2];
@@ -495,22 +498,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         };
         if (clamp) build_rows(std::true_type{});
         else build_rows(std::false_type{});
-        // f16 operand rows d and d + 1, K = rows rb .. rb + 7.  Lanes 4-7 of each
-        // quarter-warp store row d + 1 first, so that every store instruction
-        // covers eight distinct rows modulo 8 (conflict-free).
+        // f16 operand rows d and d + 1, K = rows rb .. rb + 7: the padded tiles
+        // row d, then row d + 1; in Ke'^T lanes 4-7 of each quarter-warp store
+        // row d + 1 first, so that every store instruction covers eight distinct
+        // rows modulo 8 (conflict-free either way).
         {
+            const uint32_t pa = kmaj_off(d, rb, LBO_KIN, SBO_K64P), pb = kmaj_off(d + 1, rb, LBO_KIN, SBO_K64P);
+            *reinterpret_cast<uint4 *>(sm + K1_KGT + pa) = make_uint4(kg0[0], kg0[1], kg0[2], kg0[3]);
+            *reinterpret_cast<uint4 *>(sm + K1_KGT + pb) = make_uint4(kg1[0], kg1[1], kg1[2], kg1[3]);
+            *reinterpret_cast<uint4 *>(sm + K1_VT + pa) = make_uint4(vf0[0], vf0[1], vf0[2], vf0[3]);
+            *reinterpret_cast<uint4 *>(sm + K1_VT + pb) = make_uint4(vf1[0], vf1[1], vf1[2], vf1[3]);
             const bool sw = lane & 4;
             const uint32_t oa = kmaj_off(d + (sw ? 1 : 0), rb, LBO_KIN, SBO_K64);
             const uint32_t ob = kmaj_off(d + (sw ? 0 : 1), rb, LBO_KIN, SBO_K64);
-#define K1_PAIR_STORE(base, x0, x1)                                                                    \
-    *reinterpret_cast<uint4 *>(sm + (base) + oa) =                                                    \
-        sw ? make_uint4(x1[0], x1[1], x1[2], x1[3]) : make_uint4(x0[0], x0[1], x0[2], x0[3]);         \
-    *reinterpret_cast<uint4 *>(sm + (base) + ob) =                                                    \
-        sw ? make_uint4(x0[0], x0[1], x0[2], x0[3]) : make_uint4(x1[0], x1[1], x1[2], x1[3]);
-            K1_PAIR_STORE(K1_KGT, kg0, kg1)
-            K1_PAIR_STORE(K1_VT, vf0, vf1)
-            K1_PAIR_STORE(K1_KET, ke0, ke1)
-#undef K1_PAIR_STORE
+            *reinterpret_cast<uint4 *>(sm + K1_KET + oa) =
+                sw ? make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]) : make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]);
+            *reinterpret_cast<uint4 *>(sm + K1_KET + ob) =
+                sw ? make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]) : make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
         }
         // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
         *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
@@ -756,9 +760,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const uint32_t btk = smem_u32(sm + K1_TBK), btv = smem_u32(sm + K1_TBV);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            mma_f16(tm + T1_W1, make_desc(akg + ks * 256, LBO_KIN, SBO_K64),
+            mma_f16(tm + T1_W1, make_desc(akg + ks * 256, LBO_KIN, SBO_K64P),
                     make_desc(btk + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
-            mma_f16(tm + T1_W2, make_desc(av + ks * 256, LBO_KIN, SBO_K64),
+            mma_f16(tm + T1_W2, make_desc(av + ks * 256, LBO_KIN, SBO_K64P),
                     make_desc(btv + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
         }
         mma_commit(&mbar);
@@ -1125,24 +1129,9 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     break;
                 }
                 fence_after_sync();
-                // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16 now and
-                // stored after the state is handed on; then S = gamma * S + P over this
-                // thread's 32 rows d
-                uint32_t ob16[8];
-                {
-                    float o[16];
-                    tmem_ld16(tm + lane_base + T2_O + 256 * (cc & 1) + 16 * qd, o);
-                    tmem_ld_wait();
-                    if constexpr (kGate) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = __fdividef(o[i], 1.f + __expf(-__uint_as_float(zg[i] << 16)));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-                        ob16[j] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                }
+                // S = gamma * S + P over this thread's 32 rows d, handed on as the next
+                // S^T before this chunk's output is read (the next product waits
+                // only for the state)
                 {
                     const float *gam = reinterpret_cast<const float *>(sm + K2_GAM + (cc % kGamSlots) * 512) + 32 * qd;
 #pragma unroll
@@ -1162,12 +1151,28 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                         }
                     }
                 }
-                fence_before_sync();
-                mbar_arrive(&pread[cc & 1]);
                 if (c + 1 < nch) {   // the next chunk's S^T (none after the chain's last chunk)
                     write_sop_quarter(sm + K2_SOP, e, qd, S);
                     fence_async_smem();
                     mbar_arrive(&sready[qd >> 1]);
+                }
+                // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16
+                uint32_t ob16[8];
+                {
+                    float o[16];
+                    tmem_ld16(tm + lane_base + T2_O + 256 * (cc & 1) + 16 * qd, o);
+                    tmem_ld_wait();
+                    fence_before_sync();
+                    mbar_arrive(&pread[cc & 1]);   // P and O of the buffer read
+                    if constexpr (kGate) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __fdividef(o[i], 1.f + __expf(-__uint_as_float(zg[i] << 16)));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+                        ob16[j] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
                 }
 
                 // this chunk's output, while the next state product runs: straight from
