@@ -704,11 +704,18 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             *reinterpret_cast<uint2 *>(sm + K1_TBV + o) = make_uint2(pack_f16x2(v01.x, v01.y), pack_f16x2(v23.x, v23.y));
         }
         // 6. the other blocks of T (T_AA, T_BB, final since the 16 -> 32 merge,
-        //    and the zeros above the diagonal) -> the same operands: 384 pieces
-        //    of 8 columns; pieces 0-255 are rows 0-31 (warp = column piece),
-        //    pieces 256-383 rows 32-63, column pieces 4-7
-        for (int gi = tid; gi < 384; gi += K1_THREADS) {
-            const int r = (gi < 256 ? 0 : 32) + (gi & 31), c0 = 8 * ((gi < 256 ? 0 : 4) + ((gi & 255) >> 5));
+        //    and the zeros above the diagonal) -> the same operands, in pieces
+        //    of 8 columns (warp = column piece, lane = row): thread t < 128 takes
+        //    rows 0-31 x column pieces 0-3 (T_AA) and stores the zero pieces 4-7
+        //    of the same rows, thread t >= 128 rows 32-63 x column pieces 4-7 (T_BB)
+        if (tid < 128) {
+            const uint32_t o = kmaj_off(tid & 31, 8 * (4 + (tid >> 5)), LBO_KIN, SBO_K64);
+            *reinterpret_cast<uint4 *>(sm + K1_TBK + o) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(sm + K1_TBV + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        static_assert(K1_THREADS == 256, "one T piece per thread");
+        {
+            const int r = (tid < 128 ? 0 : 32) + (tid & 31), c0 = 8 * (tid >> 5);
             float tk[8], tv[8];
 #pragma unroll
             for (int j4 = 0; j4 < 8; j4 += 4) {
