@@ -906,49 +906,56 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 
 // ============================================================ K2
 // One CTA per (sequence, head), serial over the sequence's chunks.
-//   16 warps, all on the state: thread (e = 32 (w & 3) + lane, quarter
-//   qd = w >> 2) keeps S[d][e] for d in [32 qd, 32 qd + 32) in fp32 registers
-//   and writes output rows [16 qd, 16 qd + 16) of column e.  One thread also
-//   copies the records' tensor-core part into a 2-stage ring and issues the
-//   MMAs (a separate warp would take the registers the state needs: 16 warps
-//   are the most that keep 128 registers each).
+//   16 state warps: thread (e = 32 (w & 3) + lane, quarter qd = w >> 2) keeps
+//   S[d][e] for d in [32 qd, 32 qd + 32) in fp32 registers and writes output
+//   rows [16 qd, 16 qd + 16) of column e; one thread of a 17th warp issues the
+//   MMAs and one of an 18th the record copies into a 2-stage ring.
 // Per chunk one product [A' S | Q' S]^T (N = 192: the record keeps the A'
 // and Q' tiles adjacent) accumulates over two K-halves of d', each issued once
-// the state threads owning those rows of S^T have written them.  The state
-// threads read both parts at once, so the next chunk's product overwrites
-// them while this chunk's output is written to memory.
+// the state threads owning those rows of S^T have written them.  S^T, the
+// product's A operand, lives in TMEM (f16, row e in lane e): the tensor core
+// then reads only the B operand from shared memory, whose bandwidth the
+// product would otherwise nearly fill, to the cost of the record copies that
+// land there meanwhile.  The state threads read P, hand the next S^T on, then
+// read O, so the next chunk's product overwrites them while this chunk's
+// output is written to memory.
 constexpr int K2_STAGES = 2;
 constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
-constexpr uint32_t K2_SOP = K2_STAGES * REC_BYTES;     // f16 S^T: rows e x K = d
-constexpr uint32_t K2_GAM = K2_SOP + 32768;            // fp32 gamma [kGamSlots][128]
+constexpr uint32_t K2_GAM = K2_STAGES * REC_BYTES;     // fp32 gamma [kGamSlots][128]
 constexpr int K2_STATE_WARPS = 16;
 constexpr uint32_t K2_SMEM = K2_GAM + kGamSlots * 512;
 constexpr int K2_STATE_THREADS = 32 * K2_STATE_WARPS;
-constexpr int K2_THREADS = K2_STATE_THREADS + 32;
+constexpr int K2_THREADS = K2_STATE_THREADS + 64;   // + the MMA issuer's warp and the copy warp
 static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
 // TMEM columns (512 allocated): accumulator buffer b at 256 b, (A' S)^T in its
-// columns 0-127 and (Q' S)^T in 128-191
-constexpr uint32_t T2_P = 0, T2_O = 128;
+// columns 0-127 and (Q' S)^T in 128-191; S^T in f16 at 192-255 (row e in lane
+// e, d and d + 1 in one column)
+constexpr uint32_t T2_P = 0, T2_O = 128, T2_S = 192;
 
-__device__ __forceinline__ void write_sop_quarter(uint8_t *sop, int e, int qd, const float (&S)[32])
+// This thread's 32 rows d of S^T (lane e, columns T2_S + 16 qd ..) in f16,
+// stored and complete when the function returns.
+__device__ __forceinline__ void write_state_tmem(uint32_t taddr, const float (&S)[32])
 {
+    float pk[16];
 #pragma unroll
-    for (int d8 = 0; d8 < 32; d8 += 8)
-        *reinterpret_cast<uint4 *>(sop + kmaj_off(e, 32 * qd + d8, LBO_KIN, SBO_K128)) = pack_f16x8(S + d8);
+    for (int i = 0; i < 16; ++i) pk[i] = __uint_as_float(pack_f16x2(S[2 * i], S[2 * i + 1]));
+    tmem_st16(taddr, pk);
+    tmem_st_wait();
 }
 
 
 // kMulti false: one chain per CTA (grid = chains); true: chains in turn.
 // kGate: the output is o * sigmoid(gate) (the fused epilogue), gate [T, H, Dv] bf16.
 template <bool kMulti, bool kGate>
-__global__ void __maxnreg__(96)   // 17 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
+__global__ void __maxnreg__(96)   // 18 warps: at most 5 per SM sub-partition x 32 x 96 <= 16384
 k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
              float *__restrict__ carry, bf16 *__restrict__ out, DevStatus *st, uint32_t wait_limit,
              const bf16 *__restrict__ gate)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t full[K2_STAGES], empty[K2_STAGES], gfull[kGamSlots], sdone, pread[2], sready[2], dbar;
+    __shared__ uint64_t full[K2_STAGES], fullr[K2_STAGES], empty[K2_STAGES], emptyr[K2_STAGES], gfull[kGamSlots],
+        sdone, pread[2], sready[2], dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -960,8 +967,10 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
     // CTA's chains: the chain's local chunk c is chunk base + c of the CTA.
     if (tid == 0) {
         for (int s = 0; s < K2_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);   // the MMA's commit: the state threads read gamma from its own ring
+            mbar_init(&full[s], 1);     // [A'; Q'] of the stage landed
+            mbar_init(&fullr[s], 1);    // [Ke^T; Mc], Uv^T of the stage landed
+            mbar_init(&empty[s], 1);    // the MMA's commits: the stage's parts were read (the state
+            mbar_init(&emptyr[s], 1);   // threads read gamma from its own ring)
         }
         for (int j = 0; j < kGamSlots; ++j) mbar_init(&gfull[j], 1);
         mbar_init(&sdone, 1);
@@ -984,17 +993,21 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
     const int q4 = warp & 3, qd = warp >> 2;
     const int e = 32 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    // Lane 0 of the last warp drives the record copies and the MMAs; the other
-    // lanes of that warp have no part.
+    // Lane 0 of the warp after the state warps issues the MMAs, lane 0 of the
+    // last warp the record copies (an MMA issue holds its thread for about the
+    // pipe's time per step, so copies issued by the same thread would wait
+    // behind the products); the other lanes of those warps have no part.
     const bool issuer = tid == K2_STATE_THREADS;
+    const bool copier = tid == K2_STATE_THREADS + 32;
     const bool state_thread = tid < K2_STATE_THREADS;
     constexpr size_t DD = (size_t)kD * kD;
     const int stride = io.stride;
-    int copied = 0;          // (issuer) chunks whose record copies were issued, CTA count
+    int copied = 0;          // (copier) chunks whose second record part was issued, CTA count
+    int copied_r = 0;        // (copier) ... whose first part and gamma were issued
     int base_run = 0;        // chunks of this CTA's earlier chains
     bool alive = true;
 
-    for (int chain = blockIdx.x; chain < N * H && alive && (issuer || state_thread); chain += gridDim.x) {
+    for (int chain = blockIdx.x; chain < N * H && alive && (issuer || copier || state_thread); chain += gridDim.x) {
         const int base = kMulti ? base_run : 0;
         const int n = chain / H, h = chain % H;
         // This launch covers the sequence's local chunks [c_lo, c_lo + nch) of
@@ -1031,37 +1044,54 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
         // record of the sequence's chunk c_lo + i
         auto rec_at = [&](int i) { return ring + ((rec_base + i) * H + h) * REC_BYTES; };
 
-        if (issuer) {
-            // record of local chunk c -> stage cc % K2_STAGES (cc = base + c),
-            // once the product of chunk cc - K2_STAGES has read that stage
-            auto issue_copy = [&](int c) -> bool {
+        if (copier) {
+            // ---------------------------------------------------------- copies
+            // Record of local chunk c -> stage cc % K2_STAGES (cc = base + c), in
+            // two parts with barriers of their own: the tiles of the
+            // state-independent steps (Ke^T, Mc, Uv^T; 40 KB), once those steps
+            // of chunk cc - K2_STAGES have read the stage's copy, and [A'; Q']
+            // (48 KB), once that chunk's product is complete.  The first part's
+            // stage frees up about a chunk earlier, so two parts are in flight
+            // most of the time; gamma goes into its own slot with its own barrier
+            // (the state threads read it later).
+            static_assert(REC_KM + 40960 == REC_G && REC_AP == 0, "record parts");
+            for (int c = 0; c < nch && alive; ++c) {
                 const int cc = base + c, s = cc % K2_STAGES;
-                if (cc >= K2_STAGES && !wait_or_abort(&empty[s], ((cc - K2_STAGES) / K2_STAGES) & 1, abort_v, wait_limit))
-                    return false;
-                // the operand tiles into the stage (free again as soon as the MMA
-                // has read it), gamma into its own slot with its own barrier (the
-                // state threads read it later); the record two chunks further on
-                // is brought towards L2 meanwhile
-                mbar_arrive_expect_tx(&full[s], REC_G);
-                bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_G, &full[s]);
+                if (cc >= K2_STAGES &&
+                    !wait_or_abort(&emptyr[s], ((cc - K2_STAGES) / K2_STAGES) & 1, abort_v, wait_limit)) {
+                    alive = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&fullr[s], REC_G - REC_KM);
+                bulk_g2s(sm + s * REC_BYTES + REC_KM, rec_at(c) + REC_KM, REC_G - REC_KM, &fullr[s]);
                 mbar_arrive_expect_tx(&gfull[cc % kGamSlots], 512);
                 bulk_g2s(sm + K2_GAM + (cc % kGamSlots) * 512, rec_at(c) + REC_G, 512, &gfull[cc % kGamSlots]);
-                if (kMulti && c + K2_STAGES < nch) prefetch_l2(rec_at(c + K2_STAGES), REC_BYTES);
+                copied_r = cc + 1;
+                if (cc >= K2_STAGES &&
+                    !wait_or_abort(&empty[s], ((cc - K2_STAGES) / K2_STAGES) & 1, abort_v, wait_limit)) {
+                    alive = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], REC_KM);
+                bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_KM, &full[s]);
                 copied = cc + 1;
-                return true;
-            };
+                // the record two chunks further on, from HBM on the chains-in-turn
+                // path, is brought towards L2 meanwhile
+                if (kMulti && c + K2_STAGES < nch) prefetch_l2(rec_at(c + K2_STAGES), REC_BYTES);
+            }
+        } else if (issuer) {
             // chunk cc: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T,
             // in TMEM buffer cc & 1 (N = 192 rows of B: d, then r).  The K = r
             // steps (A = Uv^T) do not involve the state: they are issued as soon
-            // as the record has landed and the buffer's previous contents (chunk
-            // cc - 2) were read, so they run while the state threads still work
-            // on chunk cc - 1; the K = d' steps (A = S^T) follow half by half as
-            // the state threads write S^T.
+            // as their part of the record has landed and the buffer's previous
+            // contents (chunk cc - 2) were read, so they run while the state
+            // threads still work on chunk cc - 1; the K = d' steps (A = S^T)
+            // follow half by half as the state threads write S^T.
             auto issue_rpart = [&](int cc) -> bool {
                 const int s = cc % K2_STAGES;
                 const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
                 const uint32_t idesc = idesc_f16(128, 192);
-                bool okw = wait_or_abort(&full[s], (cc / K2_STAGES) & 1, abort_v, wait_limit);
+                bool okw = wait_or_abort(&fullr[s], (cc / K2_STAGES) & 1, abort_v, wait_limit);
                 okw = okw && (cc < 2 || wait_or_abort(&pread[cc & 1], ((cc >> 1) - 1) & 1, abort_v, wait_limit));
                 if (!okw) return false;
                 fence_after_sync();
@@ -1069,38 +1099,37 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 for (int ks = 0; ks < 4; ++ks)
                     mma_f16(acc, make_desc(stg + REC_UV + ks * 256, LBO_KIN, SBO_K64),
                             make_desc(stg + REC_KM + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
+                mma_commit(&emptyr[s]);
                 return true;
             };
             auto issue_dpart = [&](int cc) -> bool {
                 const int s = cc % K2_STAGES;
                 const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
-                const uint32_t sop = smem_u32(sm + K2_SOP);
+                const uint32_t sop = tm + T2_S;   // S^T in TMEM: a K step of 16 is 8 columns
                 const uint32_t idesc = idesc_f16(128, 192);
-                if (!wait_or_abort(&sready[0], cc & 1, abort_v, wait_limit)) return false;
+                if (!wait_or_abort(&full[s], (cc / K2_STAGES) & 1, abort_v, wait_limit) ||
+                    !wait_or_abort(&sready[0], cc & 1, abort_v, wait_limit))
+                    return false;
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+                    mma_f16_ts(acc, sop + 8 * ks, make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
                 if (!wait_or_abort(&sready[1], cc & 1, abort_v, wait_limit)) return false;
                 fence_after_sync();
 #pragma unroll
                 for (int ks = 4; ks < 8; ++ks)
-                    mma_f16(acc, make_desc(sop + ks * 256, LBO_KIN, SBO_K128),
-                            make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
+                    mma_f16_ts(acc, sop + 8 * ks, make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
                 mma_commit(&sdone);
                 mma_commit(&empty[s]);
                 return true;
             };
             // ---------------------------------------------------------- issuer
-            for (int c = 0; c < min(nch, K2_STAGES) && alive; ++c) alive = issue_copy(c);
             alive = alive && issue_rpart(base);
             for (int c = 0; c < nch && alive; ++c) {
-                // chunk c's state-dependent steps; then record c + 2 into the
-                // stage chunk c used, once its product is complete; then the
-                // state-independent steps of chunk c + 1
+                // chunk c's state-dependent steps, then the state-independent
+                // steps of chunk c + 1 (queued behind them, they run while the
+                // state threads update the state)
                 if (!issue_dpart(base + c)) { alive = false; break; }
-                if (c + K2_STAGES < nch && !issue_copy(c + K2_STAGES)) { alive = false; break; }
                 if (c + 1 < nch && !issue_rpart(base + c + 1)) { alive = false; break; }
             }
         } else {
@@ -1110,8 +1139,9 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 S[j] = src_state ? src_state[(size_t)(32 * qd + j) * kD + e] : 0.f;
-            write_sop_quarter(sm + K2_SOP, e, qd, S);
-            fence_async_smem();
+            const uint32_t s_taddr = tm + lane_base + T2_S + 16 * qd;   // this thread's part of S^T
+            write_state_tmem(s_taddr, S);
+            fence_before_sync();
             mbar_arrive(&sready[qd >> 1]);
             for (int c = 0; c < nch && alive; ++c) {
                 const int cc = base + c;
@@ -1159,8 +1189,8 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     }
                 }
                 if (c + 1 < nch) {   // the next chunk's S^T (none after the chain's last chunk)
-                    write_sop_quarter(sm + K2_SOP, e, qd, S);
-                    fence_async_smem();
+                    write_state_tmem(s_taddr, S);
+                    fence_before_sync();
                     mbar_arrive(&sready[qd >> 1]);
                 }
                 // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16
@@ -1220,16 +1250,22 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
     if (!alive) {
         *abort_v = 1;
         if (lane == 0) record_timeout(st);
-        // never leave a copy or an MMA in flight: the last stages' copies land,
-        // and a commit arrives once every MMA the issuer started is complete
-        if (issuer) {
-            for (int c = max(0, copied - K2_STAGES); c < copied; ++c)
-                mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kDrainLimit);
-            for (int c = max(0, copied - kGamSlots); c < copied; ++c)
-                mbar_wait_bounded(&gfull[c % kGamSlots], (c / kGamSlots) & 1, kDrainLimit);
-            mma_commit(&dbar);
-            mbar_wait_bounded(&dbar, 0, kDrainLimit);
-        }
+    }
+    // Never leave a copy or an MMA in flight (another role may have given up
+    // while these two finished): the last stages' copies land, and a commit
+    // arrives once every MMA the issuer started is complete.  After a normal
+    // run both have already happened and the waits return at once.
+    if (copier) {
+        for (int c = max(0, copied_r - K2_STAGES); c < copied_r; ++c)
+            mbar_wait_bounded(&fullr[c % K2_STAGES], (c / K2_STAGES) & 1, kDrainLimit);
+        for (int c = max(0, copied - K2_STAGES); c < copied; ++c)
+            mbar_wait_bounded(&full[c % K2_STAGES], (c / K2_STAGES) & 1, kDrainLimit);
+        for (int c = max(0, copied_r - kGamSlots); c < copied_r; ++c)
+            mbar_wait_bounded(&gfull[c % kGamSlots], (c / kGamSlots) & 1, kDrainLimit);
+    }
+    if (issuer) {
+        mma_commit(&dbar);
+        mbar_wait_bounded(&dbar, 0, kDrainLimit);
     }
 
     fence_before_sync();
