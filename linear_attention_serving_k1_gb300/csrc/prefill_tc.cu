@@ -913,12 +913,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 // Per chunk one product [A' S | Q' S]^T (N = 192: the record keeps the A'
 // and Q' tiles adjacent) accumulates over two K-halves of d', each issued once
 // the state threads owning those rows of S^T have written them.  S^T, the
-// product's A operand, lives in TMEM (f16, row e in lane e): the tensor core
-// then reads only the B operand from shared memory, whose bandwidth the
-// product would otherwise nearly fill, to the cost of the record copies that
-// land there meanwhile.  The state threads read P, hand the next S^T on, then
-// read O, so the next chunk's product overwrites them while this chunk's
-// output is written to memory.
+// product's A operand, lives in TMEM (f16, row e in lane e): the state threads
+// hand it on with tcgen05.st instead of shared-memory stores and a proxy
+// fence, and the tensor core reads only the B operand from shared memory.
+// The state threads read P, hand the next S^T on, then read O, so the next
+// chunk's product overwrites them while this chunk's output is written to
+// memory.
 constexpr int K2_STAGES = 2;
 constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
 constexpr uint32_t K2_GAM = K2_STAGES * REC_BYTES;     // fp32 gamma [kGamSlots][128]
