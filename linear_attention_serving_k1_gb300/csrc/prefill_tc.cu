@@ -224,21 +224,27 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // and come before any allocation.
     const int h = (int)(blockIdx.x % (unsigned)H), item = (int)(blockIdx.x / (unsigned)H);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int n, lc;
+    int n, lc, cu0, cu1;
     size_t ri;
     if (G == 0) {
         if (item >= tab.chunk_off[N]) return;
         n = find_seq_tc(tab.chunk_off, N, item);
         lc = item - tab.chunk_off[n];
         ri = (size_t)item;
+        cu0 = tab.cu[n];
+        cu1 = tab.cu[n + 1];
     } else {
+        // n < N: both bounds of the sequence in one round trip, and its chunk
+        // count follows from them (lc < ceil(len / C) exactly when lc C < len)
         n = item / G;
         lc = seg_lo + item % G;
-        if (lc >= tab.chunk_off[n + 1] - tab.chunk_off[n]) return;
+        cu0 = tab.cu[n];
+        cu1 = tab.cu[n + 1];
+        if (lc * kC >= cu1 - cu0) return;
         ri = ((size_t)slot * N + n) * slot_chunks + item % G;
     }
-    const int t0 = tab.cu[n] + lc * kC;
-    const int L = min(kC, tab.cu[n + 1] - t0);
+    const int t0 = cu0 + lc * kC;
+    const int L = min(kC, cu1 - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
     // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in the record's
     // A' area (written once the product that reads it back is complete) until a
@@ -435,7 +441,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         // rb .. rb + 7, then k rows)
         float sq[8];
         const bool up16 = lane & 16;
-        // the two channels of a thread as packed fp32 pairs
+        // byte offset of (row rb, channels 2 lane and + 1 of the half) in the tf32 K-major tiles
+        const uint32_t gbase = kmaj_off4(rb, 2 * lane, K1_F32_LBO, K1_F32_SBO);
         // With g <= 0 each channel's b runs from 0 down to b_last, so |b - B| <=
         // |B|: while |B| <= kMaxDecayExp for every channel of the half (the
         // same channels in every warp), no factor can leave the range and the
@@ -450,7 +457,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             float kgx[2][2], vx[2][2], kex[2][2], qgx[2][2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int j = j2 + u, r = rb + j;
+                const int j = j2 + u;
                 bb = __fadd2_rn(bb, gv[j]);
                 // e^(b - B) and e^(B - b) as 2^(+-(b - B) log2 e): one packed FMA for
                 // the exponent, then the hardware base-2 exponential (flush to zero:
@@ -466,20 +473,21 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     ei = make_float2(ex2_ftz(-x.x), ex2_ftz(-x.y));
                 }
                 const float2 qq = up2(qv[j]), kk = up2(kv[j]);
-                const float2 qk0 = make_float2(qq.x, kk.x), qk1 = make_float2(qq.y, kk.y);
-                const float2 s2 = __ffma2_rn(qk1, qk1, __fmul2_rn(qk0, qk0));
-                sq[j] = (up16 ? s2.y : s2.x) + __shfl_xor_sync(0xffffffffu, up16 ? s2.x : s2.y, 16);
+                // (kept row, row sent across lane bit 4) = (q, k), or (k, q) when the bit is set
+                const float2 m0 = up16 ? make_float2(kk.x, qq.x) : make_float2(qq.x, kk.x);
+                const float2 m1 = up16 ? make_float2(kk.y, qq.y) : make_float2(qq.y, kk.y);
+                const float2 s2 = __ffma2_rn(m1, m1, __fmul2_rn(m0, m0));
+                sq[j] = s2.x + __shfl_xor_sync(0xffffffffu, s2.y, 16);
                 // Gram factors (referred to B), then the true decayed rows
                 const float2 kgr = __fmul2_rn(kk, e), qgr = __fmul2_rn(qq, e), kd = __fmul2_rn(kk, ei);
                 const float2 kg = __fmul2_rn(kgr, mu2), qg = __fmul2_rn(qgr, mu2);
                 const float2 ke = __fmul2_rn(kd, mu2);   // k' e^(b_last - b)
-                const uint32_t lo = 2 * lane;
-                *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(kgr.x), round_tf32(kgr.y));
-                *reinterpret_cast<float2 *>(sm + K1_GA + kmaj_off4(64 + r, lo, K1_F32_LBO, K1_F32_SBO)) =
+                // row r = rb + j of the K-major tiles: the warp's 8-row group, then j
+                uint8_t *const gp = sm + gbase + 16u * j;
+                *reinterpret_cast<float2 *>(gp + K1_GA) = make_float2(round_tf32(kgr.x), round_tf32(kgr.y));
+                *reinterpret_cast<float2 *>(gp + K1_GA + 8 * K1_F32_SBO) =   // row 64 + r
                     make_float2(round_tf32(qgr.x), round_tf32(qgr.y));
-                *reinterpret_cast<float2 *>(sm + K1_KD + kmaj_off4(r, lo, K1_F32_LBO, K1_F32_SBO)) =
-                    make_float2(round_tf32(kd.x), round_tf32(kd.y));
+                *reinterpret_cast<float2 *>(gp + K1_KD) = make_float2(round_tf32(kd.x), round_tf32(kd.y));
                 qgx[0][u] = qg.x; qgx[1][u] = qg.y;
                 kgx[0][u] = kg.x; kgx[1][u] = kg.y;
                 const float2 vf = up2(vv[j]);
@@ -595,7 +603,17 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             }
         }
     }
+    fence_async_smem();
     __syncthreads();
+    // Ke'^T and Mc', already K2's operand tiles, go to the record by bulk copies
+    // while the inverse runs (waited for before the CTA exits; neither tile is
+    // overwritten)
+    if (tid == 0) {
+        static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
+        bulk_s2g(rec + REC_KM, sm + K1_KET, 16384);
+        bulk_s2g(rec + REC_MC, sm + K1_MC, 8192);
+        bulk_commit();
+    }
     // 5. T = (I + L)^-1.  Diagonal 16 x 16 blocks by forward substitution (one
     //    column per thread, four partial sums per step), then two doubling
     //    merges, 16 -> 32 and 32 -> 64: for a lower block pair A (top) and B,
@@ -611,8 +629,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int ii = 0; ii < rr; ++ii)   // tcol[ii] = 0 for ii < c: no lane-dependent predicate
                 x[ii & 3] -= Lm[r * K1_PL + 16 * blk + ii] * tcol[ii];
             tcol[rr] = (rr >= c) ? (x[0] + x[1]) + (x[2] + x[3]) : 0.f;
-            Tm[r * K1_P + col] = tcol[rr];
         }
+        // stored after the loop: with no store between them, the loads of L
+        // can be issued ahead of the dependent chain
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * K1_P + col] = tcol[rr];
     } else if (tid < 192) {
         // zeros in the 16 x 16 blocks above the diagonal of T_AA and T_BB
         // (rows 0-15 x columns 16-31, rows 32-47 x columns 48-63): the merges
@@ -745,20 +766,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // Ke'^T and Mc', already K2's operand tiles, go to the record by bulk copies
-    // (waited for before the CTA exits; neither tile is overwritten), and the
-    // parked Qg'^T tile comes back over T, free now that the inverse is done
+    // the parked Qg'^T tile comes back over T, free now that the inverse is done
     bool q_issued = false;   // (thread 0) the copy is in flight until qbar completes
-    if (tid == 0) {
-        static_assert(REC_MC == REC_KM + 16384, "Mc follows Ke^T");
-        bulk_s2g(rec + REC_KM, sm + K1_KET, 16384);
-        bulk_s2g(rec + REC_MC, sm + K1_MC, 8192);
-        bulk_commit();
-        if (ok) {
-            mbar_arrive_expect_tx(&qbar, 16384);
-            bulk_g2s(sm + K1_QG, qg_park, 16384, &qbar);
-            q_issued = true;
-        }
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(&qbar, 16384);
+        bulk_g2s(sm + K1_QG, qg_park, 16384, &qbar);
+        q_issued = true;
     }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
@@ -778,7 +791,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // while the products run (the merge scratch it overwrites is dead)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int idx = tid + K1_THREADS * h, i = idx >> 3, kg = idx & 7;
+        // lanes take consecutive rows i (eight lanes fill 128 contiguous bytes)
+        const int idx = tid + K1_THREADS * h, i = idx & 63, kg = idx >> 6;
         float dv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) dv[j] = (8 * kg + j == i) ? rq[i] : 0.f;
