@@ -372,15 +372,21 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     }
     const float beta_r = (tid < kC && tid < L) ? __ldg(beta + (size_t)(t0 + tid) * H + h) : 0.f;
     load_half(0);
-    // L2 prefetch of the second channel half of this chunk's rows (bulk, one
-    // row slice per thread), so that its loads after the first half hit L2
+    // L2 prefetch of the second channel half of this chunk's rows (one row
+    // slice per thread: one 128-byte line of q, k or v, two of g), so that its
+    // loads after the first half hit L2.  Line prefetches go through the
+    // load/store path; the bulk prefetch of the same slices, issued through
+    // the copy engine, held the issuing warps longer (calls 1.5% slower).
     {
         const int r = tid & 63, which = tid >> 6;   // q, k, v, g
         const char *base = which == 0 ? (const char *)q : which == 1 ? (const char *)k
                          : which == 2 ? (const char *)v : (const char *)g;
         const uint32_t esz = which == 3 ? 4u : 2u;
-        if (!kConv && r < L && (which < 3 || !scalar_gate))
-            prefetch_l2(base + (((size_t)(t0 + r) * H + h) * kD + 64) * esz, 64 * esz);
+        if (!kConv && r < L && (which < 3 || !scalar_gate)) {
+            const char *slice = base + (((size_t)(t0 + r) * H + h) * kD + 64) * esz;
+            prefetch_line_l2(slice);
+            if (esz == 4u) prefetch_line_l2(slice + 128);
+        }
     }
 
     if (warp == 0) {
@@ -575,11 +581,14 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     float *Tm = reinterpret_cast<float *>(sm + K1_TM);
     float *Xs = reinterpret_cast<float *>(sm + K1_XS);
     float *Xw = reinterpret_cast<float *>(sm + K1_XW);
-    if (ok) {
-        float gq[32];
-        tmem_ld32(tm + lane_base + T1_G + 32 * ch, gq);
-        tmem_ld_wait();
-        if (row < 64) {
+    if (ok && row < 64) {
+        // L.  The inverse reads only its entries below the diagonal: they are
+        // stored unmasked, and warp 4 (rows 0-31, columns 32-63, all on or above
+        // the diagonal) neither reads G' nor stores.
+        if (ch <= q4) {
+            float gq[32];
+            tmem_ld32(tm + lane_base + T1_G + 32 * ch, gq);
+            tmem_ld_wait();
             const int r = row;
             const float sr = bs[r] * rk[r];
             const float2 sr2 = make_float2(sr, sr);
@@ -588,20 +597,38 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 const int col = 32 * ch + i;
                 const float2 lv = __fmul2_rn(__fmul2_rn(sr2, *reinterpret_cast<const float2 *>(rk + col)),
                                              make_float2(gq[i], gq[i + 1]));
-                Lm[r * K1_PL + col] = (col < r) ? lv.x : 0.f;
-                Lm[r * K1_PL + col + 1] = (col + 1 < r) ? lv.y : 0.f;
+                Lm[r * K1_PL + col] = lv.x;
+                Lm[r * K1_PL + col + 1] = lv.y;
             }
-        } else {
-            const int r = row - 64;
+        }
+    } else if (ok) {
+        // Mc' = rows r of G'_qk with the columns above the diagonal zeroed (K2
+        // reads the whole tile).  Rows 32 dq .. + 31: columns 32 ch .. + 31 lie
+        // wholly below the diagonal when ch < dq, wholly above it when ch > dq.
+        const int r = row - 64, dq = q4 - 2;
+        auto store_mc = [&](auto kMode) {   // 0: masked, 1: below, 2: above
+            constexpr int mode = decltype(kMode)::value;
+            float gq[32];
+            if constexpr (mode != 2) {
+                tmem_ld32(tm + lane_base + T1_G + 32 * ch, gq);
+                tmem_ld_wait();
+            }
             const float sr = rq[r];
 #pragma unroll
             for (int i8 = 0; i8 < 32; i8 += 8) {
                 float m8[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) m8[j] = (32 * ch + i8 + j <= r) ? sr * gq[i8 + j] : 0.f;
+                for (int j = 0; j < 8; ++j) {
+                    if constexpr (mode == 0) m8[j] = (32 * ch + i8 + j <= r) ? sr * gq[i8 + j] : 0.f;
+                    else if constexpr (mode == 1) m8[j] = sr * gq[i8 + j];
+                    else m8[j] = 0.f;
+                }
                 *reinterpret_cast<uint4 *>(sm + K1_MC + kmaj_off(r, 32 * ch + i8, LBO_KIN, SBO_K64)) = pack_f16x8(m8);
             }
-        }
+        };
+        if (ch == dq) store_mc(std::integral_constant<int, 0>{});
+        else if (ch < dq) store_mc(std::integral_constant<int, 1>{});
+        else store_mc(std::integral_constant<int, 2>{});
     }
     fence_async_smem();
     __syncthreads();
@@ -803,10 +830,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     fence_after_sync();
     ok = ok && wflag[2];
 
-    // 8. (-diag(rk) Wk)^T -> smem operand and (diag(rk) Uv)^T -> record (rows d / e, K = r).
-    //    Warp w reads lanes of quarter q4, columns [32 ch, 32 ch + 32).
+    // 8. (-diag(rk) Wk)^T -> smem operand (rows d, K = r); Uv^T stays in
+    //    registers until the products of phase 9 are issued.  Warp w reads
+    //    lanes of quarter q4, columns [32 ch, 32 ch + 32).
+    float wu[4][16];   // Wk^T and Uv^T, columns c and c + 16: all four loads before one wait
     if (ok) {
-        float wu[4][16];   // Wk^T and Uv^T, columns c and c + 16: all four loads before one wait
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
             tmem_ld16(tm + lane_base + T1_W1 + 32 * ch + 16 * c2, wu[2 * c2]);
@@ -815,23 +843,19 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; c += 16) {
-            float (&w)[16] = wu[c / 8], (&u)[16] = wu[c / 8 + 1];
+            float (&w)[16] = wu[c / 8];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
                 const float2 s2 = *reinterpret_cast<const float2 *>(rk + 32 * ch + c + j);
                 // Wk's tile carries -rk: the products of phase 9 come out as A'
                 // and -Mc Wk directly
                 const float2 w2 = __fmul2_rn(make_float2(w[j], w[j + 1]), make_float2(-s2.x, -s2.y));
-                const float2 u2 = __fmul2_rn(make_float2(u[j], u[j + 1]), s2);
                 w[j] = w2.x; w[j + 1] = w2.y;
-                u[j] = u2.x; u[j + 1] = u2.y;
             }
 #pragma unroll
-            for (int h8 = 0; h8 < 16; h8 += 8) {
-                const int kk = 32 * ch + c + h8;
-                *reinterpret_cast<uint4 *>(sm + K1_WKT + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(w + h8);
-                *reinterpret_cast<uint4 *>(rec + REC_UV + kmaj_off(row, kk, LBO_KIN, SBO_K64)) = pack_f16x8(u + h8);
-            }
+            for (int h8 = 0; h8 < 16; h8 += 8)
+                *reinterpret_cast<uint4 *>(sm + K1_WKT + kmaj_off(row, 32 * ch + c + h8, LBO_KIN, SBO_K64)) =
+                    pack_f16x8(w + h8);
         }
     }
     fence_async_smem();
@@ -861,6 +885,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             mma_f16(tm + T1_QP, make_desc(ard + ks * 256, LBO_KIN, SBO_K64),
                     make_desc(bq + ks * 256, LBO_KIN, SBO_K64), id64, 1);
         mma_commit(&mbar);
+    }
+    // (diag(rk) Uv)^T -> record (rows e, K = r) while the products run
+    if (ok) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            float (&u)[16] = wu[c / 8 + 1];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float2 s2 = *reinterpret_cast<const float2 *>(rk + 32 * ch + c + j);
+                const float2 u2 = __fmul2_rn(make_float2(u[j], u[j + 1]), s2);
+                u[j] = u2.x; u[j + 1] = u2.y;
+            }
+#pragma unroll
+            for (int h8 = 0; h8 < 16; h8 += 8)
+                *reinterpret_cast<uint4 *>(rec + REC_UV + kmaj_off(row, 32 * ch + c + h8, LBO_KIN, SBO_K64)) =
+                    pack_f16x8(u + h8);
+        }
     }
     if (tid == 0) wflag[3] = ok && q_landed && mbar_wait_bounded(&abar, 0, wait_limit);
     __syncthreads();
@@ -1089,9 +1130,6 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 mbar_arrive_expect_tx(&full[s], REC_KM);
                 bulk_g2s(sm + s * REC_BYTES, rec_at(c), REC_KM, &full[s]);
                 copied = cc + 1;
-                // the record two chunks further on, from HBM on the chains-in-turn
-                // path, is brought towards L2 meanwhile
-                if (kMulti && c + K2_STAGES < nch) prefetch_l2(rec_at(c + K2_STAGES), REC_BYTES);
             }
         } else if (issuer) {
             // chunk cc: D = [P | O], P = (A' S + Ke^T Uv)^T, O = (Q' S + Mc Uv)^T,

@@ -100,10 +100,11 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Hint: bring [src, src + bytes) into L2 (bulk prefetch; no completion).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+// Prefetch of the 128-byte line holding `src` into L2 (a plain prefetch, no
+// data returned to the thread).
+__device__ __forceinline__ void prefetch_line_l2(const void *src)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
 }
 
 // Orders this thread's earlier generic-proxy global writes before later
