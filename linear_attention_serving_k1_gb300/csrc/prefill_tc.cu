@@ -100,6 +100,39 @@ __device__ __forceinline__ void record_timeout(DevStatus *st)
     record_status(st, (int32_t)KDA_ERR_TIMEOUT);
 }
 
+// D += A B on the warp-level tensor-core path (m16n8k8, tf32 operands, fp32
+// accumulation) with each operand split into its leading tf32 part and the
+// fp32 remainder: the three products that matter (remainder terms first) give
+// the sum to about 1e-6 relative instead of tf32's 1e-3.  Fragments of lane
+// (g = lane / 4, t = lane % 4): a = A[g][t], A[g + 8][t], A[g][t + 4],
+// A[g + 8][t + 4]; b = B[t][g], B[t + 4][g]; d = D[g][2t], D[g][2t + 1],
+// D[g + 8][2t], D[g + 8][2t + 1].
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float (&a)[4], const float (&b)[2])
+{
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ah[i] = __float_as_uint(a[i]) & 0xFFFFE000u;   // the bits a tf32 operand keeps
+        al[i] = __float_as_uint(a[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        bh[i] = __float_as_uint(b[i]) & 0xFFFFE000u;
+        bl[i] = __float_as_uint(b[i] - __uint_as_float(bh[i]));
+    }
+    mma_m16n8k8_tf32(d, al, bh);
+    mma_m16n8k8_tf32(d, ah, bl);
+    mma_m16n8k8_tf32(d, ah, bh);
+}
+
 // Polls `bar` for phase `parity`; gives up after `limit` polls, or early when
 // another role of the CTA has flagged an abort.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -153,20 +186,21 @@ constexpr uint32_t K1_KET = K1_VT + 16 * SBO_K64P;     // f16 Ke'^T: rows d x K 
 constexpr uint32_t K1_SMEM = K1_KET + 16384;
 // later phases, inside [0, K1_GRAM_END)
 constexpr int K1_P = 68;                 // fp32 row pitch of T (16-byte aligned rows)
-constexpr int K1_PL = 65;                // fp32 row pitch of L (odd: conflict-free column stores)
-constexpr uint32_t K1_LM = 0;            // fp32 [64][65]  L (strict lower)
+constexpr int K1_PL = 68;                // fp32 row pitch of L (16-byte rows: conflict-free float4 stores by rows)
+constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower)
 constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
 constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][16] scratch of the 16 -> 32 merge
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
-constexpr uint32_t K1_XW = 46080;        // fp32 [32][36] scratch of the 32 -> 64 merge
+constexpr uint32_t K1_XW = 46080;        // fp32 [32][40] scratch of the 32 -> 64 merge
 constexpr uint32_t K1_RQD = 46080;       // f16 diag(rq): rows i x K = r (64 x 64), over XW after the inverse
-constexpr int K1_XWP = 36;               // its row pitch (conflict-free float4 stores by 32 rows)
+constexpr int K1_XWP = 40;               // its row pitch (conflict-free fragment loads)
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
 constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (16 KB), back from the record over T
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
 static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16384 <= K1_XS, "Qg tile between Wk^T and the merge scratch");
+static_assert(K1_LM + 64 * K1_PL * 4 <= K1_TM, "L below T");
 static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
@@ -593,12 +627,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const float sr = bs[r] * rk[r];
             const float2 sr2 = make_float2(sr, sr);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < 32; i += 4) {
                 const int col = 32 * ch + i;
-                const float2 lv = __fmul2_rn(__fmul2_rn(sr2, *reinterpret_cast<const float2 *>(rk + col)),
-                                             make_float2(gq[i], gq[i + 1]));
-                Lm[r * K1_PL + col] = lv.x;
-                Lm[r * K1_PL + col + 1] = lv.y;
+                const float4 rk4 = *reinterpret_cast<const float4 *>(rk + col);
+                const float2 l01 = __fmul2_rn(__fmul2_rn(sr2, make_float2(rk4.x, rk4.y)), make_float2(gq[i], gq[i + 1]));
+                const float2 l23 =
+                    __fmul2_rn(__fmul2_rn(sr2, make_float2(rk4.z, rk4.w)), make_float2(gq[i + 2], gq[i + 3]));
+                *reinterpret_cast<float4 *>(Lm + r * K1_PL + col) = make_float4(l01.x, l01.y, l23.x, l23.y);
             }
         }
     } else if (ok) {
@@ -700,56 +735,50 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-s0.x, -s0.y);
     }
     __syncthreads();
-    {   // 32 -> 64 (A = rows 0-31, B = rows 32-63).
-        // X = L_BA T_AA: thread = row i (lane), columns j4 .. j4 + 3 (warp), over
-        // all 32 rows of T_AA (zeros above its diagonal)
-        {
-            const int i = tid & 31, j4 = 4 * warp;
-            float2 s01 = make_float2(0.f, 0.f), s23 = s01, u01 = s01, u23 = s01;
-            const float *lrow = Lm + (32 + i) * K1_PL;
+    {   // 32 -> 64 (A = rows 0-31, B = rows 32-63) on the warp-level tensor-core
+        // path: warp w takes the 16 x 8 output tile at rows 16 (w & 1), columns
+        // 8 (w >> 1), over K = 32 in steps of 8 (mma_tf32x3).  Steps whose
+        // operand block lies above a triangular factor's diagonal are zero and
+        // skipped (a warp-uniform bound).
+        const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp & 1), n0 = 8 * (warp >> 1);
+        {   // X = L_BA T_AA: T_AA[k][n] = 0 for k < n, so k starts at n0
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *la = Lm + (32 + m0 + g) * K1_PL + t;
 #pragma unroll
-            for (int m = 0; m < 32; m += 2) {
-                const float4 t0 = *reinterpret_cast<const float4 *>(Tm + m * K1_P + j4);
-                const float4 t1 = *reinterpret_cast<const float4 *>(Tm + (m + 1) * K1_P + j4);
-                const float2 l0 = make_float2(lrow[m], lrow[m]), l1 = make_float2(lrow[m + 1], lrow[m + 1]);
-                s01 = __ffma2_rn(l0, make_float2(t0.x, t0.y), s01);
-                s23 = __ffma2_rn(l0, make_float2(t0.z, t0.w), s23);
-                u01 = __ffma2_rn(l1, make_float2(t1.x, t1.y), u01);
-                u23 = __ffma2_rn(l1, make_float2(t1.z, t1.w), u23);
+            for (int k0 = 0; k0 < 32; k0 += 8) {
+                if (k0 < n0) continue;
+                const float a[4] = {la[k0], la[8 * K1_PL + k0], la[k0 + 4], la[8 * K1_PL + k0 + 4]};
+                const float b[2] = {Tm[(k0 + t) * K1_P + n0 + g], Tm[(k0 + t + 4) * K1_P + n0 + g]};
+                mma_tf32x3(d, a, b);
             }
-            s01 = __fadd2_rn(s01, u01);
-            s23 = __fadd2_rn(s23, u23);
-            *reinterpret_cast<float4 *>(Xw + i * K1_XWP + j4) = make_float4(s01.x, s01.y, s23.x, s23.y);
+            *reinterpret_cast<float2 *>(Xw + (m0 + g) * K1_XWP + n0 + 2 * t) = make_float2(d[0], d[1]);
+            *reinterpret_cast<float2 *>(Xw + (m0 + g + 8) * K1_XWP + n0 + 2 * t) = make_float2(d[2], d[3]);
         }
         __syncthreads();
-        // T_BA = -T_BB X: thread = row i, columns j4 .. j4 + 3, over all 32
-        // columns of T_BB (zeros above its diagonal).  The entries go straight into the f16 operands
-        // T diag(beta rk) and T diag(beta) (rows r, K = i), which overwrite L.
+        // T_BA = -T_BB X (T_BB[m][k] = 0 for k > m, so k stays below m0 + 16).
+        // The entries go straight into the f16 operands T diag(beta rk) and
+        // T diag(beta) (rows r, K = i), which overwrite L.
         {
-            const int i = tid >> 3, j4 = (tid & 7) * 4;
-            float2 s01 = make_float2(0.f, 0.f), s23 = s01, u01 = s01, u23 = s01;
-            const float *trow = Tm + (32 + i) * K1_P + 32;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *ta = Tm + (32 + m0 + g) * K1_P + 32 + t;
 #pragma unroll
-            for (int m = 0; m < 32; m += 2) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(Xw + m * K1_XWP + j4);
-                const float4 x1 = *reinterpret_cast<const float4 *>(Xw + (m + 1) * K1_XWP + j4);
-                const float2 t0 = make_float2(trow[m], trow[m]), t1 = make_float2(trow[m + 1], trow[m + 1]);
-                s01 = __ffma2_rn(t0, make_float2(x0.x, x0.y), s01);
-                s23 = __ffma2_rn(t0, make_float2(x0.z, x0.w), s23);
-                u01 = __ffma2_rn(t1, make_float2(x1.x, x1.y), u01);
-                u23 = __ffma2_rn(t1, make_float2(x1.z, x1.w), u23);
+            for (int k0 = 0; k0 < 32; k0 += 8) {
+                if (k0 >= m0 + 16) continue;
+                const float a[4] = {ta[k0], ta[8 * K1_P + k0], ta[k0 + 4], ta[8 * K1_P + k0 + 4]};
+                const float b[2] = {Xw[(k0 + t) * K1_XWP + n0 + g], Xw[(k0 + t + 4) * K1_XWP + n0 + g]};
+                mma_tf32x3(d, a, b);
             }
-            s01 = __fadd2_rn(s01, u01);
-            s23 = __fadd2_rn(s23, u23);
-            const float4 b4 = *reinterpret_cast<const float4 *>(bs + j4);
-            const float4 k4 = *reinterpret_cast<const float4 *>(rk + j4);
-            const float2 v01 = __fmul2_rn(make_float2(-s01.x, -s01.y), make_float2(b4.x, b4.y));
-            const float2 v23 = __fmul2_rn(make_float2(-s23.x, -s23.y), make_float2(b4.z, b4.w));
-            const float2 k01 = __fmul2_rn(v01, make_float2(k4.x, k4.y));
-            const float2 k23 = __fmul2_rn(v23, make_float2(k4.z, k4.w));
-            const uint32_t o = kmaj_off(32 + i, j4, LBO_KIN, SBO_K64);
-            *reinterpret_cast<uint2 *>(sm + K1_TBK + o) = make_uint2(pack_f16x2(k01.x, k01.y), pack_f16x2(k23.x, k23.y));
-            *reinterpret_cast<uint2 *>(sm + K1_TBV + o) = make_uint2(pack_f16x2(v01.x, v01.y), pack_f16x2(v23.x, v23.y));
+            const int c = n0 + 2 * t;
+            const float2 b2 = *reinterpret_cast<const float2 *>(bs + c);
+            const float2 k2 = *reinterpret_cast<const float2 *>(rk + c);
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                const float2 v = __fmul2_rn(make_float2(-d[2 * h8], -d[2 * h8 + 1]), b2);
+                const float2 kv = __fmul2_rn(v, k2);
+                const uint32_t o = kmaj_off(32 + m0 + g + 8 * h8, c, LBO_KIN, SBO_K64);
+                *reinterpret_cast<uint32_t *>(sm + K1_TBK + o) = pack_f16x2(kv.x, kv.y);
+                *reinterpret_cast<uint32_t *>(sm + K1_TBV + o) = pack_f16x2(v.x, v.y);
+            }
         }
         // 6. the other blocks of T (T_AA, T_BB, final since the 16 -> 32 merge,
         //    and the zeros above the diagonal) -> the same operands, in pieces
