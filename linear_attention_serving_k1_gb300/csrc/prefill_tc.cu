@@ -189,7 +189,8 @@ constexpr int K1_P = 68;                 // fp32 row pitch of T (16-byte aligned
 constexpr int K1_PL = 68;                // fp32 row pitch of L (16-byte rows: conflict-free float4 stores by rows)
 constexpr uint32_t K1_LM = 0;            // fp32 [64][68]  L (strict lower)
 constexpr uint32_t K1_TM = 17408;        // fp32 [64][68]  T = (I + L)^-1
-constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][16] scratch of the 16 -> 32 merge
+constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][24] scratch of the 16 -> 32 merge
+constexpr int K1_XSP = 24;               // its row pitch (conflict-free fragment loads)
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
 constexpr uint32_t K1_XW = 46080;        // fp32 [32][40] scratch of the 32 -> 64 merge
 constexpr uint32_t K1_RQD = 46080;       // f16 diag(rq): rows i x K = r (64 x 64), over XW after the inverse
@@ -201,7 +202,7 @@ constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (16 KB), b
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
 static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16384 <= K1_XS, "Qg tile between Wk^T and the merge scratch");
 static_assert(K1_LM + 64 * K1_PL * 4 <= K1_TM, "L below T");
-static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2048 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
+static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2 * 16 * K1_XSP * 4 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
@@ -704,35 +705,40 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         *reinterpret_cast<float4 *>(Tm + r * K1_P + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    {   // 16 -> 32, pairs k = 0, 1 (A = block 2k, B = block 2k + 1); thread: pair
-        // k, row i of B, columns j2, j2 + 1 (packed fp32 pairs)
-        const int k2 = tid >> 7, i = (tid >> 3) & 15, j2 = (tid & 7) * 2;
+    if (warp < 4) {
+        // 16 -> 32 on the warp-level tensor-core path: warp w takes pair k = w >> 1
+        // (A = block 2k, B = block 2k + 1) and the 16 x 8 tile of columns
+        // 8 (w & 1) of the pair's 16.  Each warp reads back only its own tile
+        // of X, so a warp barrier separates the two products.
+        const int g = lane >> 2, t = lane & 3, k2 = warp >> 1, n0 = 8 * (warp & 1);
         const int a0 = 32 * k2, b0 = a0 + 16;
-        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
-        const float *lrow = Lm + (b0 + i) * K1_PL + a0;
+        float *xs = Xs + k2 * 16 * K1_XSP;
+        {   // X = L_BA T_AA (T_AA[k][n] = 0 for k < n: k starts at n0)
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *la = Lm + (b0 + g) * K1_PL + a0 + t;
 #pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            const float2 t0 = *reinterpret_cast<const float2 *>(Tm + (a0 + m) * K1_P + a0 + j2);
-            const float2 t1 = *reinterpret_cast<const float2 *>(Tm + (a0 + m + 1) * K1_P + a0 + j2);
-            const float l0 = lrow[m], l1 = lrow[m + 1];
-            s0 = __ffma2_rn(make_float2(l0, l0), t0, s0);
-            s1 = __ffma2_rn(make_float2(l1, l1), t1, s1);
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                if (k0 < n0) continue;
+                const float a[4] = {la[k0], la[8 * K1_PL + k0], la[k0 + 4], la[8 * K1_PL + k0 + 4]};
+                const float b[2] = {Tm[(a0 + k0 + t) * K1_P + a0 + n0 + g], Tm[(a0 + k0 + t + 4) * K1_P + a0 + n0 + g]};
+                mma_tf32x3(d, a, b);
+            }
+            *reinterpret_cast<float2 *>(xs + g * K1_XSP + n0 + 2 * t) = make_float2(d[0], d[1]);
+            *reinterpret_cast<float2 *>(xs + (g + 8) * K1_XSP + n0 + 2 * t) = make_float2(d[2], d[3]);
         }
-        *reinterpret_cast<float2 *>(Xs + (k2 * 16 + i) * 16 + j2) = __fadd2_rn(s0, s1);
-        __syncthreads();
-        // T_BB is unit lower triangular (zeros above its diagonal)
-        s0 = make_float2(0.f, 0.f);
-        s1 = s0;
-        const float *trow = Tm + (b0 + i) * K1_P + b0;
+        __syncwarp();
+        {   // T_BA = -T_BB X (T_BB unit lower triangular, zeros above its diagonal)
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const float *ta = Tm + (b0 + g) * K1_P + b0 + t;
 #pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            const float2 x0 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m) * 16 + j2);
-            const float2 x1 = *reinterpret_cast<const float2 *>(Xs + (k2 * 16 + m + 1) * 16 + j2);
-            s0 = __ffma2_rn(make_float2(trow[m], trow[m]), x0, s0);
-            s1 = __ffma2_rn(make_float2(trow[m + 1], trow[m + 1]), x1, s1);
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                const float a[4] = {ta[k0], ta[8 * K1_P + k0], ta[k0 + 4], ta[8 * K1_P + k0 + 4]};
+                const float b[2] = {xs[(k0 + t) * K1_XSP + n0 + g], xs[(k0 + t + 4) * K1_XSP + n0 + g]};
+                mma_tf32x3(d, a, b);
+            }
+            *reinterpret_cast<float2 *>(Tm + (b0 + g) * K1_P + a0 + n0 + 2 * t) = make_float2(-d[0], -d[1]);
+            *reinterpret_cast<float2 *>(Tm + (b0 + g + 8) * K1_P + a0 + n0 + 2 * t) = make_float2(-d[2], -d[3]);
         }
-        s0 = __fadd2_rn(s0, s1);
-        *reinterpret_cast<float2 *>(Tm + (b0 + i) * K1_P + a0 + j2) = make_float2(-s0.x, -s0.y);
     }
     __syncthreads();
     {   // 32 -> 64 (A = rows 0-31, B = rows 32-63) on the warp-level tensor-core
