@@ -678,25 +678,24 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         bulk_commit();
     }
     // 5. T = (I + L)^-1.  Diagonal 16 x 16 blocks by forward substitution (one
-    //    column per thread, four partial sums per step), then two doubling
-    //    merges, 16 -> 32 and 32 -> 64: for a lower block pair A (top) and B,
-    //    T_BA = -T_BB (L_BA T_AA).
+    //    column per thread), then two doubling merges, 16 -> 32 and 32 -> 64:
+    //    for a lower block pair A (top) and B, T_BA = -T_BB (L_BA T_AA).
     if (tid < 64) {
+        // column c of block blk, right-looking: once entry rr is final it is
+        // taken out of every later row at once, so the dependent chain is one
+        // FMA per row (entries above the diagonal stay zero: they start at
+        // zero and only ever subtract multiples of zeros)
         const int blk = tid >> 4, c = tid & 15, col = 16 * blk + c;
-        float tcol[16];
+        const float *lb = Lm + 16 * blk * (K1_PL + 1);   // L block blk, row stride K1_PL
+        float x[16];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * blk + rr;
-            float x[4] = {(rr == c) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < 16; ++j) x[j] = (j == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int ii = 0; ii < rr; ++ii)   // tcol[ii] = 0 for ii < c: no lane-dependent predicate
-                x[ii & 3] -= Lm[r * K1_PL + 16 * blk + ii] * tcol[ii];
-            tcol[rr] = (rr >= c) ? (x[0] + x[1]) + (x[2] + x[3]) : 0.f;
-        }
-        // stored after the loop: with no store between them, the loads of L
-        // can be issued ahead of the dependent chain
+        for (int rr = 0; rr < 15; ++rr)
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * K1_P + col] = tcol[rr];
+            for (int j = rr + 1; j < 16; ++j) x[j] = fmaf(-lb[j * K1_PL + rr], x[rr], x[j]);
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Tm[(16 * blk + rr) * K1_P + col] = x[rr];
     } else if (tid < 192) {
         // zeros in the 16 x 16 blocks above the diagonal of T_AA and T_BB
         // (rows 0-15 x columns 16-31, rows 32-47 x columns 48-63): the merges
