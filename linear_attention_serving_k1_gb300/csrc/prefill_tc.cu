@@ -435,10 +435,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         mbar_init(&dbar, 1);
         fence_mbar_init();
     }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tm = tmem_sh;
+    // the TMEM address and the barriers are published by the loop's first CTA
+    // barrier (the warps meanwhile compute their gate totals)
+    uint32_t tm = 0;
     bool ok = true;
     bool strong = false;   // a decay factor of this thread's rows left the exact range
     float nsq = 0.f;   // squared row norm of value lane >> 1 (q rows rb .. rb + 7, then k rows)
@@ -458,7 +457,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         // the MMA of the previous half has read the operand tiles
         if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (p == 0 && tid < kC) bs[tid] = beta_r;
+        if (p == 0) fence_before_sync();
         __syncthreads();
+        if (p == 0) {
+            fence_after_sync();
+            tm = tmem_sh;
+        }
         if (p == 1) ok = ok && wflag[0];
         float2 pre = make_float2(0.f, 0.f), last = pre;   // totals of the warps before this one, of all
 #pragma unroll
