@@ -238,7 +238,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
              DevStatus *st, uint32_t wait_limit, const float *__restrict__ conv_w, int conv_width,
-             int conv_silu, const bf16 *__restrict__ conv_in)
+             int conv_silu, const bf16 *__restrict__ conv_in, int ahead)
 {
     if constexpr (kH > 0) H = kH;
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -421,6 +421,29 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const char *slice = base + (((size_t)(t0 + r) * H + h) * kD + 64) * esz;
             prefetch_line_l2(slice);
             if (esz == 4u) prefetch_line_l2(slice + 128);
+        }
+    }
+    // ... and of the first half of the rows of the CTA `ahead` positions later
+    // in the grid (segmented launches; `ahead` is half the SM count): that CTA
+    // starts about half a wave later and then finds its first loads in L2,
+    // instead of every CTA drawing its first 40 KB from HBM as it starts
+    // (which, with the other CTAs doing the same, took about 1.8K cycles).
+    // Prefetching a whole wave ahead, or both halves, measured slower.
+    {
+        const unsigned b2 = blockIdx.x + (unsigned)ahead;
+        if (!kConv && G > 0 && ahead > 0 && b2 < gridDim.x) {
+            const int h2 = (int)(b2 % (unsigned)H), item2 = (int)(b2 / (unsigned)H);
+            const int n2 = item2 / G, lc2 = seg_lo + item2 % G;   // n2 < N (grid = N G H)
+            const int c1 = tab.cu[n2 + 1], t02 = tab.cu[n2] + lc2 * kC;
+            const int r = tid & 63, which = tid >> 6;   // q, k, v, g
+            const char *base = which == 0 ? (const char *)q : which == 1 ? (const char *)k
+                             : which == 2 ? (const char *)v : (const char *)g;
+            const uint32_t esz = which == 3 ? 4u : 2u;
+            if (t02 + r < c1 && (which < 3 || !scalar_gate)) {
+                const char *slice = base + ((size_t)(t02 + r) * H + h2) * kD * esz;
+                prefetch_line_l2(slice);
+                if (esz == 4u) prefetch_line_l2(slice + 128);
+            }
         }
     }
 
@@ -1656,11 +1679,11 @@ void launch_k1(const PrefillArgs &a, unsigned grid, cudaStream_t stream, uint8_t
     if (a.conv_w)
         (h32 ? k1_tc_kernel<true, kH32> : k1_tc_kernel<true, 0>)<<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in);
+            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in, 0);
     else
         (h32 ? k1_tc_kernel<false, kH32> : k1_tc_kernel<false, 0>)<<<grid, K1_THREADS, K1_SMEM, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, nullptr, 0, 0, nullptr);
+            a.wait_limit, nullptr, 0, 0, nullptr, (int)(device_sm_count() / 2));
 }
 // One K2 launch (one chain per CTA or chains in turn; with or without the gate).
 void launch_k2(const PrefillArgs &a, bool multi, unsigned grid, cudaStream_t stream, const uint8_t *ring, int lo,
