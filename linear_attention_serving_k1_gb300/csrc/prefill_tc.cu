@@ -13,7 +13,8 @@
 //       Kd = kh e^-b, Ke = kh e^(b_last - b), gamma = e^b_last
 //       G  = [Kg; Qg] Kd^T                        (one M=128 MMA)
 //       L  = strict-lower(diag(beta) Kg Kd^T), Mc = incl-lower(Qg Kd^T)
-//       T  = (I + L)^-1                            (fp32, blocked, CUDA cores)
+//       T  = (I + L)^-1      (fp32, blocked: diagonal blocks on CUDA cores,
+//                             merges on warp-level tensor-core MMAs)
 //       Wk = T diag(beta) Kg, Uv = T diag(beta) V   (MMAs)
 //       A' = -Ke^T Wk,  Q' = Qg - Mc Wk             (MMAs)
 //   K2  [S_next - Diag(gamma) S | O] = [A' | Ke^T] [S; Uv] , [Q' | Mc] [S; Uv]
