@@ -575,44 +575,49 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         };
         if (clamp) build_rows(std::true_type{});
         else build_rows(std::false_type{});
-        // f16 operand rows d and d + 1, K = rows rb .. rb + 7: the padded tiles
-        // row d, then row d + 1; in Ke'^T lanes 4-7 of each quarter-warp store
-        // row d + 1 first, so that every store instruction covers eight distinct
-        // rows modulo 8 (conflict-free either way).
-        {
-            const uint32_t pa = kmaj_off(d, rb, LBO_KIN, SBO_K64P), pb = kmaj_off(d + 1, rb, LBO_KIN, SBO_K64P);
-            *reinterpret_cast<uint4 *>(sm + K1_KGT + pa) = make_uint4(kg0[0], kg0[1], kg0[2], kg0[3]);
-            *reinterpret_cast<uint4 *>(sm + K1_KGT + pb) = make_uint4(kg1[0], kg1[1], kg1[2], kg1[3]);
-            *reinterpret_cast<uint4 *>(sm + K1_VT + pa) = make_uint4(vf0[0], vf0[1], vf0[2], vf0[3]);
-            *reinterpret_cast<uint4 *>(sm + K1_VT + pb) = make_uint4(vf1[0], vf1[1], vf1[2], vf1[3]);
-            const bool sw = lane & 4;
-            const uint32_t oa = kmaj_off(d + (sw ? 1 : 0), rb, LBO_KIN, SBO_K64);
-            const uint32_t ob = kmaj_off(d + (sw ? 0 : 1), rb, LBO_KIN, SBO_K64);
-            *reinterpret_cast<uint4 *>(sm + K1_KET + oa) =
-                sw ? make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]) : make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]);
-            *reinterpret_cast<uint4 *>(sm + K1_KET + ob) =
-                sw ? make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]) : make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
-        }
-        // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
-        *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
-        *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1) {
-            const bool up = lane & (2 * w);
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-                const float send = up ? sq[i] : sq[i + w], keep = up ? sq[i + w] : sq[i];
-                sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+        // The f16 operand tiles, the parked Qg' rows and the norm exchange, once
+        // the half's Gram product is issued: they overlap it (the product reads
+        // only the tf32 tiles).
+        auto finish_half = [&]() {
+            // f16 operand rows d and d + 1, K = rows rb .. rb + 7: the padded tiles
+            // row d, then row d + 1; in Ke'^T lanes 4-7 of each quarter-warp store
+            // row d + 1 first, so that every store instruction covers eight distinct
+            // rows modulo 8 (conflict-free either way).
+            {
+                const uint32_t pa = kmaj_off(d, rb, LBO_KIN, SBO_K64P), pb = kmaj_off(d + 1, rb, LBO_KIN, SBO_K64P);
+                *reinterpret_cast<uint4 *>(sm + K1_KGT + pa) = make_uint4(kg0[0], kg0[1], kg0[2], kg0[3]);
+                *reinterpret_cast<uint4 *>(sm + K1_KGT + pb) = make_uint4(kg1[0], kg1[1], kg1[2], kg1[3]);
+                *reinterpret_cast<uint4 *>(sm + K1_VT + pa) = make_uint4(vf0[0], vf0[1], vf0[2], vf0[3]);
+                *reinterpret_cast<uint4 *>(sm + K1_VT + pb) = make_uint4(vf1[0], vf1[1], vf1[2], vf1[3]);
+                const bool sw = lane & 4;
+                const uint32_t oa = kmaj_off(d + (sw ? 1 : 0), rb, LBO_KIN, SBO_K64);
+                const uint32_t ob = kmaj_off(d + (sw ? 0 : 1), rb, LBO_KIN, SBO_K64);
+                *reinterpret_cast<uint4 *>(sm + K1_KET + oa) =
+                    sw ? make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]) : make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]);
+                *reinterpret_cast<uint4 *>(sm + K1_KET + ob) =
+                    sw ? make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]) : make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
             }
-        }
-        nsq += sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
-        if (p == 1) {
-            fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
-            if ((lane & 1) == 0) {
-                const int i = lane >> 1, r = rb + (i & 7);
-                (i < 8 ? rq : rk)[r] = r < L ? rsqrtf(nsq + 1e-6f) : 0.f;
+            // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
+            *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
+            *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1) {
+                const bool up = lane & (2 * w);
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const float send = up ? sq[i] : sq[i + w], keep = up ? sq[i + w] : sq[i];
+                    sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+                }
             }
-        }
+            nsq += sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
+            if (p == 1) {
+                fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
+                if ((lane & 1) == 0) {
+                    const int i = lane >> 1, r = rb + (i & 7);
+                    (i < 8 ? rq : rk)[r] = r < L ? rsqrtf(nsq + 1e-6f) : 0.f;
+                }
+            }
+        };
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -627,6 +632,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                          make_desc(b0d + ks * 2 * K1_F32_LBO, K1_F32_LBO, K1_F32_SBO), idesc, p > 0 || ks > 0);
             mma_commit(&mbar);
         }
+        finish_half();
+        fence_async_smem();   // the f16 tiles are read by later products
     }
     if (strong) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
     if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
