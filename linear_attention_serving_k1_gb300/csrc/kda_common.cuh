@@ -206,6 +206,8 @@ cudaError_t enqueue_prefill_tc(PrefillArgs a, cudaStream_t stream);
 cudaError_t launch_prefill_tc_graph(const PrefillArgs &a);
 // Kernel attributes noted by the last failed tensor-core launch on this thread ("" if none).
 const char *launch_failure_detail();
+// Streaming multiprocessors of the current device (cached per device).
+int64_t device_sm_count();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,

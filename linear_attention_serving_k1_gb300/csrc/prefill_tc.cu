@@ -1399,7 +1399,6 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
 
 size_t tc_handoff_bytes_per_chunk() { return REC_BYTES; }
 
-namespace {
 // Streaming multiprocessors of the current device (read once per device); 152,
 // a GB300's count, when no device can be queried (a host-only call without a
 // GPU).
@@ -1422,7 +1421,6 @@ int64_t device_sm_count()
     }
     return n;
 }
-}  // namespace
 
 SegPlan tc_segment_plan(const kda_prefill_desc *d)
 {
