@@ -1047,7 +1047,10 @@ constexpr int K2_STAGES = 2;
 constexpr int kGamSlots = 4;  // gamma vectors kept apart from the stages (ring of 4)
 constexpr uint32_t K2_GAM = K2_STAGES * REC_BYTES;     // fp32 gamma [kGamSlots][128]
 constexpr int K2_STATE_WARPS = 16;
-constexpr uint32_t K2_SMEM = K2_GAM + kGamSlots * 512;
+// per state warp a 1 KB tile that turns its 16 output rows of 32 columns into
+// 16-byte pieces of rows
+constexpr uint32_t K2_OST = K2_GAM + kGamSlots * 512;
+constexpr uint32_t K2_SMEM = K2_OST + K2_STATE_WARPS * 1024;
 constexpr int K2_STATE_THREADS = 32 * K2_STATE_WARPS;
 constexpr int K2_THREADS = K2_STATE_THREADS + 64;   // + the MMA issuer's warp and the copy warp
 static_assert(K2_SMEM <= 227 * 1024 - 1024, "shared memory");
@@ -1333,19 +1336,31 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     }
                 }
 
-                // this chunk's output, while the next state product runs: straight from
-                // registers (shared memory is busy feeding that product), each warp
-                // store covering 64 contiguous bytes of one row
+                // this chunk's output, while the next state product runs: the warp's
+                // 16 rows x 32 columns go through its own shared-memory tile (16-bit
+                // stores, 64 contiguous bytes per row), and leave as 16-byte pieces
+                // of rows, two stores per thread instead of sixteen 2-byte ones (the
+                // narrow stores held the state warps' memory pipe: about 7% of a
+                // one-chain call)
                 const int t0 = seq_t0 + (c_lo + c) * kC;
                 const int L = min(kC, seq_t1 - t0);
                 {
-                    unsigned short *orow = reinterpret_cast<unsigned short *>(out) + ((size_t)(t0 + 16 * qd) * H + h) * kD + e;
-                    const size_t rs = (size_t)H * kD;
+                    unsigned short *ost = reinterpret_cast<unsigned short *>(sm + K2_OST + warp * 1024);
 #pragma unroll
                     for (int rl2 = 0; rl2 < 8; ++rl2) {
-                        if (16 * qd + 2 * rl2 < L) orow[(size_t)(2 * rl2) * rs] = (unsigned short)(ob16[rl2] & 0xFFFFu);
-                        if (16 * qd + 2 * rl2 + 1 < L) orow[(size_t)(2 * rl2 + 1) * rs] = (unsigned short)(ob16[rl2] >> 16);
+                        ost[(2 * rl2) * 32 + lane] = (unsigned short)(ob16[rl2] & 0xFFFFu);
+                        ost[(2 * rl2 + 1) * 32 + lane] = (unsigned short)(ob16[rl2] >> 16);
                     }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int piece = lane + 32 * i, rl = piece >> 2, c8 = 8 * (piece & 3);   // row, 8 columns
+                        const uint4 val = *reinterpret_cast<const uint4 *>(ost + rl * 32 + c8);
+                        if (16 * qd + rl < L)
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(out) +
+                                                       ((size_t)(t0 + 16 * qd + rl) * H + h) * kD + 32 * q4 + c8) = val;
+                    }
+                    __syncwarp();   // the tile is rewritten for the next chunk
                 }
                 // checkpoint after every `stride` tokens of the sequence
                 const int done = (c_lo + c) * kC + L;
