@@ -199,9 +199,9 @@ constexpr int K1_XWP = 40;               // its row pitch (conflict-free fragmen
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
-constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (16 KB), back from the record over T
+constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (SBO_K64P), from registers over T
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
-static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16384 <= K1_XS, "Qg tile between Wk^T and the merge scratch");
+static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16 * SBO_K64P <= K1_XS, "Qg tile between Wk^T and the merge scratch");
 static_assert(K1_LM + 64 * K1_PL * 4 <= K1_TM, "L below T");
 static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2 * 16 * K1_XSP * 4 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
@@ -243,7 +243,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 {
     if constexpr (kH > 0) H = kH;
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t mbar, qbar, abar, dbar;
+    __shared__ uint64_t mbar, abar, dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ __align__(16) float tot[8][64];   // per warp: totals of g over its 8 rows, per channel of the half
     // (16-byte aligned: read as float2 / float4)
@@ -282,11 +282,10 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     const int t0 = cu0 + lc * kC;
     const int L = min(kC, cu1 - t0);
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
-    // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in the record's
-    // A' area (written once the product that reads it back is complete) until a
-    // bulk copy brings it back into shared memory for the products of phase 9
-    uint8_t *qg_park = rec + REC_AP;
-    static_assert(REC_AP + 16384 <= REC_QP, "park area");
+    // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in registers
+    // (each thread's two channels of its 8 rows, per channel half) until the
+    // inverse is done and its shared-memory area is free
+    uint32_t qgk[2][8];
 
     // 0. inputs of the first channel half.  Thread: rows rb .. rb + 7 of its
     //    warp, channels 64 p + 2 lane and + 1 of half p (4-byte bf16 pairs,
@@ -454,7 +453,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     }
     if (tid == 0) {
         mbar_init(&mbar, 1);
-        mbar_init(&qbar, 1);
         mbar_init(&abar, 1);
         mbar_init(&dbar, 1);
         fence_mbar_init();
@@ -597,9 +595,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 *reinterpret_cast<uint4 *>(sm + K1_KET + ob) =
                     sw ? make_uint4(ke0[0], ke0[1], ke0[2], ke0[3]) : make_uint4(ke1[0], ke1[1], ke1[2], ke1[3]);
             }
-            // Qg'^T rows d and d + 1 of the parked tile (global; read back by a bulk copy)
-            *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d, rb, LBO_KIN, SBO_K64)) = make_uint4(qp0[0], qp0[1], qp0[2], qp0[3]);
-            *reinterpret_cast<uint4 *>(qg_park + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64)) = make_uint4(qp1[0], qp1[1], qp1[2], qp1[3]);
+            // Qg'^T rows d and d + 1, kept in registers until phase 7
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                qgk[p][i] = qp0[i];
+                qgk[p][4 + i] = qp1[i];
+            }
 #pragma unroll
             for (int w = 4; w >= 1; w >>= 1) {
                 const bool up = lane & (2 * w);
@@ -611,7 +612,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             }
             nsq += sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
             if (p == 1) {
-                fence_async_global();   // the bulk copy of phase 8 reads both halves' rows through the async proxy
+                // the convolved rows (kConv) were written to the record by plain stores;
+                // a bulk copy overwrites the k' rows after the inverse
+                fence_async_global();
                 if ((lane & 1) == 0) {
                     const int i = lane >> 1, r = rb + (i & 7);
                     (i < 8 ? rq : rk)[r] = r < L ? rsqrtf(nsq + 1e-6f) : 0.f;
@@ -862,12 +865,15 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // the parked Qg'^T tile comes back over T, free now that the inverse is done
-    bool q_issued = false;   // (thread 0) the copy is in flight until qbar completes
-    if (tid == 0 && ok) {
-        mbar_arrive_expect_tx(&qbar, 16384);
-        bulk_g2s(sm + K1_QG, qg_park, 16384, &qbar);
-        q_issued = true;
+    // the Qg'^T tile from registers into shared memory over T, free now that
+    // the inverse is done (8-row groups padded like Kg'^T's: conflict-free)
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int d = 64 * p + 2 * lane;
+        *reinterpret_cast<uint4 *>(sm + K1_QG + kmaj_off(d, rb, LBO_KIN, SBO_K64P)) =
+            make_uint4(qgk[p][0], qgk[p][1], qgk[p][2], qgk[p][3]);
+        *reinterpret_cast<uint4 *>(sm + K1_QG + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64P)) =
+            make_uint4(qgk[p][4], qgk[p][5], qgk[p][6], qgk[p][7]);
     }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
@@ -935,8 +941,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64), committed on its own so
     //    that its readout overlaps the second product; -Mc Wk = -Mc' diag(rk) Wk
     //    (M = 64, N = 128, K = 64) plus diag(rq) Qg' (K = 64) into Q'
-    bool q_landed = false;
-    if (tid == 0 && ok && (q_landed = mbar_wait_bounded(&qbar, 0, wait_limit))) {
+    if (tid == 0 && ok) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
         const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_QG);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
@@ -952,7 +957,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             mma_f16(tm + T1_QP, make_desc(ard + ks * 256, LBO_KIN, SBO_K64),
-                    make_desc(bq + ks * 256, LBO_KIN, SBO_K64), id64, 1);
+                    make_desc(bq + ks * 256, LBO_KIN, SBO_K64P), id64, 1);
         mma_commit(&mbar);
     }
     // (diag(rk) Uv)^T -> record (rows e, K = r) while the products run
@@ -972,7 +977,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     pack_f16x8(u + h8);
         }
     }
-    if (tid == 0) wflag[3] = ok && q_landed && mbar_wait_bounded(&abar, 0, wait_limit);
+    if (tid == 0) wflag[3] = ok && mbar_wait_bounded(&abar, 0, wait_limit);
     __syncthreads();
     fence_after_sync();
     ok = ok && wflag[3];
@@ -1019,7 +1024,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         record_timeout(st);
         mma_commit(&dbar);
         mbar_wait_bounded(&dbar, 0, kDrainLimit);
-        if (q_issued) mbar_wait_bounded(&qbar, 0, kDrainLimit);
     }
     if (tid == 0) bulk_wait_all();
     fence_before_sync();
