@@ -194,14 +194,14 @@ constexpr uint32_t K1_XS = 34816;        // fp32 [2][16][24] scratch of the 16 -
 constexpr int K1_XSP = 24;               // its row pitch (conflict-free fragment loads)
 constexpr uint32_t K1_MC = 37888;        // f16 Mc': rows r x K = i (64 x 64)
 constexpr uint32_t K1_XW = 46080;        // fp32 [32][40] scratch of the 32 -> 64 merge
-constexpr uint32_t K1_RQD = 46080;       // f16 diag(rq): rows i x K = r (64 x 64), over XW after the inverse
 constexpr int K1_XWP = 40;               // its row pitch (conflict-free fragment loads)
 constexpr uint32_t K1_TBK = 0;           // f16 T diag(beta rk): rows r x K = i, over L once T is built
 constexpr uint32_t K1_TBV = 8192;        // f16 T diag(beta)
 constexpr uint32_t K1_WKT = 0;           // f16 (diag(rk) Wk)^T: rows d x K = r, over TB once W is done
-constexpr uint32_t K1_QG = K1_TM;        // f16 Qg'^T: rows d x K = r (SBO_K64P), from registers over T
+constexpr uint32_t K1_QG = K1_TM;        // f16 Qg': rows r of 128 channels, from registers over T
+constexpr int K1_QGP = 136;              // its row pitch in f16 (272 bytes: conflict-free row reads by 16 lanes)
 static_assert(K1_MC + 8192 <= K1_GRAM_END && K1_WKT + 16384 <= K1_MC, "later phases must fit the Gram region");
-static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 16 * SBO_K64P <= K1_XS, "Qg tile between Wk^T and the merge scratch");
+static_assert(K1_WKT + 16384 <= K1_QG && K1_QG + 64 * K1_QGP * 2 <= K1_XS, "Qg tile between Wk^T and the merge scratch");
 static_assert(K1_LM + 64 * K1_PL * 4 <= K1_TM, "L below T");
 static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2 * 16 * K1_XSP * 4 <= K1_MC && K1_XW + 32 * K1_XWP * 4 <= K1_GRAM_END,
               "phase overlap");
@@ -865,16 +865,17 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // the Qg'^T tile from registers into shared memory over T, free now that
-    // the inverse is done (8-row groups padded like Kg'^T's: conflict-free)
+    // Qg' from registers into shared memory over T, free now that the inverse
+    // is done: plain rows (r, 128 channels of f16), read back by the Q' readout
+    // (each register pair holds rows 2i and 2i + 1 of channels d and d + 1)
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const int d = 64 * p + 2 * lane;
-        *reinterpret_cast<uint4 *>(sm + K1_QG + kmaj_off(d, rb, LBO_KIN, SBO_K64P)) =
-            make_uint4(qgk[p][0], qgk[p][1], qgk[p][2], qgk[p][3]);
-        *reinterpret_cast<uint4 *>(sm + K1_QG + kmaj_off(d + 1, rb, LBO_KIN, SBO_K64P)) =
-            make_uint4(qgk[p][4], qgk[p][5], qgk[p][6], qgk[p][7]);
-    }
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t *qrow = reinterpret_cast<uint32_t *>(sm + K1_QG) + (size_t)(rb + 2 * i) * (K1_QGP / 2) + 32 * p + lane;
+            qrow[0] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x5410);
+            qrow[K1_QGP / 2] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x7632);
+        }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
         const uint32_t idesc = idesc_f16(128, 64);
@@ -888,17 +889,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     make_desc(btv + ks * 256, LBO_KIN, SBO_K64), idesc, ks > 0);
         }
         mma_commit(&mbar);
-    }
-    // diag(rq) as an f16 operand tile (rows i, K = r; 64 x 64) for Q' = diag(rq) Qg' - Mc Wk,
-    // while the products run (the merge scratch it overwrites is dead)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        // lanes take consecutive rows i (eight lanes fill 128 contiguous bytes)
-        const int idx = tid + K1_THREADS * h, i = idx & 63, kg = idx >> 6;
-        float dv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dv[j] = (8 * kg + j == i) ? rq[i] : 0.f;
-        *reinterpret_cast<uint4 *>(sm + K1_RQD + kmaj_off(i, 8 * kg, LBO_KIN, SBO_K64)) = pack_f16x8(dv);
     }
     if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
     __syncthreads();
@@ -940,10 +930,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 
     // 9. A' = -Ke'^T diag(rk) Wk (M = 128, N = 128, K = 64), committed on its own so
     //    that its readout overlaps the second product; -Mc Wk = -Mc' diag(rk) Wk
-    //    (M = 64, N = 128, K = 64) plus diag(rq) Qg' (K = 64) into Q'
+    //    (M = 64, N = 128, K = 64), to which the Q' readout adds diag(rq) Qg'
     if (tid == 0 && ok) {
         const uint32_t ake = smem_u32(sm + K1_KET), amc = smem_u32(sm + K1_MC), bw = smem_u32(sm + K1_WKT);
-        const uint32_t ard = smem_u32(sm + K1_RQD), bq = smem_u32(sm + K1_QG);
         const uint32_t id128 = idesc_f16(128, 128), id64 = idesc_f16(64, 128);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -954,10 +943,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         for (int ks = 0; ks < 4; ++ks)
             mma_f16(tm + T1_QP, make_desc(amc + ks * 256, LBO_KIN, SBO_K64),
                     make_desc(bw + ks * 256, LBO_KIN, SBO_K64), id64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tm + T1_QP, make_desc(ard + ks * 256, LBO_KIN, SBO_K64),
-                    make_desc(bq + ks * 256, LBO_KIN, SBO_K64P), id64, 1);
         mma_commit(&mbar);
     }
     // (diag(rk) Uv)^T -> record (rows e, K = r) while the products run
@@ -1000,8 +985,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
     ok = ok && wflag[0];
-    // 11. Q' -> record: the M = 64 accumulator puts row r = 16 q4 + l in lane
-    //     32 q4 + l (l < 16)
+    // 11. Q' = diag(rq) Qg' - Mc Wk -> record: the M = 64 accumulator puts row
+    //     r = 16 q4 + l in lane 32 q4 + l (l < 16); the readout adds rq[r] Qg'[r]
+    //     (fp32) from the plain rows of Qg' in shared memory
     if (ok) {
         const int r = 16 * q4 + lane;
         float a[4][16];
@@ -1009,12 +995,23 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         for (int q = 0; q < 4; ++q) tmem_ld16(tm + lane_base + T1_QP + 64 * ch + 16 * q, a[q]);
         tmem_ld_wait();
         if (lane < 16) {
+            const float rqr = rq[r];
+            const uint4 *qg = reinterpret_cast<const uint4 *>(sm + K1_QG + (size_t)r * K1_QGP * 2 + 64 * ch * 2);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int h8 = 0; h8 < 16; h8 += 8)
+                for (int h8 = 0; h8 < 16; h8 += 8) {
+                    const uint4 g8 = qg[(16 * q + h8) / 8];
+                    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 gf = __half22float2(*reinterpret_cast<const __half2 *>(&gw[j]));
+                        a[q][h8 + 2 * j] = fmaf(rqr, gf.x, a[q][h8 + 2 * j]);
+                        a[q][h8 + 2 * j + 1] = fmaf(rqr, gf.y, a[q][h8 + 2 * j + 1]);
+                    }
                     *reinterpret_cast<uint4 *>(rec + REC_QP + kmaj_off(r, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
                         pack_f16x8(a[q] + h8);
+                }
         }
     }
     if (!ok && tid == 0) {
