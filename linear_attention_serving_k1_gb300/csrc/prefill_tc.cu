@@ -462,7 +462,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     uint32_t tm = 0;
     bool ok = true;
     bool strong = false;   // a decay factor of this thread's rows left the exact range
-    float nsq = 0.f;   // squared row norm of value lane >> 1 (q rows rb .. rb + 7, then k rows)
+    float sqa[8];      // the first half's squared row norms after the exchange across lane bit 4
 
     // 1-3. per channel half p: cumulative gates, decayed operands, partial row
     //      norms; then the half's share of G' = [Kg'; Qg'] Kd'^T (tf32, M = 128,
@@ -501,11 +501,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         const float2 mu2 = make_float2(__expf(ref.x), __expf(ref.y));
         if (warp == 0) *reinterpret_cast<float2 *>(rec + REC_G + d * 4) = __fmul2_rn(mu2, mu2);
         uint32_t kg0[4], kg1[4], vf0[4], vf1[4], ke0[4], ke1[4], qp0[4], qp1[4];
-        // this half's squared row norms, summed over the warp's 32 lanes by
-        // halving exchanges: the exchange across lane bit 4 leaves q of row
-        // rb + j (bit 4 clear) or k (set) in sq[j], bit 3 keeps four of those
-        // rows, and so on, so that lanes 2i and 2i + 1 end with value i (q rows
-        // rb .. rb + 7, then k rows)
+        // this half's squared row norms: the exchange across lane bit 4 leaves q
+        // of row rb + j (bit 4 clear) or k (set) in sq[j]; after the second half
+        // the two halves' values are added and summed over the warp by halving
+        // exchanges (bit 3 keeps four of the rows, and so on), so that lanes 2i
+        // and 2i + 1 end with value i (q rows rb .. rb + 7, then k rows)
         float sq[8];
         const bool up16 = lane & 16;
         // byte offset of (row rb, channels 2 lane and + 1 of the half) in the tf32 K-major tiles
@@ -601,17 +601,22 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 qgk[p][i] = qp0[i];
                 qgk[p][4 + i] = qp1[i];
             }
+            if (p == 0) {
 #pragma unroll
-            for (int w = 4; w >= 1; w >>= 1) {
-                const bool up = lane & (2 * w);
+                for (int j = 0; j < 8; ++j) sqa[j] = sq[j];
+            } else {
 #pragma unroll
-                for (int i = 0; i < w; ++i) {
-                    const float send = up ? sq[i] : sq[i + w], keep = up ? sq[i + w] : sq[i];
-                    sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+                for (int j = 0; j < 8; ++j) sq[j] += sqa[j];
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1) {
+                    const bool up = lane & (2 * w);
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        const float send = up ? sq[i] : sq[i + w], keep = up ? sq[i + w] : sq[i];
+                        sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+                    }
                 }
-            }
-            nsq += sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
-            if (p == 1) {
+                const float nsq = sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);   // row lane >> 1
                 // the convolved rows (kConv) were written to the record by plain stores;
                 // a bulk copy overwrites the k' rows after the inverse
                 fence_async_global();
