@@ -895,10 +895,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
-    if (tid == 0) wflag[2] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
-    __syncthreads();
+    // From here on each thread waits for the products itself (all lanes of a
+    // warp poll together): what follows each wait reads only TMEM and writes
+    // areas no other warp still reads, so no CTA barrier is needed there.
+    ok = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
     fence_after_sync();
-    ok = ok && wflag[2];
 
     // 8. (-diag(rk) Wk)^T -> smem operand (rows d, K = r); Uv^T stays in
     //    registers until the products of phase 9 are issued.  Warp w reads
@@ -967,10 +968,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                     pack_f16x8(u + h8);
         }
     }
-    if (tid == 0) wflag[3] = ok && mbar_wait_bounded(&abar, 0, wait_limit);
-    __syncthreads();
+    ok = ok && mbar_wait_bounded(&abar, 0, wait_limit);
     fence_after_sync();
-    ok = ok && wflag[3];
 
     // 10. A' -> record (rows d, K = d'); columns [64 ch, 64 ch + 64), all four
     //     16-column loads in flight before one wait
@@ -986,10 +985,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 *reinterpret_cast<uint4 *>(rec + REC_AP + kmaj_off(row, 64 * ch + 16 * q + h8, LBO_KIN, SBO_K128)) =
                     pack_f16x8(a[q] + h8);
     }
-    if (tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
-    __syncthreads();
+    ok = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
     fence_after_sync();
-    ok = ok && wflag[0];
     // 11. Q' = diag(rq) Qg' - Mc Wk -> record: the M = 64 accumulator puts row
     //     r = 16 q4 + l in lane 32 q4 + l (l < 16); the readout adds rq[r] Qg'[r]
     //     (fp32) from the plain rows of Qg' in shared memory
@@ -1019,11 +1016,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 }
         }
     }
+    if (!ok && lane == 0) record_timeout(st);   // any warp whose wait gave up
     if (!ok && tid == 0) {
-        // A wait gave up: before the TMEM is freed and the shared memory
-        // handed back, every MMA this thread issued and the parked tile's copy
-        // must have completed (a commit arrives once all earlier MMAs are done).
-        record_timeout(st);
+        // A wait of the issuing thread gave up: before the TMEM is freed and the
+        // shared memory handed back, every MMA it issued must have completed (a
+        // commit arrives once all earlier MMAs are done).
         mma_commit(&dbar);
         mbar_wait_bounded(&dbar, 0, kDrainLimit);
     }
