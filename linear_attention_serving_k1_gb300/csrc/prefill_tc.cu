@@ -644,10 +644,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         fence_async_smem();   // the f16 tiles are read by later products
     }
     if (strong) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
-    if (tid == 0) wflag[1] = ok && mbar_wait_bounded(&mbar, 1, wait_limit);
-    __syncthreads();   // G' complete and seen by all: the Gram region may be reused
+    __syncthreads();   // rq, rk and the f16 tiles of both halves are written
+    ok = ok && mbar_wait_bounded(&mbar, 1, wait_limit);   // G' complete: the Gram region may be reused
     fence_after_sync();
-    ok = ok && wflag[1];
 
     // 4. read G': lane quarter q4 = warp & 3 holds rows 32 q4 .. +31; warps w and
     //    w + 4 take columns [0, 32) and [32, 64).  Rows < 64: Kg' Kd'^T -> L;
@@ -870,17 +869,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __syncthreads();
     fence_after_sync();
 
-    // Qg' from registers into shared memory over T, free now that the inverse
-    // is done: plain rows (r, 128 channels of f16), read back by the Q' readout
-    // (each register pair holds rows 2i and 2i + 1 of channels d and d + 1)
-#pragma unroll
-    for (int p = 0; p < 2; ++p)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t *qrow = reinterpret_cast<uint32_t *>(sm + K1_QG) + (size_t)(rb + 2 * i) * (K1_QGP / 2) + 32 * p + lane;
-            qrow[0] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x5410);
-            qrow[K1_QGP / 2] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x7632);
-        }
     // 7. Wk^T = Kg'^T (T diag(beta rk))^T and Uv^T = V^T (T diag beta)^T  (M = 128, N = 64, K = 64)
     if (tid == 0 && ok) {
         const uint32_t idesc = idesc_f16(128, 64);
@@ -895,6 +883,18 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         }
         mma_commit(&mbar);
     }
+    // Qg' from registers into shared memory over T, free now that the inverse
+    // is done (after the W product is issued): plain rows (r, 128 channels of
+    // f16), read back by the Q' readout (each register pair holds rows 2i and
+    // 2i + 1 of channels d and d + 1)
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t *qrow = reinterpret_cast<uint32_t *>(sm + K1_QG) + (size_t)(rb + 2 * i) * (K1_QGP / 2) + 32 * p + lane;
+            qrow[0] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x5410);
+            qrow[K1_QGP / 2] = __byte_perm(qgk[p][i], qgk[p][4 + i], 0x7632);
+        }
     // From here on each thread waits for the products itself (all lanes of a
     // warp poll together): what follows each wait reads only TMEM and writes
     // areas no other warp still reads, so no CTA barrier is needed there.
