@@ -250,7 +250,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     __shared__ __align__(16) float rq[kC];
     __shared__ __align__(16) float rk[kC];
     __shared__ __align__(16) float bs[kC];
-    __shared__ int wflag[4];           // MMA waits: one thread polls, the barrier releases the rest
 
     // grid: one CTA per (item, head), head fastest (CTAs running together read
     // adjacent 256-byte slices of the same token rows).  G == 0: the item is a
@@ -476,8 +475,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int j = 1; j < 8; ++j) c = __fadd2_rn(c, gv[j]);
             *reinterpret_cast<float2 *>(&tot[warp][2 * lane]) = c;
         }
-        // the MMA of the previous half has read the operand tiles
-        if (p == 1 && tid == 0) wflag[0] = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (p == 0 && tid < kC) bs[tid] = beta_r;
         if (p == 0) fence_before_sync();
         __syncthreads();
@@ -485,7 +482,6 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             fence_after_sync();
             tm = tmem_sh;
         }
-        if (p == 1) ok = ok && wflag[0];
         float2 pre = make_float2(0.f, 0.f), last = pre;   // totals of the warps before this one, of all
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
@@ -571,6 +567,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             ke1[j2 / 2] = pack_f16x2(kex[1][0], kex[1][1]);
         }
         };
+        // the Gram product of the previous half has read the tiles this half
+        // overwrites (each thread waits itself; usually long done)
+        if (p == 1) ok = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (clamp) build_rows(std::true_type{});
         else build_rows(std::false_type{});
         // The f16 operand tiles, the parked Qg' rows and the norm exchange, once
