@@ -572,9 +572,9 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         if (p == 1) ok = ok && mbar_wait_bounded(&mbar, 0, wait_limit);
         if (clamp) build_rows(std::true_type{});
         else build_rows(std::false_type{});
-        // The f16 operand tiles, the parked Qg' rows and the norm exchange, once
-        // the half's Gram product is issued: they overlap it (the product reads
-        // only the tf32 tiles).
+        // The f16 operand tiles, the Qg' rows (kept in registers) and the norm
+        // exchange, once the half's Gram product is issued: they overlap it (the
+        // product reads only the tf32 tiles).
         auto finish_half = [&]() {
             // f16 operand rows d and d + 1, K = rows rb .. rb + 7: the padded tiles
             // row d, then row d + 1; in Ke'^T lanes 4-7 of each quarter-warp store
