@@ -42,6 +42,24 @@
  *     synchronises the stream).
  *   - Supported shapes: Dk == Dv in {64, 128}; chunk == 64; dtype of q, k, v
  *     and out bf16 or fp32; g, beta, states and checkpoints always fp32.
+ *
+ * Debug build (libkda_debug.so: the same sources compiled with -DKDA_DEBUG,
+ * the same symbols and results)
+ *   - Every global index that the kernels derive from data (token rows from
+ *     cu_seqlens, records in the workspace, state, pool-slot and checkpoint
+ *     blocks) is checked against the extent of its buffer before the access.
+ *     An index outside it skips the access (no trap, nothing outside the
+ *     buffer is touched; the results are then undefined) and the first such
+ *     index is recorded in a device word.
+ *   - Every entry point that launched work then synchronises `stream` (not
+ *     while the stream is being captured) and returns KDA_ERR_BOUNDS if a
+ *     check failed, with kda_last_error() naming the buffer, the index and
+ *     the extent (device conditions of the release build, such as those
+ *     kda_prefill_status reports, are reported as there).
+ *   - Environment variable KDA_DEBUG_CLIP_TOKENS=n (debug build only): the
+ *     checks take the token-row buffers of every call (q, k, v, g, beta, out,
+ *     gate) to be n rows shorter than the call's size says, so that a test can
+ *     make the last rows fail the check while the memory behind them exists.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -63,7 +81,8 @@ typedef enum {
     KDA_ERR_CUDA = -3,           /* a CUDA launch or runtime call failed */
     KDA_ERR_CKPT_OVERFLOW = -4,  /* more checkpoints due than ckpt_capacity slots */
     KDA_ERR_WORKSPACE = -5,      /* workspace missing or smaller than required */
-    KDA_ERR_TIMEOUT = -6         /* a bounded device-side wait gave up */
+    KDA_ERR_TIMEOUT = -6,        /* a bounded device-side wait gave up */
+    KDA_ERR_BOUNDS = -7          /* debug build: a global index outside its buffer (access skipped) */
 } kda_status;
 
 typedef enum {

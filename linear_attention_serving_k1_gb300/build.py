@@ -1,8 +1,12 @@
-"""Builds the in-tree CUDA library ``_build/libkda.so`` for sm_103a with nvcc.
+"""Builds the in-tree CUDA library ``_build/libkda.so`` for sm_103a with nvcc,
+and its bounds-checking debug build ``_build/debug/libkda_debug.so`` (the
+same sources with ``-DKDA_DEBUG``: every data-dependent global index checked
+before the access, failures reported by the C ABI as KDA_ERR_BOUNDS).
 
-Each translation unit under ``csrc/`` compiles in parallel to an object file;
-the objects link into one shared library with the CUDA runtime linked
-statically, so the library exports only the C ABI of ``include/kda.h``.
+Each translation unit under ``csrc/`` compiles, for both builds at once, in
+parallel to an object file; each build's objects link into one shared library
+with the CUDA runtime linked statically, so the library exports only the C
+ABI of ``include/kda.h``.
 """
 from __future__ import annotations
 
@@ -17,6 +21,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "libkda_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]
@@ -42,27 +48,44 @@ def library_path() -> str:
     return LIB
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def debug_library_path() -> str:
+    return DEBUG_LIB
+
+
+# (library, object directory, extra nvcc flags) of the two builds
+VARIANTS = ((LIB, BUILD, []), (DEBUG_LIB, DEBUG_BUILD, ["-DKDA_DEBUG"]))
+
+
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
+def is_stale() -> bool:
+    return any(_stale(lib) for lib, _, _ in VARIANTS)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ and link libkda.so (skipped when up to date)."""
-    if not force and not is_stale():
+    """Compile every .cu under csrc/ for both builds and link libkda.so and
+    libkda_debug.so (each skipped when up to date); returns libkda.so's path."""
+    todo = [v for v in VARIANTS if force or _stale(v[0])]
+    if not todo:
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
     nv = nvcc()
     procs = []
-    objs = []
-    for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        log = obj + ".log"
-        cmd = [nv, *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
-        procs.append((src, log, subprocess.Popen(cmd, stdout=open(log, "w"), stderr=subprocess.STDOUT)))
-        objs.append(obj)
+    links = []
+    for lib, objdir, extra in todo:
+        os.makedirs(objdir, exist_ok=True)
+        objs = []
+        for src in sources():
+            obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+            log = obj + ".log"
+            cmd = [nv, *ARCH, *NVCC_FLAGS, *extra, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+            procs.append((src, log, subprocess.Popen(cmd, stdout=open(log, "w"), stderr=subprocess.STDOUT)))
+            objs.append(obj)
+        links.append((lib, objs))
     failed = []
     for src, log, p in procs:
         if p.wait() != 0:
@@ -72,9 +95,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{l}" for s, l in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([nv, *ARCH, "-shared", "--cudart", "static", *objs, "-o", tmp], check=True)
-    os.replace(tmp, LIB)
+    for lib, objs in links:
+        tmp = lib + f".tmp{os.getpid()}"
+        subprocess.run([nv, *ARCH, "-shared", "--cudart", "static", *objs, "-o", tmp], check=True)
+        os.replace(tmp, lib)
     return LIB
 
 

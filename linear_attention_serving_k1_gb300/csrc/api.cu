@@ -1,8 +1,10 @@
 // api.cu -- the C ABI declared in include/kda.h: argument validation,
 // workspace layout and kernel dispatch.  No allocation, no synchronisation
-// (except kda_prefill_status, documented as synchronising).
+// (except kda_prefill_status, documented as synchronising, and every call of
+// the debug build, which waits for its work to read the index checks).
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <string>
@@ -39,6 +41,52 @@ kda_status cuda_fail(cudaError_t e, const char *where)
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Rows by which the debug build's checks take the token-row buffers to be
+// shorter than the call says (KDA_DEBUG_CLIP_TOKENS; 0 in the release build).
+int64_t debug_clip_tokens()
+{
+#ifdef KDA_DEBUG
+    if (const char *e = getenv("KDA_DEBUG_CLIP_TOKENS")) {
+        const long long n = strtoll(e, nullptr, 10);
+        return n > 0 ? (int64_t)n : 0;
+    }
+#endif
+    return 0;
+}
+
+const char *dbg_site_name(int32_t site)
+{
+    switch (site) {
+    case kda::kDbgTokenRow: return "token row";
+    case kda::kDbgRecord: return "K1 -> K2 record";
+    case kda::kDbgState: return "state block";
+    case kda::kDbgCkpt: return "checkpoint block";
+    default: return "index";
+    }
+}
+
+// Debug build: once the call's work on `stream` is done, the first index
+// check that failed in it (KDA_ERR_BOUNDS); `s` otherwise, and always in the
+// release build or while the stream is being captured.
+kda_status debug_finish(kda_status s, cudaStream_t stream)
+{
+    if (!kda::kDebug || s != KDA_OK) return s;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return s;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return s;
+    const cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "debug build: waiting for the call");
+    const kda::DbgWord words[] = {kda::dbg_take_prefill_tc(), kda::dbg_take_prefill_simt(), kda::dbg_take_decode()};
+    for (const kda::DbgWord &w : words)
+        if (w.code != 0)
+            return fail(KDA_ERR_BOUNDS, "debug build: %s index %lld outside [0, %lld); the access was skipped",
+                        dbg_site_name(w.site), (long long)w.index, (long long)w.extent);
+    return s;
+}
 
 struct Layout {
     size_t status, cu, chunk_off, ckpt_off, handoff, carry, total;
@@ -236,20 +284,28 @@ kda_status prefill_call(const void *q, const void *k, const void *v, const float
     a.conv_in = a.conv_w && a.conv_width > 1 ? fused->conv_in : nullptr;
     a.conv_out = a.conv_w && a.conv_width > 1 ? fused->conv_out : nullptr;
     a.stream = (cudaStream_t)stream;
+    {
+        const bool tc = kda::use_tc_path(a.dtype, a.D, a.C);
+        const size_t rec = tc ? kda::tc_handoff_bytes_per_chunk() : kda::simt_handoff_bytes_per_chunk(a.D, a.C);
+        a.bounds.tokens = T - debug_clip_tokens();
+        a.bounds.records = (int64_t)(a.handoff_bytes / rec);
+        a.bounds.states = pool ? pool->slots : a.N;
+        a.bounds.ckpts = pool ? pool->slots : a.ckpt_capacity;
+    }
 
     cudaError_t e;
     if (kda::use_tc_path(a.dtype, a.D, a.C)) {
         e = use_graph ? kda::launch_prefill_tc_graph(a) : kda::enqueue_prefill_tc(a, a.stream);
         if (e != cudaSuccess)
             return fail(KDA_ERR_CUDA, "prefill kernels: %s %s", cudaGetErrorString(e), kda::launch_failure_detail());
-        return KDA_OK;
+        return debug_finish(KDA_OK, a.stream);
     }
     if ((e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), a.stream)) != cudaSuccess) return cuda_fail(e, "status reset");
     if ((e = kda::launch_seq_table(a)) != cudaSuccess) return cuda_fail(e, "sequence table");
     if ((e = kda::launch_prefill_simt(a)) != cudaSuccess)
         return fail(KDA_ERR_CUDA, "prefill kernels: %s", cudaGetErrorString(e));
     if (a.conv_out && (e = kda::launch_conv_tail(a)) != cudaSuccess) return cuda_fail(e, "convolution state");
-    return KDA_OK;
+    return debug_finish(KDA_OK, a.stream);
 }
 }  // namespace kda
 
@@ -333,10 +389,11 @@ kda_status decode_common(const void *q, const void *k, const void *v, const floa
     if (((uintptr_t)state & 15) != 0) return fail(KDA_ERR_INVALID_ARG, "state must be 16-byte aligned");
     if (out == q || out == k || out == v || out == (void *)state)
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
+    const kda::Bounds bd{(int64_t)N * m - debug_clip_tokens(), 0, slots ? pool : N, 0};
     cudaError_t e = kda::launch_decode(q, k, v, g, beta, state, out, N, H, Dk, dtype, slots, pool, m,
-                                       commit, status, (cudaStream_t)stream);
+                                       commit, status, bd, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-    return KDA_OK;
+    return debug_finish(KDA_OK, (cudaStream_t)stream);
 }
 }  // namespace
 
@@ -372,9 +429,11 @@ kda_status kda_decode_fused(const void *q, const void *k, const void *v, const f
     if (out == q || out == k || out == v || out == (void *)state || (gate && out == gate))
         return fail(KDA_ERR_INVALID_ARG, "out aliases an input");
     const kda::DecodeFused f{conv_w, conv_w ? conv_width : 0, conv_silu, conv_w ? conv_state : nullptr, gate};
-    cudaError_t e = kda::launch_decode_fused(q, k, v, g, beta, state, out, N, H, Dk, dtype, f, (cudaStream_t)stream);
+    const kda::Bounds bd{(int64_t)N - debug_clip_tokens(), 0, N, 0};
+    cudaError_t e = kda::launch_decode_fused(q, k, v, g, beta, state, out, N, H, Dk, dtype, f, bd,
+                                             (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-    return KDA_OK;
+    return debug_finish(KDA_OK, (cudaStream_t)stream);
 }
 
 kda_status kda_decode_paged(const void *q, const void *k, const void *v, const float *g,

@@ -37,7 +37,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
               int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status,
-              int ahead, FusedIO fz = FusedIO{})
+              int ahead, Bounds bd, FusedIO fz = FusedIO{})
 {
     const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
@@ -60,11 +60,13 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         const int64_t sl = slots[n];
         if (sl < 0 || sl >= pool) {
             for (int t = 0; t < m; ++t)
-                if (tid < D) out[((n * m + t) * H + hh) * D + tid] = from_f32<T>(0.f);
+                if (tid < D && dbg_in((int64_t)(n * m + t), bd.tokens, kDbgTokenRow))
+                    out[((n * m + t) * H + hh) * D + tid] = from_f32<T>(0.f);
             return;
         }
         sblock = (size_t)sl * H + hh;
     }
+    if (!dbg_in((int64_t)sblock, bd.states * H, kDbgState)) return;
     // The sequence's m tokens run one after another with the state in
     // registers; the state after `ncommit` of them is written back.
     const int ncommit = (MULTI && commit) ? min(max(commit[n], 0), m) : m;
@@ -85,7 +87,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             const int64_t sl2 = slots[head2 / (size_t)H];
             sb2 = (sl2 >= 0 && sl2 < pool) ? sl2 * H + (int64_t)(head2 % (size_t)H) : -1;
         }
-        if (sb2 >= 0) {
+        if (sb2 >= 0 && dbg_in(sb2, bd.states * H, kDbgState)) {
             const char *nx = reinterpret_cast<const char *>(state + (size_t)sb2 * D * D);
             for (int i = tid; i < D * D * 4 / 128; i += THREADS)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + (size_t)i * 128));
@@ -108,6 +110,9 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     __shared__ float4 red_q[RPI][C4];
 
     for (int t = 0; t < m; ++t) {
+        // (debug build) a token row outside the token buffers: the whole CTA
+        // skips the token (a uniform condition)
+        if (!dbg_in((int64_t)(n * m + t), bd.tokens, kDbgTokenRow)) continue;
         const size_t tok = (n * m + t) * H + hh;   // token-head row of q, k, v, g, beta, out
         // Token vectors and the two L2 norms (fp32).
         float qv = 0.f, kv = 0.f, vconv = 0.f;
@@ -225,7 +230,7 @@ template <int D, typename T>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, float *state, void *out, int N, int H,
                      const int32_t *slots, int64_t pool, int m, const int32_t *commit, int32_t *status,
-                     cudaStream_t st)
+                     const Bounds &bd, cudaStream_t st)
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
@@ -233,11 +238,11 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
     if (m == 1 && !commit)
         decode_kernel<D, T, THREADS, false><<<blocks, THREADS, 0, st>>>(
             (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr,
-            status, ahead);
+            status, ahead, bd);
     else
         decode_kernel<D, T, THREADS, true><<<blocks, THREADS, 0, st>>>(
             (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, m, commit,
-            status, ahead);
+            status, ahead, bd);
     return cudaGetLastError();
 }
 
@@ -245,45 +250,49 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
 
 template <int D, typename T>
 cudaError_t launch_fused_t(const void *q, const void *k, const void *v, const float *g, const float *beta,
-                           float *state, void *out, int N, int H, const DecodeFused &f, cudaStream_t st)
+                           float *state, void *out, int N, int H, const DecodeFused &f, const Bounds &bd,
+                           cudaStream_t st)
 {
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const FusedIO fz{f.conv_w, f.conv_width, f.conv_silu, f.conv_state, f.gate};
     decode_kernel<D, T, THREADS, false, true><<<(unsigned)((size_t)N * H), THREADS, 0, st>>>(
         (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, nullptr, H, 0, 1, nullptr, nullptr,
-        (int)device_sm_count(), fz);
+        (int)device_sm_count(), bd, fz);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode_fused(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, float *state, void *out, int N, int H, int D,
-                                kda_dtype dtype, const DecodeFused &f, cudaStream_t stream)
+                                kda_dtype dtype, const DecodeFused &f, const Bounds &bd, cudaStream_t stream)
 {
     if ((size_t)N * H == 0) return cudaSuccess;
     if (D == 128)
         return dtype == KDA_DTYPE_BF16
-                   ? launch_fused_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, stream)
-                   : launch_fused_t<128, float>(q, k, v, g, beta, state, out, N, H, f, stream);
-    return dtype == KDA_DTYPE_BF16 ? launch_fused_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, stream)
-                                   : launch_fused_t<64, float>(q, k, v, g, beta, state, out, N, H, f, stream);
+                   ? launch_fused_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, bd, stream)
+                   : launch_fused_t<128, float>(q, k, v, g, beta, state, out, N, H, f, bd, stream);
+    return dtype == KDA_DTYPE_BF16
+               ? launch_fused_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, f, bd, stream)
+               : launch_fused_t<64, float>(q, k, v, g, beta, state, out, N, H, f, bd, stream);
 }
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
-                          const int32_t *commit, int32_t *status, cudaStream_t stream)
+                          const int32_t *commit, int32_t *status, const Bounds &bd, cudaStream_t stream)
 {
     if ((size_t)N * H == 0 || m == 0) return cudaSuccess;
     if (D == 128)
         return dtype == KDA_DTYPE_BF16
                    ? launch_t<128, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit,
-                                                  status, stream)
+                                                  status, bd, stream)
                    : launch_t<128, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status,
-                                          stream);
+                                          bd, stream);
     return dtype == KDA_DTYPE_BF16
                ? launch_t<64, __nv_bfloat16>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status,
-                                             stream)
-               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status, stream);
+                                             bd, stream)
+               : launch_t<64, float>(q, k, v, g, beta, state, out, N, H, slots, pool, m, commit, status, bd, stream);
 }
+
+KDA_DBG_TAKE(dbg_take_decode)
 
 }  // namespace kda

@@ -41,6 +41,83 @@ __device__ __forceinline__ void record_status(DevStatus *st, int32_t code)
     atomicCAS(&st->code, 0, code);
 }
 
+// ------------------------------------------------------------ debug build
+// Compiled with -DKDA_DEBUG, the kernels check every global index they derive
+// from data against the extent of its buffer before the access; an index
+// outside it skips the access and the first one is recorded in a device word
+// of its translation unit, which the entry point reads once the stream is
+// synchronised.  Without KDA_DEBUG every check is the constant `true`.
+struct Bounds {
+    int64_t tokens;      // token rows of q, k, v, g, beta, out, gate (each row H x D)
+    int64_t records;     // K1 -> K2 records (per chunk and head) the workspace holds
+    int64_t states;      // [H, D, D] blocks of the initial / final states (N, or the pool's slots)
+    int64_t ckpts;       // [H, D, D] checkpoint blocks (the capacity, or the pool's slots)
+};
+enum DbgSite : int32_t { kDbgTokenRow = 1, kDbgRecord = 2, kDbgState = 3, kDbgCkpt = 4 };
+struct DbgWord {
+    int32_t code;        // 0, or KDA_ERR_BOUNDS once a check failed
+    int32_t site;        // DbgSite of the first failed check
+    int64_t index, extent;
+};
+#ifdef KDA_DEBUG
+constexpr bool kDebug = true;
+static __device__ DbgWord g_dbg;
+#else
+constexpr bool kDebug = false;
+#endif
+
+// True when 0 <= i < n; otherwise (debug build) records the first such index.
+__device__ __forceinline__ bool dbg_in(int64_t i, int64_t n, DbgSite site)
+{
+#ifdef KDA_DEBUG
+    if (i >= 0 && i < n) return true;
+    if (atomicCAS(&g_dbg.code, 0, (int32_t)KDA_ERR_BOUNDS) == 0) {
+        g_dbg.site = site;
+        g_dbg.index = i;
+        g_dbg.extent = n;
+    }
+    return false;
+#else
+    (void)i; (void)n; (void)site;
+    return true;
+#endif
+}
+
+// Rows of a block of `rows` token rows from row t0 that lie inside the token
+// buffers: `rows` itself, or (debug build) fewer, recording the first row past
+// the end.
+__device__ __forceinline__ int dbg_rows(int64_t t0, int rows, const Bounds &bd)
+{
+    if constexpr (kDebug) {
+        if (rows > 0 && !dbg_in(t0 + rows - 1, bd.tokens, kDbgTokenRow)) {
+            const int64_t r = bd.tokens - t0;
+            return r < 0 ? 0 : (int)r;
+        }
+    }
+    return rows;
+}
+
+// Defines `DbgWord name()`, which reads and clears this translation unit's
+// device word (host side; the stream must be synchronised), or returns a
+// cleared word without KDA_DEBUG.
+#ifdef KDA_DEBUG
+#define KDA_DBG_TAKE(name)                                                  \
+    DbgWord name()                                                          \
+    {                                                                       \
+        DbgWord w{}, z{};                                                   \
+        if (cudaMemcpyFromSymbol(&w, g_dbg, sizeof w) != cudaSuccess ||     \
+            cudaMemcpyToSymbol(g_dbg, &z, sizeof z) != cudaSuccess)         \
+            (void)cudaGetLastError();                                       \
+        return w;                                                           \
+    }
+#else
+#define KDA_DBG_TAKE(name) \
+    DbgWord name() { return DbgWord{}; }
+#endif
+DbgWord dbg_take_prefill_tc();
+DbgWord dbg_take_prefill_simt();
+DbgWord dbg_take_decode();
+
 // Largest magnitude of the exponent of one factor of the chunked form's
 // decayed Gram product.  Per key channel the in-chunk log-decays b_r are
 // referred to the midpoint B of their range (b_r - B and B - b_r), so the
@@ -114,6 +191,7 @@ struct PrefillArgs {
     // each sequence (NULL: zeros) and, written at the end of the call, after it
     const void *conv_in;
     void *conv_out;
+    Bounds bounds;               // extents the debug build checks indices against
     cudaStream_t stream;
 };
 
@@ -211,7 +289,7 @@ int64_t device_sm_count();
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int N, int H, int D,
                           kda_dtype dtype, const int32_t *slots, int64_t pool, int m,
-                          const int32_t *commit, int32_t *status, cudaStream_t stream);
+                          const int32_t *commit, int32_t *status, const Bounds &bd, cudaStream_t stream);
 // The fused decode step (kda_decode_fused): convolution with a per-sequence
 // history, the step, the output gate.
 struct DecodeFused {
@@ -222,6 +300,6 @@ struct DecodeFused {
 };
 cudaError_t launch_decode_fused(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, float *state, void *out, int N, int H, int D,
-                                kda_dtype dtype, const DecodeFused &f, cudaStream_t stream);
+                                kda_dtype dtype, const DecodeFused &f, const Bounds &bd, cudaStream_t stream);
 
 }  // namespace kda

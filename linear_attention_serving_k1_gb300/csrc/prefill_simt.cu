@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(kThreads)
 k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, int N, int H,
                SeqTable tab, float *__restrict__ handoff, int scalar_gate, DevStatus *st,
-               const float *__restrict__ conv_w, int conv_width, int conv_silu, const T *__restrict__ conv_in)
+               const float *__restrict__ conv_w, int conv_width, int conv_silu, const T *__restrict__ conv_in,
+               Bounds bd)
 {
     constexpr int P = D + 1;   // padded row pitch (bank-conflict free columns)
     extern __shared__ float smem[];
@@ -116,7 +117,10 @@ k1_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__rest
     const int n = find_seq(tab.chunk_off, N, gc);
     const int seq_t0 = tab.cu[n];
     const int t0 = tab.cu[n] + (gc - tab.chunk_off[n]) * kC;
-    const int L = min(kC, tab.cu[n + 1] - t0);
+    // (debug build: rows past the token buffers' end count as rows past the
+    // sequence's end, and a record outside the workspace is not written)
+    const int L = dbg_rows(t0, min(kC, tab.cu[n + 1] - t0), bd);
+    if (!dbg_in((int64_t)gc * H + h, bd.records, kDbgRecord)) return;
     Handoff ho = handoff_at(handoff, (size_t)gc * H + h, D);
 
     // 1. rows: qh, kh (normalised, one warp per row), v, beta.  Rows >= L are zero.
@@ -260,7 +264,7 @@ constexpr int kBV = 32;
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads)
 k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__ handoff,
-               T *__restrict__ out, const T *__restrict__ gate)
+               T *__restrict__ out, const T *__restrict__ gate, Bounds bd)
 {
     constexpr int P = D + 1;
     constexpr int NB = D / kBV;
@@ -281,8 +285,10 @@ k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__
     // this CTA's column block of the chain's initial and final states (dense
     // arrays or pool slots)
     const size_t DD = (size_t)D * D;
-    const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
-    const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
+    int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
+    int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
+    if (is >= 0 && !dbg_in(is, bd.states, kDbgState)) is = -1;
+    if (fs >= 0 && !dbg_in(fs, bd.states, kDbgState)) fs = -1;
     const float *init_blk = is >= 0 ? io.init + ((size_t)is * H + h) * DD + jb * kBV : nullptr;
     float *fin_blk = fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD + jb * kBV : nullptr;
     const int stride = io.stride;
@@ -299,6 +305,8 @@ k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__
         const int lc = gc - c_begin;
         const int t0 = seq_t0 + lc * kC;
         const int L = min(kC, seq_t1 - t0);
+        if (!dbg_in((int64_t)gc * H + h, bd.records, kDbgRecord)) break;   // uniform over the CTA
+        const int Lo = dbg_rows(t0, L, bd);   // output rows inside the token buffers (L but in a debug build)
         const float *p = handoff + ((size_t)gc * H + h) * handoff_floats(D);
         const float *hQg = p, *hWk = p + kC * D, *hUv = p + 2 * kC * D, *hKe = p + 3 * kC * D;
         const float *hM = p + 4 * kC * D, *hgl = hM + kC * kC;
@@ -323,7 +331,7 @@ k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__
         }
         __syncthreads();
         // O = Qg S0 + M W
-        for (int r = rgrp; r < L; r += kThreads / kBV) {
+        for (int r = rgrp; r < Lo; r += kThreads / kBV) {
             float acc = 0.f;
             for (int d = 0; d < D; ++d) acc += Qg[r * P + d] * Ss[d * kBV + j];
             for (int i = 0; i <= r; ++i) acc += Ms[r * (kC + 1) + i] * Ws[i * kBV + j];
@@ -343,7 +351,7 @@ k2_simt_kernel(StateIO io, int N, int H, SeqTable tab, const float *__restrict__
         if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
             const int64_t jc = (int64_t)tab.ckpt_off[n] + done / stride - 1;
             const int64_t ps = jc < io.capacity ? pool_slot(io.ckpt_slots, jc, io.pool) : -1;
-            if (ps >= 0) {
+            if (ps >= 0 && dbg_in(ps, bd.ckpts, kDbgCkpt)) {
                 __syncthreads();
                 float *dst = io.ckpts + ((size_t)ps * H + h) * DD + jb * kBV;
                 for (int i = tid; i < D * kBV; i += kThreads)
@@ -375,12 +383,13 @@ cudaError_t launch_simt_t(const PrefillArgs &a)
         k1_simt_kernel<D, T><<<g1, kThreads, sm1, a.stream>>>(
             (const T *)a.q, (const T *)a.k, (const T *)a.v, a.g, a.beta, a.N, a.H, a.tab,
             (float *)a.handoff, a.scalar_gate ? 1 : 0, a.status, a.conv_w, a.conv_width, a.conv_silu,
-            (const T *)a.conv_in);
+            (const T *)a.conv_in, a.bounds);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const unsigned g2 = (unsigned)((size_t)a.N * a.H * (D / kBV));
     k2_simt_kernel<D, T><<<g2, kThreads, sm2, a.stream>>>(state_io(a), a.N, a.H, a.tab,
-                                                           (const float *)a.handoff, (T *)a.out, (const T *)a.gate);
+                                                           (const float *)a.handoff, (T *)a.out, (const T *)a.gate,
+                                                           a.bounds);
     return cudaGetLastError();
 }
 
@@ -395,7 +404,8 @@ size_t simt_handoff_bytes_per_chunk(int D, int /*C*/) { return sizeof(float) * h
 // history buffer itself.
 template <typename T>
 __global__ void conv_tail_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                                 const T *conv_in, T *conv_out, int N, int H, int D, int W, SeqTable tab)
+                                 const T *conv_in, T *conv_out, int N, int H, int D, int W, SeqTable tab,
+                                 Bounds bd)
 {
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const int len = tab.cu[n + 1] - tab.cu[n];
@@ -405,7 +415,9 @@ __global__ void conv_tail_kernel(const T *__restrict__ q, const T *__restrict__ 
         T vals[kConvTaps - 1];
         for (int j = 0; j < W - 1; ++j) {
             const int p = len - (W - 1) + j;   // position in the sequence
-            if (p >= 0) vals[j] = x[((size_t)(tab.cu[n] + p) * H + h) * D + c];
+            if (p >= 0)
+                vals[j] = dbg_in((int64_t)tab.cu[n] + p, bd.tokens, kDbgTokenRow)
+                              ? x[((size_t)(tab.cu[n] + p) * H + h) * D + c] : from_f32<T>(0.f);
             else if (conv_in)
                 vals[j] = conv_in[((((size_t)n * 3 + t) * (W - 1) + (W - 1 + p)) * H + h) * D + c];
             else vals[j] = from_f32<T>(0.f);
@@ -421,12 +433,13 @@ cudaError_t launch_conv_tail(const PrefillArgs &a)
     if (a.dtype == KDA_DTYPE_BF16)
         conv_tail_kernel<__nv_bfloat16><<<grid, 128, 0, a.stream>>>(
             (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v,
-            (const __nv_bfloat16 *)a.conv_in, (__nv_bfloat16 *)a.conv_out, a.N, a.H, a.D, a.conv_width, a.tab);
+            (const __nv_bfloat16 *)a.conv_in, (__nv_bfloat16 *)a.conv_out, a.N, a.H, a.D, a.conv_width, a.tab,
+            a.bounds);
     else
         conv_tail_kernel<float><<<grid, 128, 0, a.stream>>>((const float *)a.q, (const float *)a.k,
                                                              (const float *)a.v, (const float *)a.conv_in,
                                                              (float *)a.conv_out, a.N, a.H, a.D, a.conv_width,
-                                                             a.tab);
+                                                             a.tab, a.bounds);
     return cudaGetLastError();
 }
 
@@ -445,5 +458,7 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a)
     return a.dtype == KDA_DTYPE_BF16 ? launch_simt_t<64, __nv_bfloat16>(a)
                                      : launch_simt_t<64, float>(a);
 }
+
+KDA_DBG_TAKE(dbg_take_prefill_simt)
 
 }  // namespace kda

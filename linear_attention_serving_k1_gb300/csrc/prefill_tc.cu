@@ -239,7 +239,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
              const float *__restrict__ g, const float *__restrict__ beta, int N, int H, SeqTable tab,
              uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot, int scalar_gate,
              DevStatus *st, uint32_t wait_limit, const float *__restrict__ conv_w, int conv_width,
-             int conv_silu, const bf16 *__restrict__ conv_in, int ahead)
+             int conv_silu, const bf16 *__restrict__ conv_in, int ahead, Bounds bd)
 {
     if constexpr (kH > 0) H = kH;
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -279,7 +279,11 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         ri = ((size_t)slot * N + n) * slot_chunks + item % G;
     }
     const int t0 = cu0 + lc * kC;
-    const int L = min(kC, cu1 - t0);
+    // (debug build: rows past the token buffers' end count as rows past the
+    // sequence's end, and a chunk with none left, or a record outside the
+    // workspace, is skipped)
+    const int L = dbg_rows(t0, min(kC, cu1 - t0), bd);
+    if (kDebug && (L <= 0 || !dbg_in((int64_t)(ri * H + h), bd.records, kDbgRecord))) return;
     uint8_t *rec = ring + (ri * H + h) * REC_BYTES;
     // Qg' as an f16 operand tile (rows d, K = r; 16 KB) waits in registers
     // (each thread's two channels of its 8 rows, per channel half) until the
@@ -372,10 +376,12 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             for (int i = 0; i < kConvTaps; ++i) {
                 w[i] = *reinterpret_cast<const float2 *>(taps + (t * kConvTaps + i) * kD + cp);
                 // window slots 1 .. 3 start with rows r0 - 3 .. r0 - 1 (slot 0 is
-                // shifted out before first use); each step shifts and appends a row
+                // shifted out before first use); each step shifts and appends a row.
+                // Rows from L on feed only outputs that are zero and are not read
+                // (in the sequence's last chunk they may lie past the buffers' end).
                 const int rr = r0 - kConvTaps + i, pos = lc * kC + rr;   // position in the sequence
                 uint32_t u = 0u;
-                if (i > 0 && pos >= 0)
+                if (i > 0 && pos >= 0 && rr < L)
                     u = __ldg(reinterpret_cast<const unsigned int *>(src + (ptrdiff_t)rr * (ptrdiff_t)rstride + cp));
                 else if (i > 0 && conv_in && pos >= -(conv_width - 1))   // the history before the sequence
                     u = __ldg(reinterpret_cast<const unsigned int *>(
@@ -438,7 +444,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
             const char *base = which == 0 ? (const char *)q : which == 1 ? (const char *)k
                              : which == 2 ? (const char *)v : (const char *)g;
             const uint32_t esz = which == 3 ? 4u : 2u;
-            if (t02 + r < c1 && (which < 3 || !scalar_gate)) {
+            if (t02 + r < c1 && (which < 3 || !scalar_gate) && dbg_in(t02 + r, bd.tokens, kDbgTokenRow)) {
                 const char *slice = base + ((size_t)(t02 + r) * H + h2) * kD * esz;
                 prefetch_line_l2(slice);
                 if (esz == 4u) prefetch_line_l2(slice + 128);
@@ -1080,7 +1086,7 @@ __global__ void __maxnreg__(96)   // 18 warps: at most 5 per SM sub-partition x 
 k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
              const uint8_t *__restrict__ ring, int seg_lo, int G, int slot_chunks, int slot,
              float *__restrict__ carry, bf16 *__restrict__ out, DevStatus *st, uint32_t wait_limit,
-             const bf16 *__restrict__ gate)
+             const bf16 *__restrict__ gate, Bounds bd)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t full[K2_STAGES], fullr[K2_STAGES], empty[K2_STAGES], emptyr[K2_STAGES], gfull[kGamSlots],
@@ -1155,11 +1161,11 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
         // live across the chunk loop
         auto init_block = [&]() -> const float * {
             const int64_t is = io.init ? pool_slot(io.init_slots, n, io.pool) : -1;
-            return is >= 0 ? io.init + ((size_t)is * H + h) * DD : nullptr;
+            return is >= 0 && dbg_in(is, bd.states, kDbgState) ? io.init + ((size_t)is * H + h) * DD : nullptr;
         };
         auto final_block = [&]() -> float * {
             const int64_t fs = io.fin ? pool_slot(io.final_slots, n, io.pool) : -1;
-            return fs >= 0 ? io.fin + ((size_t)fs * H + h) * DD : nullptr;
+            return fs >= 0 && dbg_in(fs, bd.states, kDbgState) ? io.fin + ((size_t)fs * H + h) * DD : nullptr;
         };
         const size_t rec_base = G == 0 ? (size_t)tab.chunk_off[n] : ((size_t)slot * N + n) * slot_chunks;
         if (nch == 0) {   // nothing of this sequence here; an empty sequence keeps its state
@@ -1184,6 +1190,12 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
             // most of the time; gamma goes into its own slot with its own barrier
             // (the state threads read it later).
             static_assert(REC_KM + 40960 == REC_G && REC_AP == 0, "record parts");
+            // (debug build) the chain's records lie inside the workspace, else
+            // nothing is copied and the CTA's other roles are told to stop
+            if (!dbg_in((int64_t)((rec_base + nch - 1) * H + h), bd.records, kDbgRecord)) {
+                *abort_v = 1;
+                alive = false;
+            }
             for (int c = 0; c < nch && alive; ++c) {
                 const int cc = base + c, s = cc % K2_STAGES;
                 if (cc >= K2_STAGES &&
@@ -1281,7 +1293,9 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     const unsigned short *zrow = reinterpret_cast<const unsigned short *>(gate) +
                                                  ((size_t)(tz + 16 * qd) * H + h) * kD + e;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) zg[i] = 16 * qd + i < Lz ? zrow[(size_t)i * H * kD] : 0u;
+                    for (int i = 0; i < 16; ++i)
+                        zg[i] = 16 * qd + i < Lz && dbg_in(tz + 16 * qd + i, bd.tokens, kDbgTokenRow)
+                                    ? zrow[(size_t)i * H * kD] : 0u;
                 }
                 // gamma has landed (its slot's barrier cannot run ahead: slot cc % 4
                 // is refilled only after the product of chunk cc + 2, which needs
@@ -1358,7 +1372,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                     for (int i = 0; i < 2; ++i) {
                         const int piece = lane + 32 * i, rl = piece >> 2, c8 = 8 * (piece & 3);   // row, 8 columns
                         const uint4 val = *reinterpret_cast<const uint4 *>(ost + rl * 32 + c8);
-                        if (16 * qd + rl < L)
+                        if (16 * qd + rl < L && dbg_in(t0 + 16 * qd + rl, bd.tokens, kDbgTokenRow))
                             *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(out) +
                                                        ((size_t)(t0 + 16 * qd + rl) * H + h) * kD + 32 * q4 + c8) = val;
                     }
@@ -1369,7 +1383,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 if (stride > 0 && io.ckpts && L == kC && done % stride == 0) {
                     const int64_t jc = (int64_t)tab.ckpt_off[n] + done / stride - 1;
                     const int64_t ps = jc < io.capacity ? pool_slot(io.ckpt_slots, jc, io.pool) : -1;
-                    if (ps >= 0) {
+                    if (ps >= 0 && dbg_in(ps, bd.ckpts, kDbgCkpt)) {
                         float *dst = io.ckpts + ((size_t)ps * H + h) * DD + e;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) dst[(size_t)(32 * qd + j) * kD] = S[j];
@@ -1702,11 +1716,11 @@ void launch_k1(const PrefillArgs &a, unsigned grid, cudaStream_t stream, uint8_t
     if (a.conv_w)
         (h32 ? k1_tc_kernel<true, kH32> : k1_tc_kernel<true, 0>)<<<grid, K1_THREADS, K1_SMEM + K1_TAPS_BYTES, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in, 0);
+            a.wait_limit, a.conv_w, a.conv_width, a.conv_silu, (const bf16 *)a.conv_in, 0, a.bounds);
     else
         (h32 ? k1_tc_kernel<false, kH32> : k1_tc_kernel<false, 0>)<<<grid, K1_THREADS, K1_SMEM, stream>>>(
             q, k, v, a.g, a.beta, a.N, a.H, a.tab, ring, lo, cnt, G, slot, a.scalar_gate ? 1 : 0, a.status,
-            a.wait_limit, nullptr, 0, 0, nullptr, (int)(device_sm_count() / 2));
+            a.wait_limit, nullptr, 0, 0, nullptr, (int)(device_sm_count() / 2), a.bounds);
 }
 // One K2 launch (one chain per CTA or chains in turn; with or without the gate).
 void launch_k2(const PrefillArgs &a, bool multi, unsigned grid, cudaStream_t stream, const uint8_t *ring, int lo,
@@ -1717,16 +1731,16 @@ void launch_k2(const PrefillArgs &a, bool multi, unsigned grid, cudaStream_t str
     const StateIO io = state_io(a);
     if (multi && gate)
         k2_tc_kernel<true, true><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
-                                                                         carry, out, a.status, a.wait_limit, gate);
+                                                                         carry, out, a.status, a.wait_limit, gate, a.bounds);
     else if (multi)
         k2_tc_kernel<true, false><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
-                                                                          carry, out, a.status, a.wait_limit, nullptr);
+                                                                          carry, out, a.status, a.wait_limit, nullptr, a.bounds);
     else if (gate)
         k2_tc_kernel<false, true><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
-                                                                          carry, out, a.status, a.wait_limit, gate);
+                                                                          carry, out, a.status, a.wait_limit, gate, a.bounds);
     else
         k2_tc_kernel<false, false><<<grid, K2_THREADS, K2_SMEM, stream>>>(io, a.N, a.H, a.tab, ring, lo, cnt, G, slot,
-                                                                           carry, out, a.status, a.wait_limit, nullptr);
+                                                                           carry, out, a.status, a.wait_limit, nullptr, a.bounds);
 }
 }  // namespace
 
@@ -1783,5 +1797,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a)
     if (ej == cudaSuccess) ej = cudaStreamWaitEvent(a.stream, c->join, 0);
     return e != cudaSuccess ? e : ej;
 }
+
+KDA_DBG_TAKE(dbg_take_prefill_tc)
 
 }  // namespace kda

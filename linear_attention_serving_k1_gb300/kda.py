@@ -1,11 +1,14 @@
 """Thin Python binding of the C ABI in include/kda.h (argument marshalling only).
 
-Every step of the computation runs in the CUDA kernels of ``_build/libkda.so``;
-PyTorch only provides device memory and the current stream.  There is no CPU
-fallback: if the library is missing or no GPU is present, calls raise.
+Every step of the computation runs in the CUDA kernels of ``_build/libkda.so``
+(or, inside ``using_library(load_debug_library())``, of its bounds-checking
+debug build); PyTorch only provides device memory and the current stream.
+There is no CPU fallback: if the library is missing or no GPU is present,
+calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -16,7 +19,8 @@ from . import build as _build
 
 KDA_OK = 0
 STATUS_NAMES = {0: "KDA_OK", -1: "KDA_ERR_INVALID_ARG", -2: "KDA_ERR_UNSUPPORTED", -3: "KDA_ERR_CUDA",
-                -4: "KDA_ERR_CKPT_OVERFLOW", -5: "KDA_ERR_WORKSPACE", -6: "KDA_ERR_TIMEOUT"}
+                -4: "KDA_ERR_CKPT_OVERFLOW", -5: "KDA_ERR_WORKSPACE", -6: "KDA_ERR_TIMEOUT",
+                -7: "KDA_ERR_BOUNDS"}
 STATUS_CODES = {v: k for k, v in STATUS_NAMES.items()}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 
@@ -90,6 +94,25 @@ def load_library(path: Optional[str] = None):
     if path == _build.library_path():
         _lib = lib
     return lib
+
+
+def load_debug_library():
+    """Load the debug build libkda_debug.so (same ABI; every data-dependent
+    global index checked, failures returned as KDA_ERR_BOUNDS)."""
+    return load_library(_build.debug_library_path())
+
+
+@contextlib.contextmanager
+def using_library(lib):
+    """Route this module's calls to `lib` (for example the debug build) inside
+    the block."""
+    global _lib
+    prev = load_library()
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = prev
 
 
 def _check(code: int):

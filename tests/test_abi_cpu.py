@@ -36,6 +36,17 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_debug_build_exports_the_same_abi(lib):
+    """The bounds-checking debug build is built beside the library and exports
+    the same functions (its checks run on the GPU: tests/test_gpu_debug.py)."""
+    dbg = kda.load_debug_library()
+    assert os.path.exists(build.debug_library_path())
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    assert dbg.kda_version() == lib.kda_version()
+    assert kda.STATUS_CODES["KDA_ERR_BOUNDS"] == -7
+
+
 def test_version(lib):
     assert lib.kda_version() >= 100
 
