@@ -31,13 +31,13 @@ struct FusedIO {
     const void *gate;      // [N, H, D] of T, or NULL
 };
 
-template <int D, typename T, int THREADS, bool MULTI, bool FUSED = false>
-__global__ void __launch_bounds__(THREADS)
-decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-              const float *__restrict__ g, const float *__restrict__ beta,
-              float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
-              int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status,
-              int ahead, Bounds bd, FusedIO fz = FusedIO{})
+template <int D, typename T, int THREADS, bool MULTI, bool FUSED>
+__device__ __forceinline__ void
+decode_body(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+            const float *__restrict__ g, const float *__restrict__ beta,
+            float *__restrict__ state, T *__restrict__ out, const int32_t *__restrict__ slots,
+            int H, int64_t pool, int m_arg, const int32_t *__restrict__ commit, int32_t *status,
+            int ahead, const Bounds &bd, const FusedIO &fz)
 {
     const int m = MULTI ? m_arg : 1;   // a compile-time single token for plain decode
     constexpr int C4 = D / 4;            // float4 groups per state row
@@ -226,6 +226,29 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     }
 }
 
+#define KDA_DECODE_PARAMS                                                                          \
+    const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,                      \
+        const float *__restrict__ g, const float *__restrict__ beta, float *__restrict__ state,      \
+        T *__restrict__ out, const int32_t *__restrict__ slots, int H, int64_t pool, int m_arg,      \
+        const int32_t *__restrict__ commit, int32_t *status, int ahead, Bounds bd
+template <int D, typename T, int THREADS, bool MULTI, bool FUSED = false>
+__global__ void __launch_bounds__(THREADS) decode_kernel(KDA_DECODE_PARAMS, FusedIO fz = FusedIO{})
+{
+    decode_body<D, T, THREADS, MULTI, FUSED>(q, k, v, g, beta, state, out, slots, H, pool, m_arg, commit, status,
+                                             ahead, bd, fz);
+}
+// The single-token step (plain and paged decode) at 80 registers, so that
+// three CTAs (192 KB of state loads in flight) share an SM instead of two: the
+// few words it spills cost less than the third CTA gains (workload 3: 170.7
+// against 172.7 us per step).
+template <int D, typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS, 3) decode_kernel_3cta(KDA_DECODE_PARAMS)
+{
+    decode_body<D, T, THREADS, false, false>(q, k, v, g, beta, state, out, slots, H, pool, m_arg, commit, status,
+                                             ahead, bd, FusedIO{});
+}
+#undef KDA_DECODE_PARAMS
+
 template <int D, typename T>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, float *state, void *out, int N, int H,
@@ -235,7 +258,11 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
     constexpr int THREADS = (D == 128) ? 256 : 128;
     const unsigned blocks = (unsigned)((size_t)N * H);
     const int ahead = (int)device_sm_count();
-    if (m == 1 && !commit)
+    if (m == 1 && !commit && D == 128)
+        decode_kernel_3cta<D, T, THREADS><<<blocks, THREADS, 0, st>>>(
+            (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr,
+            status, ahead, bd);
+    else if (m == 1 && !commit)
         decode_kernel<D, T, THREADS, false><<<blocks, THREADS, 0, st>>>(
             (const T *)q, (const T *)k, (const T *)v, g, beta, state, (T *)out, slots, H, pool, 1, nullptr,
             status, ahead, bd);
