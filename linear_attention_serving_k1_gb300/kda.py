@@ -54,12 +54,22 @@ _lib = None
 _vp = ctypes.c_void_p
 
 
+def default_library_path() -> str:
+    """libkda.so, or its bounds-checking debug build when the environment
+    variable KDA_LIBRARY is "debug" (every call of the binding then runs with
+    the index checks, and one that fails raises KDAError KDA_ERR_BOUNDS)."""
+    if os.environ.get("KDA_LIBRARY", "") == "debug":
+        return _build.debug_library_path()
+    return _build.library_path()
+
+
 def load_library(path: Optional[str] = None):
-    """Load libkda.so (raises if it has not been built)."""
+    """Load the library (default_library_path() unless `path` is given; raises
+    if it has not been built)."""
     global _lib
     if _lib is not None and path is None:
         return _lib
-    path = path or _build.library_path()
+    path = path or default_library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with linear_attention_serving_k1_gb300.build.build()")
     lib = ctypes.CDLL(path)
@@ -91,7 +101,7 @@ def load_library(path: Optional[str] = None):
     lib.kda_last_error.argtypes = []
     lib.kda_version.restype = ctypes.c_int32
     lib.kda_version.argtypes = []
-    if path == _build.library_path():
+    if path == default_library_path():
         _lib = lib
     return lib
 
