@@ -192,6 +192,12 @@ int32_t kda_prefill_launch_count(const kda_prefill_desc *desc);
  *
  *   q, k        [T, H, Dk]  dtype          (normalised inside, in fp32)
  *   v           [T, H, Dv]  dtype
+ *               The tensor-core path (bf16, Dk = Dv = 128) takes q, k, v and
+ *               the state as f16 tensor-core operands: every q and k row
+ *               needs an L2 norm below 65504, every v and state entry a
+ *               magnitude below 65504.  The debug build reports a q, k or v
+ *               beyond this as KDA_ERR_UNSUPPORTED (kda_prefill_status);
+ *               the release build does not check it.
  *   g           [T, H, Dk]  fp32  log-decay, alpha = exp(g) ([T, H] when
  *                                 desc->scalar_gate), g <= 0.  Per key
  *                                 channel, the decay of one chunk of 64
@@ -223,7 +229,8 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
  * queued on `stream`: KDA_OK, KDA_ERR_INVALID_ARG (malformed cu_seqlens, or a
  * sequence longer than max_seq_len; the affected sequences were skipped),
  * KDA_ERR_CKPT_OVERFLOW (snapshots beyond ckpt_capacity were dropped),
- * KDA_ERR_UNSUPPORTED (a chunk's decay exceeded the range stated for g) or
+ * KDA_ERR_UNSUPPORTED (a chunk's decay exceeded the range stated for g; in
+ * the debug build also q, k or v beyond the f16 range stated for them) or
  * KDA_ERR_TIMEOUT (a bounded device-side wait gave up).  The first condition
  * recorded during the call is the one reported.  Synchronises `stream`.
  */

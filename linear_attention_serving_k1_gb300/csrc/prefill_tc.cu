@@ -207,6 +207,7 @@ static_assert(K1_TBV + 8192 <= K1_TM && K1_XS + 2 * 16 * K1_XSP * 4 <= K1_MC && 
               "phase overlap");
 static_assert(2 * (K1_SMEM + 8192) <= 228 * 1024, "two CTAs per SM");
 constexpr int K1_THREADS = 256;
+constexpr float kF16Max = 65504.f;       // largest finite f16
 constexpr int kH32 = 32;                 // head count with its own K1 instance
 
 // TMEM columns (256 allocated)
@@ -467,6 +468,13 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
     uint32_t tm = 0;
     bool ok = true;
     bool strong = false;   // a decay factor of this thread's rows left the exact range
+    // (debug build) The f16 operand tiles hold q, k and v before
+    // normalisation: a q or k row of L2 norm 65504 or more (every element
+    // beyond the f16 range, and some within it), or a v element beyond it, is
+    // reported like a decay beyond range.  The release build leaves these
+    // checks out (they measured 0.4-0.9% of a call).
+    bool f16_over = false;
+    float vmax = 0.f;
     float sqa[8];      // the first half's squared row norms after the exchange across lane bit 4
 
     // 1-3. per channel half p: cumulative gates, decayed operands, partial row
@@ -560,6 +568,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 qgx[0][u] = qg.x; qgx[1][u] = qg.y;
                 kgx[0][u] = kg.x; kgx[1][u] = kg.y;
                 const float2 vf = up2(vv[j]);
+                if constexpr (kDebug) vmax = fmaxf(vmax, fmaxf(fabsf(vf.x), fabsf(vf.y)));
                 vx[0][u] = vf.x; vx[1][u] = vf.y;
                 kex[0][u] = ke.x; kex[1][u] = ke.y;
             }
@@ -628,6 +637,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
                 if ((lane & 1) == 0) {
                     const int i = lane >> 1, r = rb + (i & 7);
                     (i < 8 ? rq : rk)[r] = r < L ? rsqrtf(nsq + 1e-6f) : 0.f;
+                    if constexpr (kDebug) f16_over |= r < L && !(nsq < kF16Max * kF16Max);
                 }
             }
         };
@@ -648,7 +658,7 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
         finish_half();
         fence_async_smem();   // the f16 tiles are read by later products
     }
-    if (strong) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
+    if (strong || f16_over || !(vmax < kF16Max)) record_status(st, (int32_t)KDA_ERR_UNSUPPORTED);
     __syncthreads();   // rq, rk and the f16 tiles of both halves are written
     ok = ok && mbar_wait_bounded(&mbar, 1, wait_limit);   // G' complete: the Gram region may be reused
     fence_after_sync();

@@ -137,6 +137,43 @@ def test_decay_beyond_range_is_reported(dtype, D):
     assert torch.isfinite(o.float()).all() and torch.isfinite(f).all()
 
 
+@pytest.mark.parametrize("which,value", [("k", 1.0e5), ("q", -2.0e5), ("v", 7.0e4), ("k", 5.0e4)])
+def test_f16_operand_range_is_reported(which, value):
+    """The tensor-core path holds q, k and v in f16 operands before
+    normalisation: with the debug build, one element beyond the f16 range
+    (65504), or a q or k row whose norm reaches it (5e4 in two channels), is
+    reported as KDA_ERR_UNSUPPORTED (the release build leaves the check out). One element of 6e4 instead reports nothing: q and k
+    then match the oracle (they are normalised); v gives finite outputs (a
+    state holding entries near 3e4 beside entries near 1 is beyond what the
+    f16 state operand's 11 bits keep within the output bar)."""
+    w = workloads.custom_prefill(H=2, D=128, lens=[150], dtype="bf16", init="randn", seed=46)
+    inp = workloads.make_prefill(w)
+    desc = kda.make_desc(150, 2, 128, 1, kda.DTYPE_BF16)
+    ws = kda.alloc_workspace(desc, "cuda")
+    big = {n: inp[n].clone() for n in ("q", "k", "v")}
+    big[which][97, 1, 5] = value
+    if value < 6.5e4:
+        big[which][97, 1, 6] = value
+    d = gpu_inputs(inp)
+    with kda.using_library(kda.load_debug_library()):
+        kda.prefill(*(big[n].cuda() for n in ("q", "k", "v")), d["g"], d["beta"], d["init_state"], None,
+                    workspace=ws)
+        assert kda.prefill_status(ws) == kda.STATUS_CODES["KDA_ERR_UNSUPPORTED"]
+    # in range (one element at 6e4 leaves the row norm below the bound): no report
+    big[which][97, 1, 5] = 6.0e4 if which != "q" else -6.0e4
+    big[which][97, 1, 6] = inp[which][97, 1, 6]
+    with kda.using_library(kda.load_debug_library()):
+        o, f, _ = kda.prefill(*(big[n].cuda() for n in ("q", "k", "v")), d["g"], d["beta"], d["init_state"], None,
+                              workspace=ws)
+        assert kda.prefill_status(ws) == kda.KDA_OK
+    if which == "v":
+        assert torch.isfinite(o.float()).all() and torch.isfinite(f).all()
+        return
+    o_r, f_r, _ = oracle.prefill(big["q"], big["k"], big["v"], inp["g"], inp["beta"], inp["init_state"], None)
+    assert out_err(to_np(o), o_r) <= TOL_OUT_BF16
+    assert state_err(to_np(f), f_r) <= TOL_STATE
+
+
 @pytest.mark.parametrize("seg", [0, 2])
 def test_bounded_wait_gives_up_cleanly(seg):
     """With a wait limit of one poll, the tensor-core kernels' waits give up:
