@@ -1053,8 +1053,8 @@ k1_tc_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 
 //   rows [16 qd, 16 qd + 16) of column e; one thread of a 17th warp issues the
 //   MMAs and one of an 18th the record copies into a 2-stage ring.
 // Per chunk one product [A' S | Q' S]^T (N = 192: the record keeps the A'
-// and Q' tiles adjacent) accumulates over two K-halves of d', each issued once
-// the state threads owning those rows of S^T have written them.  S^T, the
+// and Q' tiles adjacent) accumulates over the eight K steps of d', issued in
+// one run once the state threads have written all of S^T.  S^T, the
 // product's A operand, lives in TMEM (f16, row e in lane e): the state threads
 // hand it on with tcgen05.st instead of shared-memory stores and a proxy
 // fence, and the tensor core reads only the B operand from shared memory.
@@ -1100,7 +1100,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
 {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t full[K2_STAGES], fullr[K2_STAGES], empty[K2_STAGES], emptyr[K2_STAGES], gfull[kGamSlots],
-        sdone, pread[2], sready[2], dbar;
+        sdone, pread[2], sready, dbar;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_flag;
 
@@ -1121,7 +1121,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
         mbar_init(&sdone, 1);
         mbar_init(&dbar, 1);
         for (int j = 0; j < 2; ++j) mbar_init(&pread[j], K2_STATE_THREADS);   // per accumulator buffer
-        for (int j = 0; j < 2; ++j) mbar_init(&sready[j], K2_STATE_THREADS / 2);
+        mbar_init(&sready, K2_STATE_THREADS);   // S^T of the next chunk written
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -1234,7 +1234,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
             // as their part of the record has landed and the buffer's previous
             // contents (chunk cc - 2) were read, so they run while the state
             // threads still work on chunk cc - 1; the K = d' steps (A = S^T)
-            // follow half by half as the state threads write S^T.
+            // follow once the state threads have written S^T.
             auto issue_rpart = [&](int cc) -> bool {
                 const int s = cc % K2_STAGES;
                 const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
@@ -1255,17 +1255,16 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 const uint32_t stg = smem_u32(sm + s * REC_BYTES), acc = tm + T2_P + 256 * (cc & 1);
                 const uint32_t sop = tm + T2_S;   // S^T in TMEM: a K step of 16 is 8 columns
                 const uint32_t idesc = idesc_f16(128, 192);
+                // all of S^T, then the eight steps in one run: issuing them half by
+                // half as each half of S^T arrived measured 0.5-0.9% slower, and by
+                // quarters 2-6% slower (a wait between MMA issues costs more than
+                // the earlier start gains)
                 if (!wait_or_abort(&full[s], (cc / K2_STAGES) & 1, abort_v, wait_limit) ||
-                    !wait_or_abort(&sready[0], cc & 1, abort_v, wait_limit))
+                    !wait_or_abort(&sready, cc & 1, abort_v, wait_limit))
                     return false;
                 fence_after_sync();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ts(acc, sop + 8 * ks, make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
-                if (!wait_or_abort(&sready[1], cc & 1, abort_v, wait_limit)) return false;
-                fence_after_sync();
-#pragma unroll
-                for (int ks = 4; ks < 8; ++ks)
+                for (int ks = 0; ks < 8; ++ks)
                     mma_f16_ts(acc, sop + 8 * ks, make_desc(stg + REC_AP + ks * 256, LBO_KIN, SBO_K128), idesc, 1);
                 mma_commit(&sdone);
                 mma_commit(&empty[s]);
@@ -1290,7 +1289,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
             const uint32_t s_taddr = tm + lane_base + T2_S + 16 * qd;   // this thread's part of S^T
             write_state_tmem(s_taddr, S);
             fence_before_sync();
-            mbar_arrive(&sready[qd >> 1]);
+            mbar_arrive(&sready);
             for (int c = 0; c < nch && alive; ++c) {
                 const int cc = base + c;
                 // kGate: this chunk's gate values for the thread's output rows
@@ -1341,7 +1340,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 if (c + 1 < nch) {   // the next chunk's S^T (none after the chain's last chunk)
                     write_state_tmem(s_taddr, S);
                     fence_before_sync();
-                    mbar_arrive(&sready[qd >> 1]);
+                    mbar_arrive(&sready);
                 }
                 // output rows [16 qd, 16 qd + 16) of column e, rounded to bf16
                 uint32_t ob16[8];
