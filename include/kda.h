@@ -258,8 +258,13 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
  * Arguments are those of kda_prefill minus the workspace.  The scratch is a
  * fixed device array of KDA_NOALLOC_SCRATCH_BYTES built into the library:
  * every GPU that loads the library keeps it resident until the process exits.
- * A call whose kda_prefill_workspace_size() exceeds it returns
- * KDA_ERR_UNSUPPORTED before any work is queued.  The need is about 90.6 KB
+ * When the automatic plan (desc->segment_chunks 0) of the tensor-core path
+ * needs more than the array, the call takes the longest segments that fit:
+ * one segment if every record fits, else the largest segment_chunks whose
+ * ring and carry fit (the results are the same for every segment length).
+ * A call that fits no plan returns KDA_ERR_UNSUPPORTED before any work is
+ * queued, as does one with an explicit segment_chunks whose
+ * kda_prefill_workspace_size() exceeds the array.  The need is about 90.6 KB
  * per chunk of 64 tokens and head for the bf16 path with Dk = Dv = 128 in
  * one segment (so about 360 chunk-heads, e.g. 11 chunks of 32 heads); a
  * smaller desc->segment_chunks bounds it by two ring slots of that many

@@ -20,6 +20,8 @@
 // per-call sequence table and handoff are fully rewritten.  Calls whose work
 // can overlap on the GPU (different streams, different host threads) race on
 // the array: they must be ordered by the caller.
+#include <stdint.h>
+
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -32,6 +34,44 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_lock;
 void *g_scratch_ptr[kMaxDevices];
+
+// Workspace bytes of `d` with segment_chunks = G (SIZE_MAX if the descriptor
+// is then refused).
+size_t bytes_with_segments(kda_prefill_desc d, int64_t G)
+{
+    d.segment_chunks = (int32_t)G;
+    size_t b = 0;
+    return kda::prefill_workspace_bytes(&d, &b) == KDA_OK ? b : SIZE_MAX;
+}
+
+// The automatic segment plan of the tensor-core path may need more than the
+// array while a plan of shorter segments fits; the results are the same for
+// every segment length, so `d` takes the longest segments that fit: one
+// segment when all records fit, else the largest G whose two ring slots and
+// fp32 carry fit (their bytes grow with G below the sequence's chunk count).
+// Returns the bytes of the plan chosen (of the automatic one if none fits).
+size_t fit_segments(kda_prefill_desc *d, size_t need)
+{
+    if (need <= kScratchBytes || d->segment_chunks != 0 || !kda::use_tc_path(d->dtype, d->head_dim_k, d->chunk))
+        return need;
+    const int64_t T = d->total_tokens;
+    const int64_t len = d->max_seq_len > 0 && d->max_seq_len < T ? d->max_seq_len : T;
+    const int64_t maxc = (len + d->chunk - 1) / d->chunk;
+    if (maxc <= 1 || maxc > INT32_MAX) return need;
+    if (bytes_with_segments(*d, maxc) <= kScratchBytes) {
+        d->segment_chunks = (int32_t)maxc;
+        return bytes_with_segments(*d, maxc);
+    }
+    int64_t lo = 0, hi = maxc - 1;   // largest G in [1, maxc - 1] that fits, 0 if none
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) / 2;
+        if (bytes_with_segments(*d, mid) <= kScratchBytes) lo = mid;
+        else hi = mid - 1;
+    }
+    if (lo < 1) return need;
+    d->segment_chunks = (int32_t)lo;
+    return bytes_with_segments(*d, lo);
+}
 
 // Device address of g_noalloc_scratch on the current device, looked up once.
 cudaError_t scratch_address(void **out)
@@ -62,6 +102,8 @@ extern "C" kda_status kda_prefill_noalloc(const void *q, const void *k, const vo
     size_t need = 0;
     const kda_status ds = kda::prefill_workspace_bytes(desc, &need);   // sets the message on error
     if (ds != KDA_OK) return ds;
+    kda_prefill_desc d = *desc;
+    need = fit_segments(&d, need);
     if (need > kScratchBytes) {
         return kda::fail_with_message(KDA_ERR_UNSUPPORTED,
                                       "kda_prefill_noalloc: this call needs %zu bytes of scratch, more than the "
@@ -73,6 +115,6 @@ extern "C" kda_status kda_prefill_noalloc(const void *q, const void *k, const vo
     if (e != cudaSuccess)
         return kda::fail_with_message(KDA_ERR_CUDA, "kda_prefill_noalloc: scratch address: %s",
                                       cudaGetErrorString(e));
-    return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, desc,
+    return kda::prefill_call(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, ckpts, &d,
                              scratch, kScratchBytes, stream, false);
 }

@@ -65,7 +65,34 @@ def test_noalloc_segmented_is_bit_identical(segment_chunks):
         assert torch.equal(ck, ck_ref)
 
 
+def test_noalloc_takes_shorter_segments_when_the_automatic_plan_does_not_fit():
+    """One sequence of 2,048 tokens at 32 heads: the automatic plan (one
+    segment, every record) needs about 96 MB, more than the built-in array,
+    while segments of 5 chunks fit; the call takes the longest segments that
+    fit and matches kda_prefill bit for bit (results do not depend on the
+    segment length)."""
+    w = workloads.custom_prefill(H=32, D=128, lens=[2048], dtype="bf16", init="randn", ckpt_stride=512, seed=35,
+                                 varlen=True)
+    d = gpu_inputs(workloads.make_prefill(w))
+    cap = kda.num_checkpoints(w.lens, 512)
+    desc = kda.make_desc(2048, 32, 128, 1, kda.DTYPE_BF16, 64, 512, cap)
+    assert kda.workspace_size(desc) > kda.NOALLOC_SCRATCH_BYTES
+    fit = kda.make_desc(2048, 32, 128, 1, kda.DTYPE_BF16, 64, 512, cap, segment_chunks=5)
+    assert kda.workspace_size(fit) <= kda.NOALLOC_SCRATCH_BYTES
+    o_ref, f_ref, ck_ref = kda.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                       d["cu_seqlens"], ckpt_stride=512, ckpt_capacity=cap)
+    o, f, ck = kda.prefill_noalloc(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], d["cu_seqlens"],
+                                   ckpt_stride=512, ckpt_capacity=cap)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref)
+    assert torch.equal(f, f_ref)
+    assert torch.equal(ck, ck_ref)
+
+
 def test_noalloc_rejects_calls_beyond_its_scratch():
+    """About 1M tokens of one sequence at 32 heads fit no plan: every segment
+    length is raised to at least 65 chunks (256 segments at most), and two ring
+    slots of 65 chunks of 32 heads already need about 377 MB."""
     lib = kda.load_library()
     T = 1 << 20   # about 1M tokens x 32 heads needs far more than the built-in array
     desc = kda.make_desc(T, 32, 128, 1, kda.DTYPE_BF16)
