@@ -103,6 +103,24 @@ def test_segmented_workspace_is_bounded(lib):
         assert n < 2 * Ge * 32 * record_bytes + 32 * 128 * 128 * 4 + 8192
 
 
+def test_workspace_grows_with_segment_length(lib):
+    """kda_prefill_noalloc's fallback searches for the longest segments that
+    fit its array by bisection: below a sequence's chunk count the workspace
+    must not shrink as segment_chunks grows. Checked over batch shapes of the
+    tensor-core path, with and without a max_seq_len bound."""
+    for T, N, H, L in ((2048, 1, 32, 0), (8192, 4, 8, 0), (70000, 16, 4, 8192), (131072, 1, 2, 0)):
+        maxc = -(-(L or T) // 64)
+        prev = 0
+        for G in sorted({1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, maxc // 2, maxc - 1}):
+            if not 1 <= G < maxc:
+                continue
+            d = _desc(T=T, num_seqs=N, H=H, D=128, dtype_code=kda.DTYPE_BF16, max_seq_len=L, segment_chunks=G)
+            n = lib.kda_prefill_workspace_size(ctypes.byref(d))
+            assert n > 0 and n >= prev, (T, N, H, G, n, prev)
+            prev = n
+            assert lib.kda_prefill_launch_count(ctypes.byref(d)) <= 1 + 2 * 256
+
+
 def test_launch_count(lib):
     """Three launches without segments (table, K1, K2); 1 + 2 x segments with."""
     assert lib.kda_prefill_launch_count(ctypes.byref(_desc())) == 3
