@@ -1256,7 +1256,7 @@ k2_tc_kernel(StateIO io, int N, int H, SeqTable tab,
                 const uint32_t sop = tm + T2_S;   // S^T in TMEM: a K step of 16 is 8 columns
                 const uint32_t idesc = idesc_f16(128, 192);
                 // all of S^T, then the eight steps in one run: issuing them half by
-                // half as each half of S^T arrived measured 0.5-0.9% slower, and by
+                // half as each half of S^T arrived measured 0.5-1.4% slower, and by
                 // quarters 2-6% slower (a wait between MMA issues costs more than
                 // the earlier start gains)
                 if (!wait_or_abort(&full[s], (cc / K2_STAGES) & 1, abort_v, wait_limit) ||
