@@ -69,12 +69,20 @@ def test_workspace_size(lib):
     assert bigger > n
 
 
-@pytest.mark.parametrize("kw,code", [
+INVALID_DESCS = [
     (dict(D=96), -2), (dict(chunk=32), -2), (dict(num_seqs=0), -1), (dict(T=-1), -1),
     (dict(H=0), -1), (dict(dtype_code=7), -1), (dict(ckpt_stride=100), -1),
     (dict(max_seq_len=-1), -1), (dict(segment_chunks=-2), -1), (dict(raw_scalar_gate=2), -1),
-])
-def test_invalid_desc(lib, kw, code):
+]
+
+
+@pytest.mark.parametrize("build_kind", ["release", "debug"])
+@pytest.mark.parametrize("kw,code", INVALID_DESCS)
+def test_invalid_desc(lib, build_kind, kw, code):
+    """Refused on the host before anything is launched, the same way by the
+    library and by its debug build."""
+    if build_kind == "debug":
+        lib = kda.load_debug_library()
     d = _desc(**kw)
     assert lib.kda_prefill_workspace_size(ctypes.byref(d)) == 0
     rc = lib.kda_prefill(*([ctypes.c_void_p(16)] * 7), ctypes.c_void_p(16), None, None,
